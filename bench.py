@@ -1,0 +1,424 @@
+"""Benchmark of one paged-attention layer-step on GB300.
+
+A step is one pass of the whole hot path over one batch: the cache write of
+the step's new tokens (kv_write), paged attention (paged_attn) and the
+split merge (paged_attn_combine), on inputs already resident in HBM.
+
+Default workload: the LLaMA-13B-shaped decode batch (256 requests, 40 q = 40
+kv heads, head size 128, lognormal lengths around 800 tokens, 100000-block
+cache, about 4.1 GB of KV read per step).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of
+the batch (independent requests, weak scaling); no collective touches the
+data path, only the barrier and the max of the ranks' times.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "decode paged-attn achieved HBM GB/s (% of peak), tokens/s per layer-step"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(step: wl.Step) -> dict:
+    """Bytes the method must move per step (each byte once), by phase.
+
+    attention: K and V of every key each request sees (a physical block
+    shared by several requests counts once), Q in, out, the table entries
+    read and the per-request lengths.  kv_write: new K/V read and written,
+    and slot numbers.
+    """
+    H, Hkv, d, B = step.num_q_heads, step.num_kv_heads, step.head_size, step.block_size
+    T, S = step.num_tokens, step.num_seqs
+    per_token_kv = 2 * Hkv * d * 2
+    # unique (block, used tokens): a shared block is read once
+    used = {}
+    for r in range(S):
+        L = int(step.seq_lens[r])
+        nb = (L + B - 1) // B
+        for i, b in enumerate(step.block_tables[r, :nb].tolist()):
+            n = min(B, L - i * B)
+            used[b] = max(used.get(b, 0), n)
+    kv_unique = sum(used.values()) * per_token_kv
+    kv_logical = int(step.seq_lens.long().sum()) * per_token_kv
+    tables = sum((int(l) + B - 1) // B for l in step.seq_lens.tolist()) * 4
+    attn = kv_unique + 2 * T * H * d * 2 + tables + 4 * S + 4 * (S + 1)
+    kvw = 2 * (T * per_token_kv) + 8 * T
+    return {"attention": attn, "kv_write": kvw, "kv_unique": kv_unique, "kv_logical": kv_logical,
+            "step": attn + kvw}
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json, burst copy)"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank: int, world: int) -> dict:
+    import paged_kv_cache_111_gb300 as pkv
+    from paged_kv_cache_111_gb300 import _build
+    _build.build()
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    step = wl.make_workload(args.workload, seed=wl.seed_of(args.workload) + 1000 * rank)
+    T, H, d = step.num_tokens, step.num_q_heads, step.head_size
+    to = {f: getattr(step, f).to(dev).contiguous() for f in
+          ("seq_lens", "query_start_loc", "block_tables", "query", "key", "value", "slot_mapping")}
+    pool = wl.make_poisoned_pool_like(step, device=dev)
+    hk, hv, hs = step.hist_key, step.hist_value, step.hist_slot_mapping
+    chunk = 1 << 16
+    for a in range(0, hs.numel(), chunk):
+        b = min(hs.numel(), a + chunk)
+        pkv.kv_write(pool, hk[a:b].to(dev), hv[a:b].to(dev), hs[a:b].to(dev))
+    del hk, hv
+    ws_bytes = pkv.paged_attn_workspace_size(step.num_seqs, T, step.max_query_len, step.max_seq_len, H,
+                                             step.num_kv_heads, d)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    maxq, maxs = step.max_query_len, step.max_seq_len
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.kv_write(pool, to["key"], to["value"], to["slot_mapping"])
+        if ev is not None:
+            ev[1].record(stream)
+        pkv.paged_attn(out, to["query"], pool, to["block_tables"], to["seq_lens"], to["query_start_loc"],
+                       maxq, maxs, step.scale, ws)
+        if ev is not None:
+            ev[2].record(stream)
+        pkv.paged_attn_combine(out, ws)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(dev)
+    status = pkv.workspace_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {pkv.STATUS_NAMES.get(status, status)}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            one_step(events[i])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    kvw_ms = sum(e[0].elapsed_time(e[1]) for e in events) / args.steps
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in events) / args.steps
+    comb_ms = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps
+    status = pkv.workspace_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {pkv.STATUS_NAMES.get(status, status)}")
+
+    # ---- end to end through the public API with host buffers ----------------
+    host_in = {f: getattr(step, f).contiguous().pin_memory() for f in
+               ("seq_lens", "query_start_loc", "block_tables", "query", "key", "value", "slot_mapping")}
+    host_out = torch.empty(T, H, d, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    dev_in = {f: torch.empty_like(t, device=dev) for f, t in host_in.items()}
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        for f, t in host_in.items():
+            dev_in[f].copy_(t, non_blocking=True)
+        pkv.kv_write(pool, dev_in["key"], dev_in["value"], dev_in["slot_mapping"])
+        pkv.paged_attn(out, dev_in["query"], pool, dev_in["block_tables"], dev_in["seq_lens"],
+                       dev_in["query_start_loc"], maxq, maxs, step.scale, ws)
+        pkv.paged_attn_combine(out, ws)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # ---- same-run copy probe (device-to-device copy, read + write bytes) ------
+    probe_gbs = None
+    if args.copy_probe:
+        n = 1 << 30
+        a = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        b = torch.empty_like(a)
+        a.fill_(1.0)
+        best = math.inf
+        for _ in range(10):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            b.copy_(a)
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            best = min(best, s0.elapsed_time(s1))
+        probe_gbs = 2 * n * 2 / (best * 1e-3) / 1e9
+        del a, b
+
+    return {"step": step, "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
+            "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "probe_gbs": probe_gbs}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(step: wl.Step, n_req: int, seed: int) -> wl.Step:
+    g = torch.Generator().manual_seed(seed)
+    idx = torch.randperm(step.num_seqs, generator=g)[:max(1, min(n_req, step.num_seqs))]
+    return step.subset(sorted(idx.tolist()))
+
+
+def time_oracle_step(sub: wl.Step):
+    """One oracle step on ``sub``: cache write of the new tokens + attention.
+    Returns (seconds, algorithmic bytes of the sample, threads)."""
+    import oracle
+    cache = oracle.new_cache(sub.num_blocks, sub.num_kv_heads, sub.head_size)
+    oracle.kv_write(cache, sub.hist_key, sub.hist_value, sub.hist_slot_mapping)
+    t0 = time.perf_counter()
+    oracle.kv_write(cache, sub.key, sub.value, sub.slot_mapping)
+    oracle.paged_attn(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
+                      sub.num_q_heads, sub.scale)
+    dt = time.perf_counter() - t0
+    return dt, algorithmic_bytes(sub)["step"], oracle.max_threads()
+
+
+def cpu_baseline(step: wl.Step, budget_s: float = 10.0) -> dict:
+    import oracle
+    oracle.build()
+    n_req = max(1, step.num_seqs // 4)
+    sub = oracle_sample(step, n_req, 7)
+    times, nbytes, threads = [], 0, 1
+    t_end = time.perf_counter() + budget_s
+    while len(times) < 3 or time.perf_counter() < t_end:
+        dt, nbytes, threads = time_oracle_step(sub)
+        times.append(dt)
+        if len(times) >= 50:
+            break
+    mean = sum(times) / len(times)
+    return {"value": nbytes / mean / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{sub.num_seqs} of {step.num_seqs} requests ({sub.num_tokens} query tokens), "
+                      f"{len(times)} timed oracle steps (cache write + attention), mean {mean * 1e3:.1f} ms",
+            "tokens_per_s": sub.num_tokens / mean}
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    step = wl.make_workload(args.workload)
+    # size one step's sample so that warmup + steps finish in about two minutes
+    probe = oracle_sample(step, 4, 11)
+    dt, _, _ = time_oracle_step(probe)
+    per_req = max(dt / probe.num_seqs, 1e-4)
+    budget_step = 120.0 / max(1, args.steps + args.warmup)
+    n_req = int(max(1, min(step.num_seqs, budget_step / per_req)))
+    samples = [oracle_sample(step, n_req, 100 + i) for i in range(min(4, args.steps + args.warmup))]
+    for i in range(args.warmup):
+        time_oracle_step(samples[i % len(samples)])
+    tot_t, tot_b, tot_tok, threads = 0.0, 0, 0, 1
+    for i in range(args.steps):
+        s = samples[i % len(samples)]
+        dt, nb, threads = time_oracle_step(s)
+        tot_t += dt
+        tot_b += nb
+        tot_tok += s.num_tokens
+    value = tot_b / tot_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "sample_requests_per_step": n_req},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_req} of {step.num_seqs} requests per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "tokens_per_s": tot_tok / tot_t,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="llama13b-decode", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-copy-probe", dest="copy_probe", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ["LOCAL_RANK"])))
+    r = run_gpu(args, rank, world)
+    step = r["step"]
+    ab = algorithmic_bytes(step)
+    ms_per_step = r["total_ms"] / args.steps
+    if world > 1:
+        t = torch.tensor([ms_per_step, r["attn_ms"], r["e2e_ms"]], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step, attn_max, e2e_max = (float(x) for x in t.tolist())
+    else:
+        attn_max, e2e_max = r["attn_ms"], r["e2e_ms"]
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    pk = peaks()
+    value = world * ab["step"] / (ms_per_step * 1e-3) / 1e9
+    attn_gbs = ab["attention"] / (r["attn_ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "num_seqs": step.num_seqs, "num_tokens": step.num_tokens,
+            "num_q_heads": step.num_q_heads, "num_kv_heads": step.num_kv_heads, "head_size": step.head_size,
+            "block_size": step.block_size, "num_blocks": step.num_blocks,
+            "kv_bytes_per_step": ab["kv_unique"], "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (KV read per step above 129 MB), no flush"
+            if ab["kv_unique"] > 129e6 else "inputs fit in L2; no flush (small workload)",
+        },
+        "pct_of_peak": value / pk["hbm_gbs"],
+        "tokens_per_s": world * step.num_tokens / (ms_per_step * 1e-3),
+        "us_per_step": {"kv_write": r["kvw_ms"] * 1e3, "paged_attn": r["attn_ms"] * 1e3,
+                        "combine": r["comb_ms"] * 1e3, "total": ms_per_step * 1e3},
+        "roofline": {"bound": "hbm", "kernel": "paged_attn (plan + decode kernels)",
+                     "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": attn_gbs / pk["hbm_gbs"], "peak_source": pk["source"],
+                     "algorithmic_bytes_per_launch": ab["attention"], "traffic": None},
+        "copy_probe_gbs": r["probe_gbs"],
+        "e2e": {"value": world * ab["step"] / (e2e_max * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": e2e_max},
+        "gpu_launches": 4 * args.steps,
+        "clocks": r["clocks"],
+    }
+    if ab["kv_logical"] != ab["kv_unique"]:
+        line["logical_kv_gbs_incl_l2_reuse"] = ab["kv_logical"] / (r["attn_ms"] * 1e-3) / 1e9
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(step)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

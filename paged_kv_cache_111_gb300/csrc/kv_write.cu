@@ -1,0 +1,101 @@
+// Cache write ("reshape_and_cache"): scatter new K/V tokens into their slots.
+//
+// "vLLM internals: managing the KV cache like an OS manages memory", section
+// 2.1 (the fused write op puts each new token's K/V into its physical block);
+// "continuous batching and PagedAttention" tutorial, section 3.3 (token ->
+// block slot / 16, offset slot % 16); "vLLM source reading", section 5.1
+// (slot_mapping drives the scatter).
+//
+// A pure bit copy, HBM-bound: each thread moves one 16-byte vector of one
+// token's K or V row; consecutive threads cover consecutive 16-byte pieces of
+// a head's row, so reads and writes are coalesced 128-byte+ runs.
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+struct KvWriteParams {
+    uint4 *cache;            // viewed as 16-byte vectors
+    int64_t num_slots;       // num_blocks * 16
+    const uint4 *key;
+    const uint4 *value;
+    int64_t key_stride_v;    // token stride in 16-byte vectors
+    int64_t value_stride_v;
+    const int64_t *slots;
+    int32_t num_tokens;
+    int32_t num_kv_heads;
+    int32_t vec_shift;       // log2(head_size / 8)
+    int32_t *status;
+};
+
+// One token per CTA iteration; the CTA's threads cover that token's K and V
+// rows of every kv head, 16 bytes each.
+__global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
+    const int vpr = 1 << p.vec_shift;                      // vectors per head row
+    const int per_kv = p.num_kv_heads * vpr;               // vectors of K (or V) per token
+    const int per_tok = 2 * per_kv;
+    for (int64_t t = blockIdx.x; t < p.num_tokens; t += gridDim.x) {
+        const int64_t slot = __ldg(p.slots + t);
+        if (slot < 0) continue;                             // padding token
+        if (slot >= p.num_slots) {
+            if (threadIdx.x == 0) set_status(p.status, PKV_ERR_DEVICE_INDEX);
+            continue;
+        }
+        const int64_t blk = slot / kBlock;
+        const int64_t off = slot - blk * kBlock;
+        const uint4 *ksrc = p.key + t * p.key_stride_v;
+        const uint4 *vsrc = p.value + t * p.value_stride_v;
+        for (int v = threadIdx.x; v < per_tok; v += blockDim.x) {
+            const int which = v >= per_kv;                  // 0 = K, 1 = V
+            const int rr = v - which * per_kv;
+            const int h = rr >> p.vec_shift;
+            const int c = rr & (vpr - 1);
+            const uint4 val = __ldg((which ? vsrc : ksrc) + rr);
+            const int64_t dst = (((blk * p.num_kv_heads + h) * 2 + which) * kBlock + off) * vpr + c;
+            p.cache[dst] = val;
+        }
+    }
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_kv_write(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads, int32_t head_size,
+                            int32_t block_size, const void *key, int64_t key_token_stride, const void *value,
+                            int64_t value_token_stride, const int64_t *slot_mapping, int32_t num_tokens,
+                            int32_t *device_status, void *stream) {
+    using namespace pkv;
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_SHAPE;
+    if (block_size != kBlock || (head_size != 64 && head_size != 128)) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!kv_cache || !key || !value || !slot_mapping) return PKV_ERR_NULL;
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_size;
+    if (key_token_stride < row || value_token_stride < row) return PKV_ERR_SHAPE;
+    if ((key_token_stride % 8) || (value_token_stride % 8)) return PKV_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(kv_cache) | reinterpret_cast<uintptr_t>(key) |
+         reinterpret_cast<uintptr_t>(value)) & 15u)
+        return PKV_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) return PKV_ERR_ALIGNMENT;
+    if (num_blocks > (INT64_MAX / kBlock)) return PKV_ERR_SHAPE;
+
+    KvWriteParams p;
+    p.cache = static_cast<uint4 *>(kv_cache);
+    p.num_slots = num_blocks * kBlock;
+    p.key = static_cast<const uint4 *>(key);
+    p.value = static_cast<const uint4 *>(value);
+    p.key_stride_v = key_token_stride / 8;
+    p.value_stride_v = value_token_stride / 8;
+    p.slots = slot_mapping;
+    p.num_tokens = num_tokens;
+    p.num_kv_heads = num_kv_heads;
+    p.vec_shift = head_size == 128 ? 4 : 3;
+    p.status = device_status;
+
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const int threads = 256;
+    int64_t blocks = num_tokens;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;      // 8 resident 256-thread CTAs per SM
+    if (blocks > cap) blocks = cap;
+    kv_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

@@ -1,0 +1,824 @@
+// Paged attention over a block-table-indexed KV cache, and its split-K merge.
+//
+// What is computed ("continuous batching and PagedAttention" tutorial,
+// section 3.6 "PagedAttention kernel"; "vLLM source reading", sections 2.3
+// and 5.1): every query row loops over its request's logical blocks, looks
+// up the physical block in the block table, loads that block's K and V and
+// folds softmax(scale * q.K^T) V into a running (max, sum, accumulator) state.
+// Each request only sees its own tokens ("Inside vLLM: Anatomy of a
+// High-Throughput LLM Inference System", "Executing the forward pass").
+//
+// How it runs on sm_103a (three kernels, enqueued by two calls):
+//  1. plan_kernel (one CTA) reads seq_lens / query_start_loc, checks them,
+//     and lists work chunks in the workspace, largest first.  A request whose
+//     query rows for one kv head fit one 16-row tile (q_r * G <= 16: decode,
+//     and short speculative-verify queries) has its keys split into up to 32
+//     ranges of whole pages (split-K flash-decoding); a longer request is cut
+//     into 16-row tiles that each stream every key they may see.
+//  2. decode_kernel: persistent CTAs of NW warps.  Each warp takes chunks
+//     (x kv heads) in a fixed order and streams the chunk's 16-token pages
+//     through its own ring of DEPTH shared-memory stages.  A page of one kv
+//     head (K then V, 2*16*head_size bf16, contiguous in the cache) arrives by
+//     TMA tensor loads with 128-byte swizzle, so ldmatrix reads are free of
+//     bank conflicts.  S = Q K^T and O += P V run on bf16 mma.sync tiles:
+//     rows are the tile's (query token, q head of the group) pairs, so every
+//     q head of a GQA group is served by one read of each KV page.
+//  3. combine_kernel (second call): log-sum-exp merge of split rows.
+//
+// Masking never multiplies by zero: scores of keys a row may not see are
+// replaced by -inf before the exponent, and V rows past the sequence end in
+// its last page are zeroed in shared memory before P V, so NaN in unwritten
+// cache slots cannot reach an output.
+#include <mutex>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+constexpr int kMaxSplits = 32;      // key ranges per split row, at most
+constexpr int kPlanThreads = 1024;
+constexpr int kSizeBins = 256;      // counting-sort bins for chunk sizes (pages)
+constexpr int32_t kMagic = 0x504B5631;   // "PKV1"
+
+// ---- workspace layout ---------------------------------------------------------
+
+struct WsHeader {
+    int32_t status;          // device status word (first 4 bytes)
+    int32_t magic;
+    int32_t n_chunks;
+    int32_t num_tokens;
+    int32_t num_q_heads;
+    int32_t head_size;
+    int32_t num_seqs;
+    int32_t pages_per_split;
+    int64_t off_req;         // int2 [num_seqs]: {splits, partial row base}
+    int64_t off_tok;         // int2 [num_tokens]: {request, index in request} (-1 if none)
+    int64_t off_chunks;      // int4 [max_chunks]: {request, split or tile, page begin, page end}
+    int64_t off_part_lse;    // float [max_prow]
+    int64_t off_part_o;      // float [max_prow][head_size]
+    int64_t max_chunks;
+    int64_t max_prow;
+    int64_t prow_used;
+};
+static_assert(sizeof(WsHeader) <= 256, "header must fit its 256-byte slot");
+
+struct WsLayout {
+    int64_t off_req, off_tok, off_chunks, off_part_lse, off_part_o, total;
+    int64_t max_chunks, max_prow;
+};
+
+static inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_query_len, int64_t max_seq_len,
+                          int64_t num_q_heads, int64_t num_kv_heads, int64_t head_size) {
+    const int64_t G = num_q_heads / num_kv_heads;
+    WsLayout w;
+    // split rows: requests with q_r * G <= 16, so q_r <= 16 / G
+    const int64_t q_split = G <= 16 ? 16 / G : 0;
+    int64_t split_tokens = num_seqs * q_split;
+    if (split_tokens > num_tokens) split_tokens = num_tokens;
+    const int64_t max_pages = (max_seq_len + kBlock - 1) / kBlock;
+    const int64_t splits = max_pages < kMaxSplits ? (max_pages > 0 ? max_pages : 1) : kMaxSplits;
+    w.max_prow = split_tokens * num_q_heads * splits;
+    (void)max_query_len;
+    // chunks: split requests give <= splits each; tiled ones ceil(q_r G / 16) <= q_r G / 16 + 1
+    w.max_chunks = num_seqs * splits + (num_tokens * G + 15) / 16 + num_seqs;
+    int64_t off = 256;
+    w.off_req = off;
+    off = align256(off + 8 * num_seqs);
+    w.off_tok = off;
+    off = align256(off + 8 * num_tokens);
+    w.off_chunks = off;
+    off = align256(off + 16 * w.max_chunks);
+    w.off_part_lse = off;
+    off = align256(off + 4 * w.max_prow);
+    w.off_part_o = off;
+    off = align256(off + 4 * w.max_prow * head_size);
+    w.total = off;
+    return w;
+}
+
+// ---- kernel parameters ----------------------------------------------------------
+
+struct PlanParams {
+    uint8_t *ws;
+    const int32_t *seq_lens;
+    const int32_t *qsl;
+    int32_t num_seqs, num_tokens, num_q_heads, num_kv_heads, head_size;
+    int32_t max_blocks_per_seq, max_query_len, max_seq_len;
+    int32_t num_splits;       // 0 = auto
+    int32_t total_warps;      // warps of the decode grid (for the automatic split size)
+    WsLayout lay;
+};
+
+struct AttnParams {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *query;
+    int64_t q_stride;         // elements per token
+    const int32_t *block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t *seq_lens;
+    const int32_t *qsl;
+    int32_t num_q_heads, num_kv_heads, G;
+    int64_t num_blocks;
+    float scale_log2;         // scale * log2(e)
+    uint8_t *ws;
+};
+
+// ---- 1. planning ------------------------------------------------------------------
+
+__device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
+
+// Work of request r: number of chunks, and whether its rows are split along keys.
+struct ReqPlan {
+    int valid;        // metadata consistent
+    int rows;         // q_r * G
+    int split;        // 1: split-K over key pages; 0: 16-row tiles
+    int n_chunks;
+    int pages;        // key pages of the request (split mode)
+    int per_split;    // pages per split (split mode)
+};
+
+__device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split) {
+    ReqPlan rp{0, 0, 0, 0, 0, 0};
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const int q0 = p.qsl[r], q1 = p.qsl[r + 1];
+    const int q = q1 - q0;
+    const int L = p.seq_lens[r];
+    if (q0 < 0 || q < 0 || q1 > p.num_tokens || L < q || L > p.max_seq_len || q > p.max_query_len ||
+        div_up(L, kBlock) > p.max_blocks_per_seq)
+        return rp;
+    rp.valid = 1;
+    rp.rows = q * G;
+    if (rp.rows == 0) return rp;
+    if (rp.rows <= 16) {
+        rp.split = 1;
+        rp.pages = div_up(L, kBlock);
+        int n;
+        if (p.num_splits > 0) {
+            n = min(min(p.num_splits, kMaxSplits), rp.pages);
+        } else {
+            const int per = max(pages_per_split, div_up(rp.pages, kMaxSplits));
+            n = div_up(rp.pages, per);
+        }
+        rp.n_chunks = n;
+        rp.per_split = div_up(rp.pages, n);
+        rp.n_chunks = div_up(rp.pages, rp.per_split);   // no empty split
+    } else {
+        rp.split = 0;
+        rp.n_chunks = div_up(rp.rows, 16);
+    }
+    return rp;
+}
+
+// Page range of chunk k of request r.
+__device__ __forceinline__ int2 chunk_pages(const PlanParams &p, const ReqPlan &rp, int r, int k) {
+    if (rp.split) {
+        const int b = k * rp.per_split;
+        return make_int2(b, min(rp.pages, b + rp.per_split));
+    }
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const int q = p.qsl[r + 1] - p.qsl[r];
+    const int ctx = p.seq_lens[r] - q;
+    const int last_row = min(rp.rows, 16 * k + 16) - 1;
+    const int lim = ctx + last_row / G + 1;               // keys 0 .. lim-1 visible to the tile
+    return make_int2(0, div_up(lim, kBlock));
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+    __shared__ int bin_count[kSizeBins];
+    __shared__ int bin_cursor[kSizeBins];
+    __shared__ unsigned long long total_pages;
+    __shared__ unsigned long long prow_need;
+    __shared__ int bad;
+    __shared__ int prow_cursor;
+    __shared__ int pages_per_split;
+
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
+    int2 *req = reinterpret_cast<int2 *>(p.ws + p.lay.off_req);
+    int2 *tok = reinterpret_cast<int2 *>(p.ws + p.lay.off_tok);
+    int4 *chunks = reinterpret_cast<int4 *>(p.ws + p.lay.off_chunks);
+    const int tid = threadIdx.x;
+    const int G = p.num_q_heads / p.num_kv_heads;
+
+    for (int i = tid; i < kSizeBins; i += blockDim.x) bin_count[i] = 0;
+    if (tid == 0) {
+        total_pages = 0;
+        prow_need = 0;
+        bad = 0;
+        prow_cursor = 0;
+    }
+    for (int t = tid; t < p.num_tokens; t += blockDim.x) tok[t] = make_int2(-1, -1);
+    __syncthreads();
+
+    // pass 1: total key pages of split requests (sets the automatic split size)
+    if (p.qsl[0] != 0 && tid == 0) bad = 1;
+    unsigned long long mine = 0;
+    for (int r = tid; r < p.num_seqs; r += blockDim.x) {
+        const int q = p.qsl[r + 1] - p.qsl[r];
+        const int L = p.seq_lens[r];
+        if (q > 0 && q * G <= 16 && L >= q) mine += (unsigned long long)div_up(L, kBlock);
+    }
+    atomicAdd(&total_pages, mine);
+    __syncthreads();
+    if (tid == 0) {
+        // about 8 chunks per warp of the decode grid, 4..64 pages each
+        const unsigned long long work = total_pages * (unsigned long long)p.num_kv_heads;
+        const unsigned long long target = 8ull * (unsigned long long)max(p.total_warps, 1);
+        unsigned long long per = (work + target - 1) / target;
+        pages_per_split = (int)min(64ull, max(4ull, per));
+    }
+    __syncthreads();
+
+    // pass 2: count chunks per size bin, and the partial rows split requests need
+    unsigned long long prows = 0;
+    for (int r = tid; r < p.num_seqs; r += blockDim.x) {
+        const ReqPlan rp = plan_request(p, r, pages_per_split);
+        if (!rp.valid) {
+            atomicExch(&bad, 1);
+            continue;
+        }
+        if (rp.split && rp.n_chunks > 1)
+            prows += (unsigned long long)(p.qsl[r + 1] - p.qsl[r]) * p.num_q_heads * rp.n_chunks;
+        for (int k = 0; k < rp.n_chunks; ++k) {
+            const int2 pg = chunk_pages(p, rp, r, k);
+            atomicAdd(&bin_count[min(pg.y - pg.x, kSizeBins - 1)], 1);
+        }
+    }
+    atomicAdd(&prow_need, prows);
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;                                  // largest chunks first
+        for (int b = kSizeBins - 1; b >= 0; --b) {
+            bin_cursor[b] = acc;
+            acc += bin_count[b];
+        }
+        const bool fits = acc <= p.lay.max_chunks && prow_need <= (unsigned long long)p.lay.max_prow;
+        hdr->n_chunks = fits ? acc : 0;
+        if (!fits) bad = 2;
+    }
+    __syncthreads();
+    const bool overflow = bad == 2;
+
+    // pass 3: emit chunks, request info and token owners
+    for (int r = tid; r < p.num_seqs; r += blockDim.x) {
+        const ReqPlan rp = plan_request(p, r, pages_per_split);
+        int2 info = make_int2(rp.valid && !overflow ? 1 : 0, 0);
+        if (rp.valid && !overflow) {
+            if (rp.split && rp.n_chunks > 1) {
+                const int rows = (p.qsl[r + 1] - p.qsl[r]) * p.num_q_heads * rp.n_chunks;
+                const int base = atomicAdd(&prow_cursor, rows);
+                info = make_int2(rp.n_chunks, base);
+            }
+            for (int k = 0; k < rp.n_chunks; ++k) {
+                const int2 pg = chunk_pages(p, rp, r, k);
+                const int pos = atomicAdd(&bin_cursor[min(pg.y - pg.x, kSizeBins - 1)], 1);
+                chunks[pos] = make_int4(r, k, pg.x, pg.y);
+            }
+            for (int t = p.qsl[r]; t < p.qsl[r + 1]; ++t) tok[t] = make_int2(r, t - p.qsl[r]);
+        }
+        req[r] = info;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        hdr->status = bad ? PKV_ERR_DEVICE_METADATA : PKV_OK;
+        if (prow_cursor > p.lay.max_prow) hdr->status = PKV_ERR_DEVICE_METADATA;
+        hdr->magic = kMagic;
+        hdr->num_tokens = p.num_tokens;
+        hdr->num_q_heads = p.num_q_heads;
+        hdr->head_size = p.head_size;
+        hdr->num_seqs = p.num_seqs;
+        hdr->pages_per_split = pages_per_split;
+        hdr->off_req = p.lay.off_req;
+        hdr->off_tok = p.lay.off_tok;
+        hdr->off_chunks = p.lay.off_chunks;
+        hdr->off_part_lse = p.lay.off_part_lse;
+        hdr->off_part_o = p.lay.off_part_o;
+        hdr->max_chunks = p.lay.max_chunks;
+        hdr->max_prow = p.lay.max_prow;
+        hdr->prow_used = prow_cursor;
+    }
+}
+
+// ---- 2. attention -------------------------------------------------------------------
+
+// Shared-memory address of (row, 16-byte chunk) inside one TMA box of
+// 32 rows x 128 bytes written with the 128-byte swizzle: chunk c of row R is
+// stored at chunk position c ^ (R & 7).
+__device__ __forceinline__ uint32_t swz(uint32_t box_base, int row, int chunk) {
+    return box_base + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <int HD, int NW, int DEPTH>
+struct DecodeCfg {
+    static constexpr int kBoxes = HD / 64;                 // 64-element boxes per row
+    static constexpr int kBoxBytes = 2 * kBlock * 128;     // K and V rows of one box: 4 KiB
+    static constexpr int kPageBytes = kBoxes * kBoxBytes;  // one page of one kv head
+    static constexpr int kSmem = NW * DEPTH * kPageBytes + NW * DEPTH * 8 + 1024;
+};
+
+template <int HD, int NW, int DEPTH>
+__global__ void __launch_bounds__(NW * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
+    using Cfg = DecodeCfg<HD, NW, DEPTH>;
+    constexpr int KSTEPS = HD / 16;       // k-steps of S = Q K^T
+    constexpr int NTILES = HD / 8;        // n-tiles of O
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t *ring = smem + warp * DEPTH * Cfg::kPageBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * DEPTH * Cfg::kPageBytes) + warp * DEPTH;
+    const uint32_t ring_u32 = smem_u32(ring);
+
+    const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
+    int32_t *status = reinterpret_cast<int32_t *>(p.ws);
+    const int2 *req = reinterpret_cast<const int2 *>(p.ws + hdr->off_req);
+    const int4 *chunks = reinterpret_cast<const int4 *>(p.ws + hdr->off_chunks);
+    float *part_lse = reinterpret_cast<float *>(p.ws + hdr->off_part_lse);
+    float *part_o = reinterpret_cast<float *>(p.ws + hdr->off_part_o);
+    const int n_items = hdr->n_chunks * p.num_kv_heads;
+
+    if (lane == 0) {
+        for (int s = 0; s < DEPTH; ++s) mbar_init(&bars[s], 1);
+        if (warp == 0) tma_prefetch_desc(&kv_map);
+    }
+    fence_barrier_init();
+    __syncwarp();
+
+    const int W = gridDim.x * NW;
+    const int wid = blockIdx.x * NW + warp;
+    uint32_t seq = 0;              // pages consumed so far by this warp (ring position)
+    const int g4 = lane >> 2;      // fragment row within 8
+    const int t4 = lane & 3;       // fragment column pair
+    const float NEG_INF = -__int_as_float(0x7f800000);
+
+    for (int round = 0; round * W < n_items; ++round) {
+        const int item = (round & 1) ? round * W + (W - 1 - wid) : round * W + wid;   // snake order
+        if (item >= n_items) continue;
+        const int4 ch = chunks[item / p.num_kv_heads];
+        const int g = item % p.num_kv_heads;
+        const int r = ch.x;
+        const int pb = ch.z;
+        const int npages = ch.w - ch.z;
+        const int L = p.seq_lens[r];
+        const int qs = p.qsl[r];
+        const int qlen = p.qsl[r + 1] - qs;
+        const int ctx = L - qlen;
+        const int rows_total = qlen * p.G;
+        const bool split_mode = rows_total <= 16;
+        const int tile = split_mode ? 0 : ch.y;
+        const int split = split_mode ? ch.y : 0;
+        const int2 info = req[r];
+        const int n_split = split_mode ? info.x : 1;
+        const int rows = min(16, rows_total - 16 * tile);
+
+        // this thread's two fragment rows
+        const int R0 = g4, R1 = g4 + 8;
+        const int i0 = (16 * tile + R0) / p.G, hh0 = (16 * tile + R0) % p.G;
+        const int i1 = (16 * tile + R1) / p.G, hh1 = (16 * tile + R1) % p.G;
+        const int lim0 = R0 < rows ? ctx + i0 + 1 : 0;      // keys [0, lim) visible
+        const int lim1 = R1 < rows ? ctx + i1 + 1 : 0;
+
+        // block-table window: lane l holds the block of page (wbase + l)
+        const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks_per_seq + pb;
+        int wbase = 0;
+        int win = lane < npages ? __ldg(bt + lane) : -1;
+
+        auto issue = [&](int k) {            // page k of this chunk -> its ring stage
+            const int blk = __shfl_sync(0xffffffffu, win, k - wbase);
+            if (lane == 0) {
+                if (blk < 0 || blk >= p.num_blocks) set_status(status, PKV_ERR_DEVICE_INDEX);
+                const uint32_t st = (seq + k) % DEPTH;
+                uint8_t *dst = ring + st * Cfg::kPageBytes;
+                mbar_arrive_expect_tx(&bars[st], Cfg::kPageBytes);
+#pragma unroll
+                for (int bx = 0; bx < Cfg::kBoxes; ++bx)
+                    tma_load_5d(dst + bx * Cfg::kBoxBytes, &kv_map, &bars[st], bx * 64, 0, 0, g, blk);
+            }
+        };
+        int issued = min(DEPTH, npages);
+        for (int k = 0; k < issued; ++k) issue(k);
+
+        // Q fragments (A operand, rows = (query token, q head) pairs)
+        uint32_t qf[KSTEPS][4];
+        {
+            const __nv_bfloat16 *q0p = p.query + static_cast<int64_t>(qs + i0) * p.q_stride +
+                                       static_cast<int64_t>(g * p.G + hh0) * HD;
+            const __nv_bfloat16 *q1p = p.query + static_cast<int64_t>(qs + i1) * p.q_stride +
+                                       static_cast<int64_t>(g * p.G + hh1) * HD;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int c = kk * 16 + 2 * t4;
+                qf[kk][0] = R0 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q0p + c)) : 0u;
+                qf[kk][1] = R1 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q1p + c)) : 0u;
+                qf[kk][2] = R0 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q0p + c + 8)) : 0u;
+                qf[kk][3] = R1 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q1p + c + 8)) : 0u;
+            }
+        }
+
+        float o[NTILES][4];
+#pragma unroll
+        for (int n = 0; n < NTILES; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+        int failed_at = -1;
+
+        for (int k = 0; k < npages; ++k) {
+            const uint32_t st = (seq + k) % DEPTH;
+            const uint32_t par = ((seq + k) / DEPTH) & 1u;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], par));
+            if (!ok) {
+                failed_at = k;
+                break;
+            }
+            const uint32_t page = ring_u32 + st * Cfg::kPageBytes;
+            const int j0 = (pb + k) * kBlock;       // first key of this page
+
+            // zero V rows past the end of the sequence (last page only)
+            if (j0 + kBlock > L) {
+                const int vfirst = L - j0;
+                const int nrows = kBlock - vfirst;
+                for (int e = lane; e < Cfg::kBoxes * nrows * 8; e += 32) {
+                    const int bx = e / (nrows * 8);
+                    const int rem = e % (nrows * 8);
+                    const int row = kBlock + vfirst + rem / 8;
+                    const int chunk = rem % 8;
+                    const uint32_t a = swz(page + bx * Cfg::kBoxBytes, row, chunk);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                }
+                __syncwarp();
+            }
+
+            // S = Q K^T for the page's 16 tokens (two n-tiles)
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int bx = kk / 4;
+                const int tok = ((lane >> 4) << 3) + (lane & 7);
+                const int chunk = (kk % 4) * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(swz(page + bx * Cfg::kBoxBytes, tok, chunk), b0, b1, b2, b3);
+                mma_bf16_16816(s0, qf[kk], b0, b1);
+                mma_bf16_16816(s1, qf[kk], b2, b3);
+            }
+
+            // online softmax in the log2 domain; keys a row may not see get -inf
+            const int c0 = j0 + 2 * t4, c1 = c0 + 1, c8 = c0 + 8, c9 = c0 + 9;
+            float x[8];
+            x[0] = c0 < lim0 ? s0[0] * p.scale_log2 : NEG_INF;
+            x[1] = c1 < lim0 ? s0[1] * p.scale_log2 : NEG_INF;
+            x[2] = c0 < lim1 ? s0[2] * p.scale_log2 : NEG_INF;
+            x[3] = c1 < lim1 ? s0[3] * p.scale_log2 : NEG_INF;
+            x[4] = c8 < lim0 ? s1[0] * p.scale_log2 : NEG_INF;
+            x[5] = c9 < lim0 ? s1[1] * p.scale_log2 : NEG_INF;
+            x[6] = c8 < lim1 ? s1[2] * p.scale_log2 : NEG_INF;
+            x[7] = c9 < lim1 ? s1[3] * p.scale_log2 : NEG_INF;
+            float mx0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[4], x[5]));
+            float mx1 = fmaxf(fmaxf(x[2], x[3]), fmaxf(x[6], x[7]));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float ref0 = mn0 == NEG_INF ? 0.f : mn0;
+            const float ref1 = mn1 == NEG_INF ? 0.f : mn1;
+            const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
+            m0 = mn0;
+            m1 = mn1;
+            float pr[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pr[e] = exp2f(x[e] - (((e >> 1) & 1) ? ref1 : ref0));
+            l0 = l0 * a0 + (pr[0] + pr[1] + pr[4] + pr[5]);
+            l1 = l1 * a1 + (pr[2] + pr[3] + pr[6] + pr[7]);
+#pragma unroll
+            for (int n = 0; n < NTILES; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
+            uint32_t pa[4];
+            pa[0] = pack_bf16x2(pr[0], pr[1]);
+            pa[1] = pack_bf16x2(pr[2], pr[3]);
+            pa[2] = pack_bf16x2(pr[4], pr[5]);
+            pa[3] = pack_bf16x2(pr[6], pr[7]);
+
+            // O += P V (V rows are the page's tokens, read transposed)
+#pragma unroll
+            for (int n = 0; n < NTILES; n += 2) {
+                const int bx = n / 8;
+                const int tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int chunk = (n % 8) + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(swz(page + bx * Cfg::kBoxBytes, kBlock + tok, chunk), b0, b1, b2, b3);
+                mma_bf16_16816(o[n], pa, b0, b1);
+                mma_bf16_16816(o[n + 1], pa, b2, b3);
+            }
+
+            // refill this stage with page k + DEPTH of the chunk
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int nk = k + DEPTH;
+            if (nk < npages) {
+                if (nk - wbase >= 32) {
+                    wbase += 32;
+                    win = wbase + lane < npages ? __ldg(bt + wbase + lane) : -1;
+                }
+                issue(nk);
+                ++issued;
+            }
+        }
+
+        if (failed_at >= 0) {
+            set_status(status, PKV_ERR_DEVICE_TIMEOUT);
+            // let copies already in flight land before the CTA's memory is released
+            for (int k = failed_at; k < issued; ++k) {
+                const uint32_t st = (seq + k) % DEPTH;
+                mbar_wait_bounded(&bars[st], ((seq + k) / DEPTH) & 1u);
+            }
+            return;
+        }
+        seq += npages;
+
+        // finish the rows: quad sums of l, then normalise
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
+        const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        const int h0 = g * p.G + hh0, h1 = g * p.G + hh1;
+        if (n_split <= 1) {
+            if (R0 < rows) {
+                __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(qs + i0) * p.num_q_heads + h0) * HD;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n)
+                    *reinterpret_cast<uint32_t *>(dst + n * 8 + 2 * t4) = pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
+            }
+            if (R1 < rows) {
+                __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(qs + i1) * p.num_q_heads + h1) * HD;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n)
+                    *reinterpret_cast<uint32_t *>(dst + n * 8 + 2 * t4) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
+            }
+        } else {
+            const float LN2 = 0.69314718055994531f;
+            if (R0 < rows) {
+                const int64_t prow = info.y + (static_cast<int64_t>(i0) * p.num_q_heads + h0) * n_split + split;
+                float *dst = part_o + prow * HD;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n)
+                    *reinterpret_cast<float2 *>(dst + n * 8 + 2 * t4) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                if (t4 == 0) part_lse[prow] = l0 > 0.f ? (m0 + __log2f(l0)) * LN2 : NEG_INF;
+            }
+            if (R1 < rows) {
+                const int64_t prow = info.y + (static_cast<int64_t>(i1) * p.num_q_heads + h1) * n_split + split;
+                float *dst = part_o + prow * HD;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n)
+                    *reinterpret_cast<float2 *>(dst + n * 8 + 2 * t4) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                if (t4 == 0) part_lse[prow] = l1 > 0.f ? (m1 + __log2f(l1)) * LN2 : NEG_INF;
+            }
+        }
+    }
+}
+
+// ---- 3. combine -------------------------------------------------------------------------
+
+template <int HD>
+__global__ void __launch_bounds__(256) combine_kernel(__nv_bfloat16 *out, const uint8_t *ws, int32_t num_tokens,
+                                                      int32_t num_q_heads) {
+    const WsHeader *hdr = reinterpret_cast<const WsHeader *>(ws);
+    if (hdr->magic != kMagic || hdr->num_tokens != num_tokens || hdr->num_q_heads != num_q_heads ||
+        hdr->head_size != HD) {
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            set_status(reinterpret_cast<int32_t *>(const_cast<uint8_t *>(ws)), PKV_ERR_PROTOCOL);
+        return;
+    }
+    const int2 *req = reinterpret_cast<const int2 *>(ws + hdr->off_req);
+    const int2 *tok = reinterpret_cast<const int2 *>(ws + hdr->off_tok);
+    const float *part_lse = reinterpret_cast<const float *>(ws + hdr->off_part_lse);
+    const float *part_o = reinterpret_cast<const float *>(ws + hdr->off_part_o);
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= static_cast<int64_t>(num_tokens) * num_q_heads) return;
+    const int t = static_cast<int>(row / num_q_heads);
+    const int h = static_cast<int>(row % num_q_heads);
+    const int2 ti = tok[t];
+    if (ti.x < 0) return;
+    const int2 info = req[ti.x];
+    const int n = info.x;
+    if (n <= 1) return;
+    const int64_t base = info.y + (static_cast<int64_t>(ti.y) * num_q_heads + h) * n;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const float lse = lane < n ? part_lse[base + lane] : NEG_INF;
+    float mx = lse;
+#pragma unroll
+    for (int s = 16; s; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    const float w = (lse == NEG_INF) ? 0.f : __expf(lse - mx);
+    float wsum = w;
+#pragma unroll
+    for (int s = 16; s; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
+    constexpr int PER = HD / 32;          // dims per lane (2 or 4)
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int s = 0; s < n; ++s) {
+        const float wt = __shfl_sync(0xffffffffu, w, s);
+        const float *src = part_o + (base + s) * HD + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src);
+            acc[0] += wt * v.x;
+            acc[1] += wt * v.y;
+            acc[2] += wt * v.z;
+            acc[3] += wt * v.w;
+        } else {
+            const float2 v = *reinterpret_cast<const float2 *>(src);
+            acc[0] += wt * v.x;
+            acc[1] += wt * v.y;
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __nv_bfloat16 *dst = out + row * HD + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+        *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+}
+
+// ---- host side ----------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map of the cache as a 5-D bf16 tensor {head_size, 16, 2, Hkv, num_blocks}
+// (innermost first), loaded in boxes of {64, 16, 2, 1, 1} with 128-byte swizzle.
+static int make_kv_map(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t head_size) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return PKV_ERR_CUDA;
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2,
+                                static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t row = static_cast<cuuint64_t>(head_size) * 2;
+    const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * num_kv_heads};
+    const cuuint32_t box[5] = {64, kBlock, 2, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult rc = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+template <int HD, int NW, int DEPTH>
+static int launch_decode(const CUtensorMap &map, const AttnParams &p, int grid, int dev, cudaStream_t stream) {
+    using Cfg = DecodeCfg<HD, NW, DEPTH>;
+    static std::mutex mu;
+    static uint64_t done_mask = 0;       // devices whose shared-memory limit is already raised
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+        if (!bit || !(done_mask & bit)) {
+            if (cudaFuncSetAttribute(decode_kernel<HD, NW, DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::kSmem) != cudaSuccess)
+                return PKV_ERR_CUDA;
+            done_mask |= bit;
+        }
+    }
+    decode_kernel<HD, NW, DEPTH><<<grid, NW * 32, Cfg::kSmem, stream>>>(map, p);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// decode tiling per head size: warps per CTA, ring stages per warp, CTAs per SM
+template <int HD> struct DecodeTiling;
+template <> struct DecodeTiling<64> { static constexpr int NW = 4, DEPTH = 6, CTAS_PER_SM = 2; };
+template <> struct DecodeTiling<128> { static constexpr int NW = 4, DEPTH = 3, CTAS_PER_SM = 2; };
+
+}  // namespace pkv
+
+extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_stride, const void *kv_cache,
+                              int64_t num_blocks, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                              int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_size, int32_t block_size, float scale,
+                              int32_t num_splits, void *workspace, size_t workspace_bytes, size_t *workspace_needed,
+                              void *stream) {
+    using namespace pkv;
+    // ---- host-side validation: nothing is enqueued on error ----
+    if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_query_len < 0 ||
+        max_seq_len < 0 || max_blocks_per_seq < 0 || num_splits < 0)
+        return PKV_ERR_SHAPE;
+    if (block_size != kBlock || (head_size != 64 && head_size != 128)) return PKV_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads) return PKV_ERR_SHAPE;
+    if (num_tokens > 0 && num_seqs == 0) return PKV_ERR_SHAPE;
+    if (max_query_len > max_seq_len) return PKV_ERR_SHAPE;
+    if (static_cast<int64_t>(max_blocks_per_seq) * kBlock < max_seq_len) return PKV_ERR_SHAPE;
+    if (num_blocks < 1 || num_blocks > INT32_MAX) return PKV_ERR_SHAPE;
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PKV_ERR_SHAPE;
+
+    const WsLayout lay =
+        ws_layout(num_seqs, num_tokens, max_query_len, max_seq_len, num_q_heads, num_kv_heads, head_size);
+    if (workspace_needed) *workspace_needed = static_cast<size_t>(lay.total);
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !query || !kv_cache || !block_tables || !seq_lens || !query_start_loc) return PKV_ERR_NULL;
+    if (!workspace || workspace_bytes < static_cast<size_t>(lay.total)) return PKV_ERR_WORKSPACE;
+    if (query_token_stride < static_cast<int64_t>(num_q_heads) * head_size) return PKV_ERR_SHAPE;
+    if (query_token_stride % 8) return PKV_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(query) |
+         reinterpret_cast<uintptr_t>(kv_cache)) & 15u)
+        return PKV_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PKV_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(block_tables) | reinterpret_cast<uintptr_t>(seq_lens) |
+         reinterpret_cast<uintptr_t>(query_start_loc)) & 3u)
+        return PKV_ERR_ALIGNMENT;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PKV_ERR_CUDA;
+
+    CUtensorMap map;
+    int rc = make_kv_map(&map, kv_cache, num_blocks, num_kv_heads, head_size);
+    if (rc) return rc;
+
+    const int nw = head_size == 64 ? DecodeTiling<64>::NW : DecodeTiling<128>::NW;
+    const int per_sm = head_size == 64 ? DecodeTiling<64>::CTAS_PER_SM : DecodeTiling<128>::CTAS_PER_SM;
+    int64_t grid = static_cast<int64_t>(sms) * per_sm;
+    const int64_t max_items = lay.max_chunks * num_kv_heads;
+    if (grid > (max_items + nw - 1) / nw) grid = (max_items + nw - 1) / nw;
+    if (grid < 1) grid = 1;
+
+    PlanParams pp;
+    pp.ws = static_cast<uint8_t *>(workspace);
+    pp.seq_lens = seq_lens;
+    pp.qsl = query_start_loc;
+    pp.num_seqs = num_seqs;
+    pp.num_tokens = num_tokens;
+    pp.num_q_heads = num_q_heads;
+    pp.num_kv_heads = num_kv_heads;
+    pp.head_size = head_size;
+    pp.max_blocks_per_seq = max_blocks_per_seq;
+    pp.max_query_len = max_query_len;
+    pp.max_seq_len = max_seq_len;
+    pp.num_splits = num_splits;
+    pp.total_warps = static_cast<int32_t>(grid * nw);
+    pp.lay = lay;
+    plan_kernel<<<1, kPlanThreads, 0, st>>>(pp);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+
+    AttnParams ap;
+    ap.out = static_cast<__nv_bfloat16 *>(out);
+    ap.query = static_cast<const __nv_bfloat16 *>(query);
+    ap.q_stride = query_token_stride;
+    ap.block_tables = block_tables;
+    ap.max_blocks_per_seq = max_blocks_per_seq;
+    ap.seq_lens = seq_lens;
+    ap.qsl = query_start_loc;
+    ap.num_q_heads = num_q_heads;
+    ap.num_kv_heads = num_kv_heads;
+    ap.G = num_q_heads / num_kv_heads;
+    ap.num_blocks = num_blocks;
+    ap.scale_log2 = scale * 1.4426950408889634f;
+    ap.ws = static_cast<uint8_t *>(workspace);
+    if (head_size == 64)
+        return launch_decode<64, DecodeTiling<64>::NW, DecodeTiling<64>::DEPTH>(map, ap, static_cast<int>(grid), dev,
+                                                                                st);
+    return launch_decode<128, DecodeTiling<128>::NW, DecodeTiling<128>::DEPTH>(map, ap, static_cast<int>(grid), dev,
+                                                                                  st);
+}
+
+extern "C" int pkv_paged_attn_combine(void *out, const void *workspace, size_t workspace_bytes, int32_t num_tokens,
+                                      int32_t num_q_heads, int32_t head_size, void *stream) {
+    using namespace pkv;
+    if (num_tokens < 0 || num_q_heads <= 0) return PKV_ERR_SHAPE;
+    if (head_size != 64 && head_size != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!out || !workspace) return PKV_ERR_NULL;
+    if (workspace_bytes < 256) return PKV_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(out) & 15u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_ALIGNMENT;
+    const int64_t rows = static_cast<int64_t>(num_tokens) * num_q_heads;
+    const int64_t grid = (rows + 7) / 8;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (head_size == 64)
+        combine_kernel<64><<<static_cast<unsigned>(grid), 256, 0, st>>>(
+            static_cast<__nv_bfloat16 *>(out), static_cast<const uint8_t *>(workspace), num_tokens, num_q_heads);
+    else
+        combine_kernel<128><<<static_cast<unsigned>(grid), 256, 0, st>>>(
+            static_cast<__nv_bfloat16 *>(out), static_cast<const uint8_t *>(workspace), num_tokens, num_q_heads);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
