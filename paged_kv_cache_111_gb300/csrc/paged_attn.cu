@@ -498,11 +498,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 o[n][2] *= a1;
                 o[n][3] *= a1;
             }
-            uint32_t pa[4];
-            pa[0] = pack_bf16x2(pr[0], pr[1]);
-            pa[1] = pack_bf16x2(pr[2], pr[3]);
-            pa[2] = pack_bf16x2(pr[4], pr[5]);
-            pa[3] = pack_bf16x2(pr[6], pr[7]);
+            // P as a bf16 pair (hi + remainder): the PV product keeps about
+            // 16 bits of each weight instead of bf16's 8
+            uint32_t pa[4], pl[4];
+            split_bf16x2(pr[0], pr[1], pa[0], pl[0]);
+            split_bf16x2(pr[2], pr[3], pa[1], pl[1]);
+            split_bf16x2(pr[4], pr[5], pa[2], pl[2]);
+            split_bf16x2(pr[6], pr[7], pa[3], pl[3]);
 
             // O += P V (V rows are the page's tokens, read transposed)
 #pragma unroll
@@ -514,6 +516,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 ldsm_x4_trans(swz(page + bx * Cfg::kBoxBytes, kBlock + tok, chunk), b0, b1, b2, b3);
                 mma_bf16_16816(o[n], pa, b0, b1);
                 mma_bf16_16816(o[n + 1], pa, b2, b3);
+                mma_bf16_16816(o[n], pl, b0, b1);
+                mma_bf16_16816(o[n + 1], pl, b2, b3);
             }
 
             // refill this stage with page k + DEPTH of the chunk

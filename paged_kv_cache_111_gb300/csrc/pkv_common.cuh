@@ -109,6 +109,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// (x, y) -> a bf16x2 pair `big` plus the bf16x2 remainder `rest`: big + rest
+// carries about 16 significant bits of each value, so a product with bf16
+// operands summed in fp32 loses little more than fp32 rounding.
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &big, uint32_t &rest) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(x, y);
+    const float2 bf = __bfloat1622float2(b);
+    const __nv_bfloat162 r = __floats2bfloat162_rn(x - bf.x, y - bf.y);
+    big = *reinterpret_cast<const uint32_t *>(&b);
+    rest = *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // Record an error code in a device status word (first error wins).
 __device__ __forceinline__ void set_status(int32_t *status, int32_t code) {
     if (status) atomicCAS(status, 0, code);
