@@ -183,6 +183,47 @@ int pkv_paged_attn_combine(void *out, const void *workspace, size_t workspace_by
                            int32_t num_tokens, int32_t num_q_heads, int32_t head_size,
                            void *stream);
 
+/*
+ * pkv_paged_attn_noalloc — paged attention that allocates nothing.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate GPU memory where they run attention (for example code
+ * under a strict no-allocation policy while a CUDA graph is captured, or a
+ * plugin whose host engine owns all device memory and passes in only inputs
+ * and outputs).  It computes exactly what pkv_paged_attn followed by
+ * pkv_paged_attn_combine computes, with the same arguments except the
+ * workspace: the scratch lives in a fixed array of this library's own device
+ * memory, PKV_NOALLOC_SCRATCH_BYTES (256 MiB) on every GPU where the call's
+ * code is loaded, held until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ *  - Sizes whose scratch (the workspace size pkv_paged_attn would report)
+ *    exceeds PKV_NOALLOC_SCRATCH_BYTES are refused with PKV_ERR_WORKSPACE
+ *    before anything is enqueued; argument errors return the same codes as
+ *    pkv_paged_attn.
+ *  - The first call on each device looks up the array's device address
+ *    (and, under lazy module loading, loads this code onto the device); make
+ *    that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind; each call rewrites all of the scratch it later reads, so nothing
+ *    needs clearing between calls.  Calls that overlap on the GPU (other
+ *    streams, other threads' streams) race on the array: keep them ordered,
+ *    e.g. on one stream.
+ *  - device_status: optional int32 device word; after the call's kernels it
+ *    receives the device status (PKV_OK or a PKV_ERR_DEVICE_* code).
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (256u << 20)
+
+int pkv_paged_attn_noalloc(void *out, const void *query, int64_t query_token_stride,
+                           const void *kv_cache, int64_t num_blocks,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *seq_lens, const int32_t *query_start_loc,
+                           int32_t num_seqs, int32_t num_tokens,
+                           int32_t max_query_len, int32_t max_seq_len,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                           int32_t block_size, float scale, int32_t num_splits,
+                           int32_t *device_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

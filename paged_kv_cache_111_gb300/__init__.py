@@ -159,3 +159,31 @@ def paged_attn_combine(out: torch.Tensor, workspace: torch.Tensor, stream=None) 
 def workspace_status(workspace: torch.Tensor) -> int:
     """The device status word (first int32 of the workspace); synchronises on its read."""
     return int(workspace[:4].view(torch.int32)[0].item())
+
+
+def paged_attn_noalloc(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Tensor, block_tables: torch.Tensor,
+                       seq_lens: torch.Tensor, query_start_loc: torch.Tensor, max_query_len: int, max_seq_len: int,
+                       scale: float, num_splits: int = 0, device_status: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """paged_attn + paged_attn_combine without a caller workspace: for callers
+    that cannot allocate device memory.  The scratch is the library's own
+    fixed device array (see pkv_paged_attn_noalloc in include/pkv.h)."""
+    _need_cuda(out, query, kv_cache, block_tables, seq_lens, query_start_loc, device_status)
+    lib = load()
+    fn = lib.pkv_paged_attn_noalloc
+    if fn.argtypes is None:
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        fn.argtypes = [P, P, i64, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                       ctypes.c_float, i32, P, P]
+        fn.restype = ctypes.c_int
+    nb, hkv, _, bs, d = kv_cache.shape
+    T, H = int(query.shape[0]), int(query.shape[1])
+    if query.stride(2) != 1 or query.stride(1) != d:
+        raise ValueError("query must be [T, H, d] with contiguous heads")
+    if not out.is_contiguous() or tuple(out.shape) != (T, H, d):
+        raise ValueError("out must be a contiguous [T, H, d] tensor")
+    rc = fn(_ptr(out), _ptr(query), query.stride(0), _ptr(kv_cache), nb, _ptr(block_tables),
+            int(block_tables.shape[1]), _ptr(seq_lens), _ptr(query_start_loc), int(seq_lens.shape[0]), T,
+            int(max_query_len), int(max_seq_len), H, hkv, d, bs, ctypes.c_float(scale), int(num_splits),
+            _ptr(device_status), _stream(out, stream))
+    _check(rc, "pkv_paged_attn_noalloc")
