@@ -37,6 +37,24 @@ import workloads as wl  # noqa: E402
 METRIC = "decode paged-attn achieved HBM GB/s (% of peak), tokens/s per layer-step"
 FALLBACK_HBM_GBS = 6800.0
 
+# DRAM bytes (read + write) per algorithmic byte of the attention launch, from
+# the ncu capture summarised in profiles/decode_kernel_llama13b-decode-64req.md
+# (64-request case of the 13B batch: 1.0510 GB of traffic for 1.0339 GB of
+# algorithmic bytes).  Traffic grows with the KV bytes read, so the full
+# launch's traffic is this ratio times its algorithmic bytes.  It holds only
+# for the kernel sources it was measured on (hash below); otherwise null.
+DECODE_TRAFFIC = {"sources_sha256_16": "d8d9cfae647e79d4", "ratio": 1.051008 / 1.033885,
+                  "profile": "profiles/decode_kernel_llama13b-decode-64req.md"}
+
+
+def decode_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("paged_attn.cu", "pkv_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_111_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
 
 # ---------------------------------------------------------------------------
 # algorithmic bytes
@@ -145,6 +163,9 @@ def run_gpu(args, rank: int, world: int) -> dict:
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     step = wl.make_workload(args.workload, seed=wl.seed_of(args.workload) + 1000 * rank)
+    if args.subset:
+        # the first `subset` requests with a compact pool (profiling-size case)
+        step = step.subset(list(range(min(args.subset, step.num_seqs))), name=f"{args.workload}[:{args.subset}]")
     T, H, d = step.num_tokens, step.num_q_heads, step.head_size
     to = {f: getattr(step, f).to(dev).contiguous() for f in
           ("seq_lens", "query_start_loc", "block_tables", "query", "key", "value", "slot_mapping")}
@@ -212,7 +233,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
     dev_in = {f: torch.empty_like(t, device=dev) for f, t in host_in.items()}
-    e2e_steps = max(3, min(args.steps, 200))
+    e2e_steps = max(3, min(args.steps, 200)) if args.e2e else 0
 
     def e2e_step():
         for f, t in host_in.items():
@@ -223,19 +244,21 @@ def run_gpu(args, rank: int, world: int) -> dict:
         pkv.paged_attn_combine(out, ws)
         host_out.copy_(out, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = float("nan")
+    if e2e_steps:
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     # ---- same-run copy probe (device-to-device copy, read + write bytes) ------
     probe_gbs = None
@@ -349,6 +372,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-copy-probe", dest="copy_probe", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--subset", type=int, default=0,
+                    help="keep only the first N requests, with a compact pool (small profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -390,7 +416,7 @@ def main():
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": args.workload, "num_seqs": step.num_seqs, "num_tokens": step.num_tokens,
+            "workload": step.name, "num_seqs": step.num_seqs, "num_tokens": step.num_tokens,
             "num_q_heads": step.num_q_heads, "num_kv_heads": step.num_kv_heads, "head_size": step.head_size,
             "block_size": step.block_size, "num_blocks": step.num_blocks,
             "kv_bytes_per_step": ab["kv_unique"], "parallelism": f"replicas x{world}",
@@ -404,10 +430,14 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "paged_attn (plan + decode kernels)",
                      "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": attn_gbs / pk["hbm_gbs"], "peak_source": pk["source"],
-                     "algorithmic_bytes_per_launch": ab["attention"], "traffic": None},
+                     "algorithmic_bytes_per_launch": ab["attention"],
+                     "traffic": (DECODE_TRAFFIC["ratio"] * ab["attention"]
+                                 if decode_sources_hash() == DECODE_TRAFFIC["sources_sha256_16"] else None),
+                     "traffic_source": DECODE_TRAFFIC["profile"] + " (scaled by algorithmic bytes)"},
         "copy_probe_gbs": r["probe_gbs"],
-        "e2e": {"value": world * ab["step"] / (e2e_max * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": e2e_max},
+        "e2e": ({"value": world * ab["step"] / (e2e_max * 1e-3) / 1e9, "unit": "GB/s",
+                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": e2e_max}
+                if e2e_max == e2e_max else None),
         "gpu_launches": 4 * args.steps,
         "clocks": r["clocks"],
     }
