@@ -1,0 +1,69 @@
+// Internal interface shared by the attention translation units: workspace
+// layout, plan output, kernel parameter blocks and the prefill launcher.
+#pragma once
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+constexpr int kMaxSplits = 32;        // key ranges per split row, at most
+constexpr int kDecodeTileMaxRows = 64;  // longer requests go to the tensor-core prefill kernel
+constexpr int kPrefillRows = 128;     // rows of one prefill tile (M of the MMA)
+constexpr int kPrefillKeys = 128;     // keys of one prefill KV tile (N of S = Q K^T)
+constexpr int32_t kMagic = 0x504B5632;  // "PKV2"
+
+struct WsHeader {
+    int32_t status;          // device status word (first 4 bytes)
+    int32_t magic;
+    int32_t n_chunks;        // decode-kernel chunks
+    int32_t num_tokens;
+    int32_t num_q_heads;
+    int32_t head_size;
+    int32_t num_seqs;
+    int32_t pages_per_split;
+    int32_t n_ptiles;        // prefill-kernel tiles
+    int32_t pad_;
+    int64_t off_req;         // int2 [num_seqs]: {splits, partial row base}
+    int64_t off_tok;         // int2 [num_tokens]: {request, index in request} (-1 if none)
+    int64_t off_chunks;      // int4 [max_chunks]: {request, split or tile, page begin, page end}
+    int64_t off_ptiles;      // int4 [max_ptiles]: {request, q tile, kv tiles, 0}
+    int64_t off_part_lse;    // float [max_prow]
+    int64_t off_part_o;      // float [max_prow][head_size]
+    int64_t max_chunks;
+    int64_t max_ptiles;
+    int64_t max_prow;
+    int64_t prow_used;
+};
+static_assert(sizeof(WsHeader) <= 256, "header must fit its 256-byte slot");
+
+struct WsLayout {
+    int64_t off_req, off_tok, off_chunks, off_ptiles, off_part_lse, off_part_o, total;
+    int64_t max_chunks, max_ptiles, max_prow;
+};
+
+struct PrefillParams {
+    __nv_bfloat16 *out;
+    const int32_t *block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t *seq_lens;
+    const int32_t *qsl;
+    int32_t num_q_heads, num_kv_heads, G;
+    int64_t num_blocks;
+    float scale_log2;
+    int32_t lo_tiles;         // leading KV tiles whose P always enters P V as a bf16 pair
+    uint8_t *ws;
+};
+
+// Is the tensor-core prefill kernel available for this head layout?
+inline bool prefill_supported(int num_q_heads, int num_kv_heads, int head_size) {
+    const int G = num_q_heads / num_kv_heads;
+    return (head_size == 64 || head_size == 128) && G >= 1 && G <= kPrefillRows && (kPrefillRows % G) == 0;
+}
+
+// Host launcher of the prefill kernel (prefill_tc.cu).  `grid` CTAs; CTAs
+// beyond the plan's tile count return at once.
+int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
+                   const void *kv_cache, int64_t num_blocks, int32_t head_size, int64_t grid, int dev,
+                   cudaStream_t stream);
+
+}  // namespace pkv

@@ -31,41 +31,14 @@
 // cache slots cannot reach an output.
 #include <mutex>
 
-#include "pkv_common.cuh"
+#include "attn_internal.cuh"
 
 namespace pkv {
 
-constexpr int kMaxSplits = 32;      // key ranges per split row, at most
 constexpr int kPlanThreads = 1024;
-constexpr int kSizeBins = 256;      // counting-sort bins for chunk sizes (pages)
-constexpr int32_t kMagic = 0x504B5631;   // "PKV1"
+constexpr int kSizeBins = 256;      // counting-sort bins for chunk sizes (pages or KV tiles)
 
 // ---- workspace layout ---------------------------------------------------------
-
-struct WsHeader {
-    int32_t status;          // device status word (first 4 bytes)
-    int32_t magic;
-    int32_t n_chunks;
-    int32_t num_tokens;
-    int32_t num_q_heads;
-    int32_t head_size;
-    int32_t num_seqs;
-    int32_t pages_per_split;
-    int64_t off_req;         // int2 [num_seqs]: {splits, partial row base}
-    int64_t off_tok;         // int2 [num_tokens]: {request, index in request} (-1 if none)
-    int64_t off_chunks;      // int4 [max_chunks]: {request, split or tile, page begin, page end}
-    int64_t off_part_lse;    // float [max_prow]
-    int64_t off_part_o;      // float [max_prow][head_size]
-    int64_t max_chunks;
-    int64_t max_prow;
-    int64_t prow_used;
-};
-static_assert(sizeof(WsHeader) <= 256, "header must fit its 256-byte slot");
-
-struct WsLayout {
-    int64_t off_req, off_tok, off_chunks, off_part_lse, off_part_o, total;
-    int64_t max_chunks, max_prow;
-};
 
 static inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
@@ -83,6 +56,8 @@ static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_quer
     (void)max_query_len;
     // chunks: split requests give <= splits each; tiled ones ceil(q_r G / 16) <= q_r G / 16 + 1
     w.max_chunks = num_seqs * splits + (num_tokens * G + 15) / 16 + num_seqs;
+    // prefill tiles: ceil(q_r G / 128) <= q_r G / 128 + 1
+    w.max_ptiles = (num_tokens * G + kPrefillRows - 1) / kPrefillRows + num_seqs;
     int64_t off = 256;
     w.off_req = off;
     off = align256(off + 8 * num_seqs);
@@ -90,6 +65,8 @@ static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_quer
     off = align256(off + 8 * num_tokens);
     w.off_chunks = off;
     off = align256(off + 16 * w.max_chunks);
+    w.off_ptiles = off;
+    off = align256(off + 16 * w.max_ptiles);
     w.off_part_lse = off;
     off = align256(off + 4 * w.max_prow);
     w.off_part_o = off;
@@ -108,6 +85,7 @@ struct PlanParams {
     int32_t max_blocks_per_seq, max_query_len, max_seq_len;
     int32_t num_splits;       // 0 = auto
     int32_t total_warps;      // warps of the decode grid (for the automatic split size)
+    int32_t prefill_ok;       // long requests go to the tensor-core prefill kernel
     WsLayout lay;
 };
 
@@ -129,14 +107,16 @@ struct AttnParams {
 
 __device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
 
-// Work of request r: number of chunks, and whether its rows are split along keys.
+// Work of request r.  mode 0: rows split along key pages (q_r * G <= 16);
+// mode 1: 16-row tiles on the decode kernel; mode 2: 128-row tiles on the
+// tensor-core prefill kernel.
 struct ReqPlan {
     int valid;        // metadata consistent
     int rows;         // q_r * G
-    int split;        // 1: split-K over key pages; 0: 16-row tiles
-    int n_chunks;
-    int pages;        // key pages of the request (split mode)
-    int per_split;    // pages per split (split mode)
+    int mode;
+    int n_chunks;     // decode-kernel chunks (modes 0, 1) or prefill tiles (mode 2)
+    int pages;        // key pages of the request (mode 0)
+    int per_split;    // pages per split (mode 0)
 };
 
 __device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split) {
@@ -152,7 +132,7 @@ __device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split)
     rp.rows = q * G;
     if (rp.rows == 0) return rp;
     if (rp.rows <= 16) {
-        rp.split = 1;
+        rp.mode = 0;
         rp.pages = div_up(L, kBlock);
         int n;
         if (p.num_splits > 0) {
@@ -161,33 +141,42 @@ __device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split)
             const int per = max(pages_per_split, div_up(rp.pages, kMaxSplits));
             n = div_up(rp.pages, per);
         }
-        rp.n_chunks = n;
         rp.per_split = div_up(rp.pages, n);
         rp.n_chunks = div_up(rp.pages, rp.per_split);   // no empty split
+    } else if (p.prefill_ok && rp.rows > kDecodeTileMaxRows) {
+        rp.mode = 2;
+        rp.n_chunks = div_up(rp.rows, kPrefillRows);
     } else {
-        rp.split = 0;
+        rp.mode = 1;
         rp.n_chunks = div_up(rp.rows, 16);
     }
     return rp;
 }
 
-// Page range of chunk k of request r.
-__device__ __forceinline__ int2 chunk_pages(const PlanParams &p, const ReqPlan &rp, int r, int k) {
-    if (rp.split) {
-        const int b = k * rp.per_split;
-        return make_int2(b, min(rp.pages, b + rp.per_split));
-    }
+// Keys 0 .. lim-1 visible to the last row of a tile ending before row `row_end`.
+__device__ __forceinline__ int tile_key_limit(const PlanParams &p, const ReqPlan &rp, int r, int row_end) {
     const int G = p.num_q_heads / p.num_kv_heads;
     const int q = p.qsl[r + 1] - p.qsl[r];
     const int ctx = p.seq_lens[r] - q;
-    const int last_row = min(rp.rows, 16 * k + 16) - 1;
-    const int lim = ctx + last_row / G + 1;               // keys 0 .. lim-1 visible to the tile
-    return make_int2(0, div_up(lim, kBlock));
+    const int last_row = min(rp.rows, row_end) - 1;
+    return ctx + last_row / G + 1;
+}
+
+// Mode 0/1: page range of chunk k.  Mode 2: {0, KV tiles} of tile k.
+__device__ __forceinline__ int2 chunk_pages(const PlanParams &p, const ReqPlan &rp, int r, int k) {
+    if (rp.mode == 0) {
+        const int b = k * rp.per_split;
+        return make_int2(b, min(rp.pages, b + rp.per_split));
+    }
+    if (rp.mode == 1) return make_int2(0, div_up(tile_key_limit(p, rp, r, 16 * k + 16), kBlock));
+    return make_int2(0, div_up(tile_key_limit(p, rp, r, kPrefillRows * (k + 1)), kPrefillKeys));
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __shared__ int bin_count[kSizeBins];
     __shared__ int bin_cursor[kSizeBins];
+    __shared__ int pbin_count[kSizeBins];
+    __shared__ int pbin_cursor[kSizeBins];
     __shared__ unsigned long long total_pages;
     __shared__ unsigned long long prow_need;
     __shared__ int bad;
@@ -198,10 +187,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     int2 *req = reinterpret_cast<int2 *>(p.ws + p.lay.off_req);
     int2 *tok = reinterpret_cast<int2 *>(p.ws + p.lay.off_tok);
     int4 *chunks = reinterpret_cast<int4 *>(p.ws + p.lay.off_chunks);
+    int4 *ptiles = reinterpret_cast<int4 *>(p.ws + p.lay.off_ptiles);
     const int tid = threadIdx.x;
     const int G = p.num_q_heads / p.num_kv_heads;
 
-    for (int i = tid; i < kSizeBins; i += blockDim.x) bin_count[i] = 0;
+    for (int i = tid; i < kSizeBins; i += blockDim.x) {
+        bin_count[i] = 0;
+        pbin_count[i] = 0;
+    }
     if (tid == 0) {
         total_pages = 0;
         prow_need = 0;
@@ -238,42 +231,52 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             atomicExch(&bad, 1);
             continue;
         }
-        if (rp.split && rp.n_chunks > 1)
+        if (rp.mode == 0 && rp.n_chunks > 1)
             prows += (unsigned long long)(p.qsl[r + 1] - p.qsl[r]) * p.num_q_heads * rp.n_chunks;
         for (int k = 0; k < rp.n_chunks; ++k) {
             const int2 pg = chunk_pages(p, rp, r, k);
-            atomicAdd(&bin_count[min(pg.y - pg.x, kSizeBins - 1)], 1);
+            atomicAdd(rp.mode == 2 ? &pbin_count[min(pg.y, kSizeBins - 1)]
+                                   : &bin_count[min(pg.y - pg.x, kSizeBins - 1)], 1);
         }
     }
     atomicAdd(&prow_need, prows);
     __syncthreads();
     if (tid == 0) {
-        int acc = 0;                                  // largest chunks first
+        int acc = 0, pacc = 0;                        // largest first
         for (int b = kSizeBins - 1; b >= 0; --b) {
             bin_cursor[b] = acc;
             acc += bin_count[b];
+            pbin_cursor[b] = pacc;
+            pacc += pbin_count[b];
         }
-        const bool fits = acc <= p.lay.max_chunks && prow_need <= (unsigned long long)p.lay.max_prow;
+        const bool fits = acc <= p.lay.max_chunks && pacc <= p.lay.max_ptiles &&
+                          prow_need <= (unsigned long long)p.lay.max_prow;
         hdr->n_chunks = fits ? acc : 0;
+        hdr->n_ptiles = fits ? pacc : 0;
         if (!fits) bad = 2;
     }
     __syncthreads();
     const bool overflow = bad == 2;
 
-    // pass 3: emit chunks, request info and token owners
+    // pass 3: emit chunks and tiles, request info and token owners
     for (int r = tid; r < p.num_seqs; r += blockDim.x) {
         const ReqPlan rp = plan_request(p, r, pages_per_split);
         int2 info = make_int2(rp.valid && !overflow ? 1 : 0, 0);
         if (rp.valid && !overflow) {
-            if (rp.split && rp.n_chunks > 1) {
+            if (rp.mode == 0 && rp.n_chunks > 1) {
                 const int rows = (p.qsl[r + 1] - p.qsl[r]) * p.num_q_heads * rp.n_chunks;
                 const int base = atomicAdd(&prow_cursor, rows);
                 info = make_int2(rp.n_chunks, base);
             }
             for (int k = 0; k < rp.n_chunks; ++k) {
                 const int2 pg = chunk_pages(p, rp, r, k);
-                const int pos = atomicAdd(&bin_cursor[min(pg.y - pg.x, kSizeBins - 1)], 1);
-                chunks[pos] = make_int4(r, k, pg.x, pg.y);
+                if (rp.mode == 2) {
+                    const int pos = atomicAdd(&pbin_cursor[min(pg.y, kSizeBins - 1)], 1);
+                    ptiles[pos] = make_int4(r, k, pg.y, 0);
+                } else {
+                    const int pos = atomicAdd(&bin_cursor[min(pg.y - pg.x, kSizeBins - 1)], 1);
+                    chunks[pos] = make_int4(r, k, pg.x, pg.y);
+                }
             }
             for (int t = p.qsl[r]; t < p.qsl[r + 1]; ++t) tok[t] = make_int2(r, t - p.qsl[r]);
         }
@@ -282,7 +285,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __syncthreads();
     if (tid == 0) {
         hdr->status = bad ? PKV_ERR_DEVICE_METADATA : PKV_OK;
-        if (prow_cursor > p.lay.max_prow) hdr->status = PKV_ERR_DEVICE_METADATA;
         hdr->magic = kMagic;
         hdr->num_tokens = p.num_tokens;
         hdr->num_q_heads = p.num_q_heads;
@@ -292,9 +294,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         hdr->off_req = p.lay.off_req;
         hdr->off_tok = p.lay.off_tok;
         hdr->off_chunks = p.lay.off_chunks;
+        hdr->off_ptiles = p.lay.off_ptiles;
         hdr->off_part_lse = p.lay.off_part_lse;
         hdr->off_part_o = p.lay.off_part_o;
         hdr->max_chunks = p.lay.max_chunks;
+        hdr->max_ptiles = p.lay.max_ptiles;
         hdr->max_prow = p.lay.max_prow;
         hdr->prow_used = prow_cursor;
     }
@@ -780,6 +784,10 @@ extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_
     pp.max_seq_len = max_seq_len;
     pp.num_splits = num_splits;
     pp.total_warps = static_cast<int32_t>(grid * nw);
+    const bool prefill_ok = prefill_supported(num_q_heads, num_kv_heads, head_size);
+    const int G = num_q_heads / num_kv_heads;
+    const bool may_prefill = prefill_ok && static_cast<int64_t>(max_query_len) * G > kDecodeTileMaxRows;
+    pp.prefill_ok = prefill_ok ? 1 : 0;
     pp.lay = lay;
     plan_kernel<<<1, kPlanThreads, 0, st>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
@@ -798,11 +806,26 @@ extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_
     ap.num_blocks = num_blocks;
     ap.scale_log2 = scale * 1.4426950408889634f;
     ap.ws = static_cast<uint8_t *>(workspace);
-    if (head_size == 64)
-        return launch_decode<64, DecodeTiling<64>::NW, DecodeTiling<64>::DEPTH>(map, ap, static_cast<int>(grid), dev,
-                                                                                st);
-    return launch_decode<128, DecodeTiling<128>::NW, DecodeTiling<128>::DEPTH>(map, ap, static_cast<int>(grid), dev,
-                                                                                  st);
+    rc = head_size == 64
+             ? launch_decode<64, DecodeTiling<64>::NW, DecodeTiling<64>::DEPTH>(map, ap, static_cast<int>(grid), dev, st)
+             : launch_decode<128, DecodeTiling<128>::NW, DecodeTiling<128>::DEPTH>(map, ap, static_cast<int>(grid), dev,
+                                                                                   st);
+    if (rc || !may_prefill) return rc;
+    PrefillParams fp;
+    fp.out = ap.out;
+    fp.block_tables = block_tables;
+    fp.max_blocks_per_seq = max_blocks_per_seq;
+    fp.seq_lens = seq_lens;
+    fp.qsl = query_start_loc;
+    fp.num_q_heads = num_q_heads;
+    fp.num_kv_heads = num_kv_heads;
+    fp.G = G;
+    fp.num_blocks = num_blocks;
+    fp.scale_log2 = ap.scale_log2;
+    fp.lo_tiles = 0;
+    fp.ws = ap.ws;
+    return launch_prefill(fp, query, query_token_stride, num_tokens, kv_cache, num_blocks, head_size,
+                          lay.max_ptiles * num_kv_heads, dev, st);
 }
 
 extern "C" int pkv_paged_attn_combine(void *out, const void *workspace, size_t workspace_bytes, int32_t num_tokens,

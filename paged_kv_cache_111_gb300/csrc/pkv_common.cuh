@@ -2,8 +2,9 @@
 //
 // Inline PTX for the pieces CUDA C++ does not expose directly: mbarriers,
 // TMA tensor loads, ldmatrix, and the bf16 mma.sync tile used by the decode
-// kernel.  Every wait on an asynchronous copy is bounded: past the limit the
-// caller records PKV_ERR_DEVICE_TIMEOUT and stops instead of spinning.
+// kernel.  Every wait on an asynchronous copy or MMA is bounded in wall-clock
+// time: past the limit the caller records PKV_ERR_DEVICE_TIMEOUT and stops
+// instead of spinning.
 #pragma once
 
 #include <cuda.h>
@@ -16,7 +17,7 @@
 namespace pkv {
 
 constexpr int kBlock = PKV_BLOCK_SIZE;       // tokens per cache block (page)
-constexpr uint32_t kWaitLimit = 1u << 22;    // polls of one mbarrier before giving up
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;   // one mbarrier wait gives up after 200 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,11 +58,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase of the given parity; false when the limit ran out.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase of the given parity; false once kWaitLimitNs of
+// wall-clock time has passed without the phase completing.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // ---- TMA ----------------------------------------------------------------------

@@ -1,0 +1,489 @@
+// Prefill-chunk paged attention on the 5th-generation tensor cores (tcgen05).
+//
+// The same computation as the decode path ("continuous batching and
+// PagedAttention" tutorial, section 3.6: loop over the request's blocks
+// through its block table, accumulate softmax(QK^T)V), for requests whose
+// rows are many: a chunk of a chunked prefill ("Inside vLLM: Anatomy of a
+// High-Throughput LLM Inference System", chunked prefill; "vLLM internals:
+// managing the KV cache like an OS manages memory", section 3.2) attends
+// causally, query i of the chunk seeing keys 0 .. context + i.
+//
+// One CTA computes one 128-row tile for one kv head.  Rows are
+// (query token, q head of the GQA group) pairs, so one K/V tile in shared
+// memory serves every q head of the group.  Per 128-key KV tile:
+//   S = Q K^T      tcgen05.mma, A = Q and B = K from shared memory (K-major,
+//                  128-byte swizzle), D in tensor memory (two S buffers)
+//   softmax        one thread per row reads its S row from tensor memory,
+//                  masks, keeps a running max (rescaling O in tensor memory
+//                  only when the max grows by more than 2^8) and writes P
+//                  (bf16) to shared memory
+//   O += P V       tcgen05.mma, A = P (K-major), B = V (MN-major), D = O in
+//                  tensor memory
+// Warp roles: warp 0 loads (TMA: Q once, K and V pages through the block
+// table into a two-stage ring), warp 1 issues the MMAs, warp 2 owns the
+// tensor-memory allocation, warps 4-7 do softmax and the epilogue.
+//
+// When any row of the tile puts a large share of its weight on few keys of
+// a KV tile (rows with few visible keys, or a peaked softmax), that tile's P
+// also enters P V as its bf16 remainder (a second MMA), keeping ~16 bits per
+// weight; other tiles' weights are each small and bf16 P is enough.  V rows past the sequence end in
+// its last page are zeroed before P V, so NaN in unwritten cache slots never
+// meets a zero weight.  Every wait is bounded.
+#include <mutex>
+
+#include "attn_internal.cuh"
+#include "tc_common.cuh"
+
+namespace pkv {
+
+template <int HD>
+struct PrefillCfg {
+    static constexpr int kHalves = HD / 64;
+    static constexpr int kHalfQ = kPrefillRows * 128;       // bytes of one 64-column half of a 128-row tile
+    static constexpr int kQBytes = kHalves * kHalfQ;
+    static constexpr int kKVBytes = kHalves * kPrefillKeys * 128;   // one K (or V) tile
+    static constexpr int kPBytes = 2 * kPrefillRows * 128;  // 128 x 128 bf16
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kOffV = kOffK + 2 * kKVBytes;
+    static constexpr int kOffP = kOffV + 2 * kKVBytes;
+    static constexpr int kOffBar = kOffP + kPBytes;
+    static constexpr int kSmem = kOffBar + 256 + 1024;      // + barriers + alignment slack
+    static constexpr uint32_t kTmemCols = 512;              // S0 | S1 | O
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+};
+
+enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kVFull0, kVFull1, kKVEmpty0, kKVEmpty1, kSFull0, kSFull1,
+                  kSFree0, kSFree1, kPFull, kODone, kVFix, kVote, kNumBars };
+
+// A row whose weights in a KV tile are concentrated (sum of squared weights
+// of the tile above this fraction of the squared running sum) needs P's bf16
+// remainder in P V: bf16 rounding of a few large weights would otherwise
+// exceed the output tolerance.
+constexpr float kLoConcentration = 0.01f;
+
+// Bounded wait shared by every role; on timeout records the error and
+// reports it so the role can stop.
+__device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
+    if (mbar_wait_bounded(bar, parity)) return true;
+    set_status(status, PKV_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(256, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
+                   const PrefillParams p) {
+    using Cfg = PrefillCfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    volatile uint32_t *votes = tmem_slot + 4;          // [2 tiles in flight][4 softmax warps]
+    const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
+    const uint32_t sK = smem_u32(smem + Cfg::kOffK);
+    const uint32_t sV = smem_u32(smem + Cfg::kOffV);
+    const uint32_t sP = smem_u32(smem + Cfg::kOffP);
+
+    const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
+    int32_t *status = reinterpret_cast<int32_t *>(p.ws);
+    const int n_items = hdr->n_ptiles * p.num_kv_heads;
+    const int item = blockIdx.x;
+    if (item >= n_items) return;                       // uniform over the CTA
+    const int4 tile = reinterpret_cast<const int4 *>(p.ws + hdr->off_ptiles)[item / p.num_kv_heads];
+    const int g = item % p.num_kv_heads;
+    const int r = tile.x, qt = tile.y, n_kv = tile.z;
+    const int L = p.seq_lens[r];
+    const int qs = p.qsl[r];
+    const int qlen = p.qsl[r + 1] - qs;
+    const int ctx = L - qlen;
+    const int G = p.G;
+    const int rows_total = qlen * G;
+    const int row0 = qt * kPrefillRows;                // first request row of the tile
+    const int n_pages = (L + kBlock - 1) / kBlock;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kNumBars; ++b)
+            mbar_init(&bars[b], (b == kSFree0 || b == kSFree1 || b == kPFull || b == kVote) ? 4 : 1);
+        tma_prefetch_desc(&q_map);
+        tma_prefetch_desc(&kv_map);
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    fence_barrier_init();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // the KV tile holding the sequence's last key, when that page is partial
+    const int end_tile = (L % kBlock) ? (L - 1) / kPrefillKeys : -1;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        bool ok = true;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[kQFull], Cfg::kQBytes);
+            for (int h = 0; h < Cfg::kHalves; ++h)
+                tma_load_3d(smem + Cfg::kOffQ + h * Cfg::kHalfQ, &q_map, &bars[kQFull], h * 64, g * G,
+                            qs + row0 / G);
+        }
+        const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks_per_seq;
+        for (int j = 0; j < n_kv && ok; ++j) {
+            const int st = j & 1;
+            if (j >= 2) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKVEmpty0 + st], ((j - 2) >> 1) & 1, status));
+            if (!ok) break;
+            const int page = j * (kPrefillKeys / kBlock) + lane;
+            // pages past the sequence load as zeros (block -1 is outside the tensor map)
+            const int blk = (lane < kPrefillKeys / kBlock && page < n_pages) ? __ldg(bt + page) : -1;
+            if (lane < kPrefillKeys / kBlock && page < n_pages && (blk < 0 || blk >= p.num_blocks))
+                set_status(status, PKV_ERR_DEVICE_INDEX);   // loaded as zeros by the bounded TMA, reported
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[kKFull0 + st], Cfg::kKVBytes);
+                mbar_arrive_expect_tx(&bars[kVFull0 + st], Cfg::kKVBytes);
+            }
+#pragma unroll 1
+            for (int pg = 0; pg < kPrefillKeys / kBlock; ++pg) {
+                const int b = __shfl_sync(0xffffffffu, blk, pg);
+                if (lane == 0) {
+                    for (int h = 0; h < Cfg::kHalves; ++h) {
+                        uint8_t *kd = smem + Cfg::kOffK + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048;
+                        uint8_t *vd = smem + Cfg::kOffV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048;
+                        tma_load_5d(kd, &kv_map, &bars[kKFull0 + st], h * 64, 0, 0, g, b);
+                        tma_load_5d(vd, &kv_map, &bars[kVFull0 + st], h * 64, 0, 1, g, b);
+                    }
+                }
+            }
+            if (j == end_tile) {
+                // zero V rows past the sequence end in its last (partial) page
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kVFull0 + st], (j >> 1) & 1, status));
+                if (!ok) break;
+                const int lp = (L - 1) / kBlock - j * (kPrefillKeys / kBlock);   // page within the tile
+                const int first = L % kBlock;
+                const int nrows = kBlock - first;
+                for (int e = lane; e < Cfg::kHalves * nrows * 8; e += 32) {
+                    const int h = e / (nrows * 8);
+                    const int rem = e % (nrows * 8);
+                    const int row = lp * kBlock + first + rem / 8;
+                    const uint32_t a = sV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + row * 128 + (rem % 8) * 16;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kVFix]);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillRows, kPrefillKeys, 0, 0);
+            constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillRows, HD, 0, 1);
+            bool ok = pf_wait(&bars[kQFull], 0, status);
+            uint32_t p_cnt = 0;
+            auto issue_s = [&](int j) {
+                const int st = j & 1;
+                const uint32_t d = tmem + (st ? Cfg::kColS1 : Cfg::kColS0);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (kPrefillRows * 128) + (kk & 3) * 32;
+                    const uint64_t a = smem_desc_sw128(sQ + off, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(sK + st * Cfg::kKVBytes + (kk >> 2) * (kPrefillKeys * 128) +
+                                                           (kk & 3) * 32,
+                                                       16, 1024);
+                    umma_bf16_ss(d, a, b, kIdescS, kk > 0);
+                }
+                umma_commit(&bars[kSFull0 + st]);
+            };
+            auto issue_pv = [&](int j, uint32_t accumulate) {
+                const int st = j & 1;
+#pragma unroll
+                for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
+                    const uint64_t a = smem_desc_sw128(sP + (kk >> 2) * (kPrefillRows * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(sV + st * Cfg::kKVBytes + kk * 2048, kPrefillKeys * 128, 1024);
+                    umma_bf16_ss(tmem + Cfg::kColO, a, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(&bars[kODone]);
+            };
+            if (ok) ok = pf_wait(&bars[kKFull0], 0, status);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int st = j & 1;
+                if (j + 1 < n_kv) {
+                    const int s1 = (j + 1) & 1;
+                    ok = pf_wait(&bars[kKFull0 + s1], ((j + 1) >> 1) & 1, status);
+                    if (ok && j + 1 >= 2) ok = pf_wait(&bars[kSFree0 + s1], ((j - 1) >> 1) & 1, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(j + 1);
+                }
+                ok = pf_wait(&bars[kPFull], p_cnt & 1, status);
+                ++p_cnt;
+                if (ok) ok = pf_wait(&bars[kVFull0 + st], (j >> 1) & 1, status);
+                if (ok && j == end_tile) ok = pf_wait(&bars[kVFix], 0, status);
+                if (!ok) break;
+                tc_fence_after();
+                const bool lo = (votes[(j & 1) * 4 + 0] | votes[(j & 1) * 4 + 1] | votes[(j & 1) * 4 + 2] |
+                                 votes[(j & 1) * 4 + 3]) != 0u;
+                issue_pv(j, j > 0);
+                if (lo) {
+                    ok = pf_wait(&bars[kPFull], p_cnt & 1, status);
+                    ++p_cnt;
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(j, 1);
+                }
+                umma_commit(&bars[kKVEmpty0 + st]);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------- softmax + epilogue: thread = row ----------------
+        const int row = threadIdx.x - 128;
+        const int lane_base = (warp - 4) * 32;
+        const int rrow = row0 + row;                       // request row
+        const bool valid = rrow < rows_total;
+        const int lim = valid ? ctx + rrow / G + 1 : 0;    // keys [0, lim) visible
+        const float NEG_INF = -__int_as_float(0x7f800000);
+        float m_ref = NEG_INF, l = 0.f;
+        uint32_t o_cnt = 0;
+        bool ok = true;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
+
+        for (int j = 0; j < n_kv && ok; ++j) {
+            const int sb = j & 1;
+            ok = __all_sync(0xffffffffu, pf_wait(&bars[kSFull0 + sb], (j >> 1) & 1, status));
+            if (!ok) break;
+            tc_fence_after();
+            float x[kPrefillKeys];
+#pragma unroll
+            for (int c = 0; c < kPrefillKeys / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(trow + (sb ? Cfg::kColS1 : Cfg::kColS0) + c * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kSFree0 + sb]);
+
+            const int key0 = j * kPrefillKeys;
+            float mx = NEG_INF;
+#pragma unroll
+            for (int c = 0; c < kPrefillKeys; ++c) {
+                x[c] = (key0 + c < lim) ? x[c] * p.scale_log2 : NEG_INF;
+                mx = fmaxf(mx, x[c]);
+            }
+            const float m_new = fmaxf(m_ref, mx);
+            // P V of the previous tile must be finished before O or the P buffer is touched
+            if (j > 0) {
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone], o_cnt & 1, status));
+                ++o_cnt;
+                if (!ok) break;
+                tc_fence_after();
+            }
+            // a row moves its reference max only when the max grew by more than
+            // 2^8 (its O is then rescaled); tensor-memory loads and stores are
+            // warp-wide, so the warp rescales when any of its rows needs it
+            const bool first = m_ref == NEG_INF;           // O holds nothing yet for this row
+            const bool grow = !first && m_new > m_ref + 8.f;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
+                l *= alpha;
+#pragma unroll
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(trow + Cfg::kColO + c * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                    tmem_st32(trow + Cfg::kColO + c * 32, v);
+                }
+                tmem_st_wait();
+            }
+            if (first || grow) m_ref = m_new;
+            const float ref = (m_ref == NEG_INF) ? 0.f : m_ref;
+            float psum = 0.f, psq = 0.f;
+#pragma unroll
+            for (int c = 0; c < kPrefillKeys; ++c) {
+                x[c] = exp2f(x[c] - ref);
+                psum += x[c];
+                psq += x[c] * x[c];
+            }
+            l += psum;
+            // CTA-wide vote: does any row need the remainder of P in this tile?
+            const bool need = j < p.lo_tiles || psq > kLoConcentration * l * l;
+            const uint32_t wvote = __any_sync(0xffffffffu, need) ? 1u : 0u;
+            if (lane == 0) {
+                votes[(j & 1) * 4 + (warp - 4)] = wvote;
+                mbar_arrive(&bars[kVote]);
+            }
+            ok = __all_sync(0xffffffffu, pf_wait(&bars[kVote], j & 1, status));
+            if (!ok) break;
+            const bool lo = (votes[(j & 1) * 4 + 0] | votes[(j & 1) * 4 + 1] | votes[(j & 1) * 4 + 2] |
+                             votes[(j & 1) * 4 + 3]) != 0u;
+            // P (bf16) into the K-major, 128-byte-swizzled A tile: row `row`,
+            // keys in two 64-key halves, 16-byte chunk c at c ^ (row & 7)
+#pragma unroll
+            for (int c = 0; c < kPrefillKeys / 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(x[c * 8 + 2 * e], x[c * 8 + 2 * e + 1]);
+                const uint32_t a = sP + (c >> 3) * (kPrefillRows * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                             "r"(w[3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kPFull]);
+            if (lo) {
+                // the remainder of P once the first P V has read the buffer
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone], o_cnt & 1, status));
+                ++o_cnt;
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < kPrefillKeys / 8; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a0 = x[c * 8 + 2 * e], a1 = x[c * 8 + 2 * e + 1];
+                        const float2 hb = __bfloat1622float2(__floats2bfloat162_rn(a0, a1));
+                        w[e] = pack_bf16x2(a0 - hb.x, a1 - hb.y);
+                    }
+                    const uint32_t a = sP + (c >> 3) * (kPrefillRows * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                                 "r"(w[3])
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kPFull]);
+            }
+        }
+        if (ok) {
+            // epilogue: the last P V, then O / l to bf16
+            ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone], o_cnt & 1, status));
+            ++o_cnt;
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int i = rrow / G, hh = rrow % G;
+            __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(qs + i) * p.num_q_heads + g * G + hh) * HD;
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(trow + Cfg::kColO + c * 32, v);
+                tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(v[e + 0]) * inv, __uint_as_float(v[e + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
+                    }
+                }
+            }
+        }
+    }
+
+    // teardown: every role is done with tensor memory
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+// ---- host side --------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+template <int HD>
+static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &qm, const CUtensorMap &kvm, int64_t grid,
+                             int dev, cudaStream_t stream) {
+    using Cfg = PrefillCfg<HD>;
+    static std::mutex mu;
+    static uint64_t done_mask = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+        if (!bit || !(done_mask & bit)) {
+            if (cudaFuncSetAttribute(prefill_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem) !=
+                cudaSuccess)
+                return PKV_ERR_CUDA;
+            done_mask |= bit;
+        }
+    }
+    prefill_kernel<HD><<<static_cast<unsigned>(grid), 256, Cfg::kSmem, stream>>>(qm, kvm, p);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
+                   const void *kv_cache, int64_t num_blocks, int32_t head_size, int64_t grid, int dev,
+                   cudaStream_t stream) {
+    if (grid <= 0) return PKV_OK;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PKV_ERR_CUDA;
+    const int G = p.G;
+    // query as {head_size, q heads, tokens}; box = one tile: 64 columns x G heads x 128/G tokens
+    CUtensorMap qm, kvm;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_size), static_cast<cuuint64_t>(p.num_q_heads),
+                                    static_cast<cuuint64_t>(num_tokens)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_size) * 2, static_cast<cuuint64_t>(q_stride) * 2};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kPrefillRows / G)};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(query), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PKV_ERR_CUDA;
+    }
+    {
+        // cache as {head_size, 16, 2, kv heads, blocks}; box = K or V rows of one page, 64 columns
+        const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2,
+                                    static_cast<cuuint64_t>(p.num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
+        const cuuint64_t row = static_cast<cuuint64_t>(head_size) * 2;
+        const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * p.num_kv_heads};
+        const cuuint32_t box[5] = {64, kBlock, 1, 1, 1};
+        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+        if (enc(&kvm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PKV_ERR_CUDA;
+    }
+    if (head_size == 64) return launch_prefill_hd<64>(p, qm, kvm, grid, dev, stream);
+    return launch_prefill_hd<128>(p, qm, kvm, grid, dev, stream);
+}
+
+}  // namespace pkv

@@ -72,6 +72,26 @@ def test_edge_cases(case):
     compare(custom(reqs, H, Hkv, d, seed=zlib.crc32(name.encode()) % 1000), what=name)
 
 
+PREFILL = [
+    # requests whose rows (query tokens x GQA group) exceed 64 run on the tcgen05 prefill kernel
+    ("mha d128 c=0 q=300", [(0, 300)], 4, 4, 128, None),
+    ("gqa4 d128 long context", [(1000, 200), (17, 1)], 16, 4, 128, None),
+    ("gqa8 d64 mid-block", [(37, 90), (200, 70)], 16, 2, 64, None),
+    ("gqa2 d128 ragged tail", [(5, 129), (0, 33), (250, 1)], 8, 4, 128, None),
+    ("mha d64 partial last page", [(100, 150)], 2, 2, 64, None),
+    ("gqa16 d128", [(64, 40), (3, 10)], 32, 2, 128, None),
+    ("peaked softmax (scale 1.0)", [(300, 260), (50, 1)], 8, 2, 128, 1.0),
+    ("long chunk 4096 context", [(4096, 256)], 8, 1, 128, None),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL, ids=[c[0] for c in PREFILL])
+def test_prefill_tensor_core_path(case):
+    name, reqs, H, Hkv, d, scale = case
+    step = custom(reqs, H, Hkv, d, seed=zlib.crc32(name.encode()) % 1000, scale=scale)
+    compare(step, what=name)
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 32])
 def test_forced_split_counts_merge_to_the_same_result(splits):
     step = custom([(700, 1), (33, 1), (1500, 1), (0, 1), (255, 1)], 16, 2, 128, seed=splits)
