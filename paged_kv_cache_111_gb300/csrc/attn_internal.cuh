@@ -23,7 +23,7 @@ struct WsHeader {
     int32_t pages_per_split;
     int32_t n_ptiles;        // prefill-kernel tiles
     int32_t pad_;
-    int64_t off_req;         // int2 [num_seqs]: {splits, partial row base}
+    int64_t off_req;         // int4 [num_seqs]: {splits (0: refused), partial row base, first chunk, chunks}
     int64_t off_tok;         // int2 [num_tokens]: {request, index in request} (-1 if none)
     int64_t off_chunks;      // int4 [max_chunks]: {request, split or tile, page begin, page end}
     int64_t off_ptiles;      // int4 [max_ptiles]: {request, q tile, kv tiles, 0}

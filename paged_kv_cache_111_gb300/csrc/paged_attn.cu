@@ -60,7 +60,7 @@ static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_quer
     w.max_ptiles = (num_tokens * G + kPrefillRows - 1) / kPrefillRows + num_seqs;
     int64_t off = 256;
     w.off_req = off;
-    off = align256(off + 8 * num_seqs);
+    off = align256(off + 16 * num_seqs);
     w.off_tok = off;
     off = align256(off + 8 * num_tokens);
     w.off_chunks = off;
@@ -112,6 +112,7 @@ __device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
 // tensor-core prefill kernel.
 struct ReqPlan {
     int valid;        // metadata consistent
+    int q, ctx;       // query tokens, context
     int rows;         // q_r * G
     int mode;
     int n_chunks;     // decode-kernel chunks (modes 0, 1) or prefill tiles (mode 2)
@@ -120,7 +121,7 @@ struct ReqPlan {
 };
 
 __device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split) {
-    ReqPlan rp{0, 0, 0, 0, 0, 0};
+    ReqPlan rp{0, 0, 0, 0, 0, 0, 0, 0};
     const int G = p.num_q_heads / p.num_kv_heads;
     const int q0 = p.qsl[r], q1 = p.qsl[r + 1];
     const int q = q1 - q0;
@@ -129,6 +130,8 @@ __device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split)
         div_up(L, kBlock) > p.max_blocks_per_seq)
         return rp;
     rp.valid = 1;
+    rp.q = q;
+    rp.ctx = L - q;
     rp.rows = q * G;
     if (rp.rows == 0) return rp;
     if (rp.rows <= 16) {
@@ -153,134 +156,246 @@ __device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split)
     return rp;
 }
 
-// Keys 0 .. lim-1 visible to the last row of a tile ending before row `row_end`.
-__device__ __forceinline__ int tile_key_limit(const PlanParams &p, const ReqPlan &rp, int r, int row_end) {
-    const int G = p.num_q_heads / p.num_kv_heads;
-    const int q = p.qsl[r + 1] - p.qsl[r];
-    const int ctx = p.seq_lens[r] - q;
-    const int last_row = min(rp.rows, row_end) - 1;
-    return ctx + last_row / G + 1;
-}
-
-// Mode 0/1: page range of chunk k.  Mode 2: {0, KV tiles} of tile k.
-__device__ __forceinline__ int2 chunk_pages(const PlanParams &p, const ReqPlan &rp, int r, int k) {
+// Mode 0/1: page range of chunk k.  Mode 2: {0, KV tiles} of tile k.  A tile
+// ending before request row `row_end` sees keys 0 .. ctx + last_row / G.
+__device__ __forceinline__ int2 chunk_pages(const ReqPlan &rp, int G, int k) {
     if (rp.mode == 0) {
         const int b = k * rp.per_split;
         return make_int2(b, min(rp.pages, b + rp.per_split));
     }
-    if (rp.mode == 1) return make_int2(0, div_up(tile_key_limit(p, rp, r, 16 * k + 16), kBlock));
-    return make_int2(0, div_up(tile_key_limit(p, rp, r, kPrefillRows * (k + 1)), kPrefillKeys));
+    const int row_end = rp.mode == 1 ? 16 * k + 16 : kPrefillRows * (k + 1);
+    const int lim = rp.ctx + (min(rp.rows, row_end) - 1) / G + 1;
+    if (rp.mode == 1) return make_int2(0, div_up(lim, kBlock));
+    return make_int2(0, div_up(lim, kPrefillKeys));
 }
 
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Exclusive scan of `count[b]` in descending bin order into `cursor[b]`, by
+// one warp (8 bins per lane); returns the total.
+__device__ int scan_bins_desc(const int *count, int *cursor, int lane) {
+    int local[8];
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        local[e] = count[kSizeBins - 1 - (lane * 8 + e)];
+        sum += local[e];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int acc = incl - sum;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        cursor[kSizeBins - 1 - (lane * 8 + e)] = acc;
+        acc += local[e];
+    }
+    return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// Warp-aggregated shared-memory atomicAdd of 1 per lane on counter[bin]:
+// returns this lane's slot (lanes sharing a bin get consecutive slots).
+__device__ __forceinline__ int agg_inc(int *counter, int bin) {
+    const unsigned active = __activemask();
+    const unsigned peers = __match_any_sync(active, bin);
+    const int leader = __ffs(peers) - 1;
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(&counter[bin], __popc(peers));
+    base = __shfl_sync(peers, base, leader);
+    return base + __popc(peers & ((1u << lane) - 1u));
+}
+
+// Block-wide exclusive scan of a pair of non-negative counts (one pair per
+// thread); returns this thread's prefix and writes the totals to *total.
+__device__ int2 block_scan2(int a, int b, int2 *warp_tot, int2 *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int va = __shfl_up_sync(0xffffffffu, ia, o);
+        const int vb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) {
+            ia += va;
+            ib += vb;
+        }
+    }
+    if (lane == 31) warp_tot[warp] = make_int2(ia, ib);
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int2 w = lane < nw ? warp_tot[lane] : make_int2(0, 0);
+        int wa = w.x, wb = w.y;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int va = __shfl_up_sync(0xffffffffu, wa, o);
+            const int vb = __shfl_up_sync(0xffffffffu, wb, o);
+            if (lane >= o) {
+                wa += va;
+                wb += vb;
+            }
+        }
+        if (lane < nw) warp_tot[lane] = make_int2(wa - w.x, wb - w.y);   // exclusive warp prefix
+        if (lane == nw - 1) *total = make_int2(wa, wb);
+    }
+    __syncthreads();
+    const int2 wp = warp_tot[warp];
+    return make_int2(wp.x + ia - a, wp.y + ib - b);
+}
+
+// One CTA plans the call: checks every request, splits decode rows along
+// keys, cuts long requests into tiles, and lists the work largest first
+// (counting sort by size) so the persistent decode kernel's fixed item order
+// balances its warps.  Per-request and per-chunk passes run in parallel over
+// requests and over chunks.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __shared__ int bin_count[kSizeBins];
     __shared__ int bin_cursor[kSizeBins];
     __shared__ int pbin_count[kSizeBins];
     __shared__ int pbin_cursor[kSizeBins];
+    __shared__ int2 warp_tot[kPlanThreads / 32];
+    __shared__ int2 totals;
     __shared__ unsigned long long total_pages;
-    __shared__ unsigned long long prow_need;
     __shared__ int bad;
-    __shared__ int prow_cursor;
     __shared__ int pages_per_split;
 
     WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
-    int2 *req = reinterpret_cast<int2 *>(p.ws + p.lay.off_req);
+    int4 *req = reinterpret_cast<int4 *>(p.ws + p.lay.off_req);
     int2 *tok = reinterpret_cast<int2 *>(p.ws + p.lay.off_tok);
     int4 *chunks = reinterpret_cast<int4 *>(p.ws + p.lay.off_chunks);
     int4 *ptiles = reinterpret_cast<int4 *>(p.ws + p.lay.off_ptiles);
     const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
     const int G = p.num_q_heads / p.num_kv_heads;
 
-    for (int i = tid; i < kSizeBins; i += blockDim.x) {
+    for (int i = tid; i < kSizeBins; i += nthr) {
         bin_count[i] = 0;
         pbin_count[i] = 0;
     }
     if (tid == 0) {
         total_pages = 0;
-        prow_need = 0;
-        bad = 0;
-        prow_cursor = 0;
+        bad = p.qsl[0] != 0;
     }
-    for (int t = tid; t < p.num_tokens; t += blockDim.x) tok[t] = make_int2(-1, -1);
+    for (int t = tid; t < p.num_tokens; t += nthr) tok[t] = make_int2(-1, -1);
     __syncthreads();
 
     // pass 1: total key pages of split requests (sets the automatic split size)
-    if (p.qsl[0] != 0 && tid == 0) bad = 1;
     unsigned long long mine = 0;
-    for (int r = tid; r < p.num_seqs; r += blockDim.x) {
+    for (int r = tid; r < p.num_seqs; r += nthr) {
         const int q = p.qsl[r + 1] - p.qsl[r];
         const int L = p.seq_lens[r];
         if (q > 0 && q * G <= 16 && L >= q) mine += (unsigned long long)div_up(L, kBlock);
     }
-    atomicAdd(&total_pages, mine);
+    mine = warp_sum_u64(mine);
+    if ((tid & 31) == 0 && mine) atomicAdd(&total_pages, mine);
     __syncthreads();
     if (tid == 0) {
         // about 8 chunks per warp of the decode grid, 4..64 pages each
         const unsigned long long work = total_pages * (unsigned long long)p.num_kv_heads;
         const unsigned long long target = 8ull * (unsigned long long)max(p.total_warps, 1);
-        unsigned long long per = (work + target - 1) / target;
+        const unsigned long long per = (work + target - 1) / target;
         pages_per_split = (int)min(64ull, max(4ull, per));
     }
     __syncthreads();
+    const int pps = pages_per_split;
 
-    // pass 2: count chunks per size bin, and the partial rows split requests need
-    unsigned long long prows = 0;
-    for (int r = tid; r < p.num_seqs; r += blockDim.x) {
-        const ReqPlan rp = plan_request(p, r, pages_per_split);
+    // pass 2: per request, its chunk count and partial rows; each thread owns
+    // a contiguous range of requests so one block scan gives every base
+    const int per_thr = div_up(max(p.num_seqs, 1), nthr);
+    const int r_begin = min(p.num_seqs, tid * per_thr), r_end = min(p.num_seqs, r_begin + per_thr);
+    int my_chunks = 0, my_prows = 0;
+    for (int r = r_begin; r < r_end; ++r) {
+        const ReqPlan rp = plan_request(p, r, pps);
         if (!rp.valid) {
-            atomicExch(&bad, 1);
+            bad = 1;
             continue;
         }
-        if (rp.mode == 0 && rp.n_chunks > 1)
-            prows += (unsigned long long)(p.qsl[r + 1] - p.qsl[r]) * p.num_q_heads * rp.n_chunks;
-        for (int k = 0; k < rp.n_chunks; ++k) {
-            const int2 pg = chunk_pages(p, rp, r, k);
-            atomicAdd(rp.mode == 2 ? &pbin_count[min(pg.y, kSizeBins - 1)]
-                                   : &bin_count[min(pg.y - pg.x, kSizeBins - 1)], 1);
+        my_chunks += rp.n_chunks;
+        if (rp.mode == 0 && rp.n_chunks > 1) my_prows += rp.q * p.num_q_heads * rp.n_chunks;
+    }
+    const int2 pre = block_scan2(my_chunks, my_prows, warp_tot, &totals);
+    const int n_total = totals.x;
+    const bool fits = n_total <= p.lay.max_chunks + p.lay.max_ptiles && totals.y <= p.lay.max_prow;
+    {
+        int cb = pre.x, pbase = pre.y;
+        for (int r = r_begin; r < r_end; ++r) {
+            const ReqPlan rp = plan_request(p, r, pps);
+            const int n = (rp.valid && fits) ? rp.n_chunks : 0;
+            const bool split = rp.valid && fits && rp.mode == 0 && rp.n_chunks > 1;
+            // {splits (0: request refused), partial row base, first chunk, chunks}
+            req[r] = make_int4(rp.valid && fits ? (split ? rp.n_chunks : 1) : 0, split ? pbase : 0, cb, n);
+            cb += n;
+            if (split) pbase += rp.q * p.num_q_heads * rp.n_chunks;
         }
     }
-    atomicAdd(&prow_need, prows);
     __syncthreads();
-    if (tid == 0) {
-        int acc = 0, pacc = 0;                        // largest first
-        for (int b = kSizeBins - 1; b >= 0; --b) {
-            bin_cursor[b] = acc;
-            acc += bin_count[b];
-            pbin_cursor[b] = pacc;
-            pacc += pbin_count[b];
-        }
-        const bool fits = acc <= p.lay.max_chunks && pacc <= p.lay.max_ptiles &&
-                          prow_need <= (unsigned long long)p.lay.max_prow;
-        hdr->n_chunks = fits ? acc : 0;
-        hdr->n_ptiles = fits ? pacc : 0;
-        if (!fits) bad = 2;
-    }
-    __syncthreads();
-    const bool overflow = bad == 2;
 
-    // pass 3: emit chunks and tiles, request info and token owners
-    for (int r = tid; r < p.num_seqs; r += blockDim.x) {
-        const ReqPlan rp = plan_request(p, r, pages_per_split);
-        int2 info = make_int2(rp.valid && !overflow ? 1 : 0, 0);
-        if (rp.valid && !overflow) {
-            if (rp.mode == 0 && rp.n_chunks > 1) {
-                const int rows = (p.qsl[r + 1] - p.qsl[r]) * p.num_q_heads * rp.n_chunks;
-                const int base = atomicAdd(&prow_cursor, rows);
-                info = make_int2(rp.n_chunks, base);
-            }
-            for (int k = 0; k < rp.n_chunks; ++k) {
-                const int2 pg = chunk_pages(p, rp, r, k);
-                if (rp.mode == 2) {
-                    const int pos = atomicAdd(&pbin_cursor[min(pg.y, kSizeBins - 1)], 1);
-                    ptiles[pos] = make_int4(r, k, pg.y, 0);
-                } else {
-                    const int pos = atomicAdd(&bin_cursor[min(pg.y - pg.x, kSizeBins - 1)], 1);
-                    chunks[pos] = make_int4(r, k, pg.x, pg.y);
-                }
-            }
-            for (int t = p.qsl[r]; t < p.qsl[r + 1]; ++t) tok[t] = make_int2(r, t - p.qsl[r]);
+    // pass 3: per chunk, its size bin (request found by binary search on the bases)
+    auto owner = [&](int c) {
+        int lo = 0, hi = p.num_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (req[mid].z <= c) lo = mid;
+            else hi = mid - 1;
         }
-        req[r] = info;
+        while (lo < p.num_seqs - 1 && req[lo].w == 0) ++lo;   // skip requests with no chunks
+        return lo;
+    };
+    const int n_emit = fits ? n_total : 0;
+    for (int c = tid; c < n_emit; c += nthr) {
+        const int r = owner(c);
+        const int4 ri = req[r];
+        const ReqPlan rp = plan_request(p, r, pps);
+        const int2 pg = chunk_pages(rp, G, c - ri.z);
+        if (rp.mode == 2) agg_inc(pbin_count, min(pg.y, kSizeBins - 1));
+        else agg_inc(bin_count, min(pg.y - pg.x, kSizeBins - 1));
+    }
+    __syncthreads();
+    if (tid < 32) {                                   // largest first
+        const int acc = scan_bins_desc(bin_count, bin_cursor, tid);
+        const int pacc = scan_bins_desc(pbin_count, pbin_cursor, tid);
+        if (tid == 0) {
+            const bool ok = fits && acc <= p.lay.max_chunks && pacc <= p.lay.max_ptiles;
+            hdr->n_chunks = ok ? acc : 0;
+            hdr->n_ptiles = ok ? pacc : 0;
+            if (!fits) bad = 1;
+        }
+    }
+    __syncthreads();
+
+    // pass 4: emit every chunk at its sorted position
+    for (int c = tid; c < n_emit; c += nthr) {
+        const int r = owner(c);
+        const int4 ri = req[r];
+        const ReqPlan rp = plan_request(p, r, pps);
+        const int k = c - ri.z;
+        const int2 pg = chunk_pages(rp, G, k);
+        if (rp.mode == 2) {
+            const int pos = agg_inc(pbin_cursor, min(pg.y, kSizeBins - 1));
+            if (pos < p.lay.max_ptiles) ptiles[pos] = make_int4(r, k, pg.y, 0);
+        } else {
+            const int pos = agg_inc(bin_cursor, min(pg.y - pg.x, kSizeBins - 1));
+            if (pos < p.lay.max_chunks) chunks[pos] = make_int4(r, k, pg.x, pg.y);
+        }
+    }
+    // token owners, one thread per token: the last request starting at or
+    // before t (requests with no tokens share their start with the next one)
+    for (int t = tid; t < p.num_tokens; t += nthr) {
+        int lo = 0, hi = p.num_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.qsl[mid] <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        if (p.num_seqs > 0 && p.qsl[lo] <= t && t < p.qsl[lo + 1] && req[lo].x > 0)
+            tok[t] = make_int2(lo, t - p.qsl[lo]);
     }
     __syncthreads();
     if (tid == 0) {
@@ -290,7 +405,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         hdr->num_q_heads = p.num_q_heads;
         hdr->head_size = p.head_size;
         hdr->num_seqs = p.num_seqs;
-        hdr->pages_per_split = pages_per_split;
+        hdr->pages_per_split = pps;
         hdr->off_req = p.lay.off_req;
         hdr->off_tok = p.lay.off_tok;
         hdr->off_chunks = p.lay.off_chunks;
@@ -300,7 +415,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         hdr->max_chunks = p.lay.max_chunks;
         hdr->max_ptiles = p.lay.max_ptiles;
         hdr->max_prow = p.lay.max_prow;
-        hdr->prow_used = prow_cursor;
+        hdr->prow_used = totals.y;
     }
 }
 
@@ -338,7 +453,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
     const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
-    const int2 *req = reinterpret_cast<const int2 *>(p.ws + hdr->off_req);
+    const int4 *req = reinterpret_cast<const int4 *>(p.ws + hdr->off_req);
     const int4 *chunks = reinterpret_cast<const int4 *>(p.ws + hdr->off_chunks);
     float *part_lse = reinterpret_cast<float *>(p.ws + hdr->off_part_lse);
     float *part_o = reinterpret_cast<float *>(p.ws + hdr->off_part_o);
@@ -374,7 +489,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
         const bool split_mode = rows_total <= 16;
         const int tile = split_mode ? 0 : ch.y;
         const int split = split_mode ? ch.y : 0;
-        const int2 info = req[r];
+        const int4 info = req[r];
         const int n_split = split_mode ? info.x : 1;
         const int rows = min(16, rows_total - 16 * tile);
 
@@ -604,7 +719,7 @@ __global__ void __launch_bounds__(256) combine_kernel(__nv_bfloat16 *out, const 
             set_status(reinterpret_cast<int32_t *>(const_cast<uint8_t *>(ws)), PKV_ERR_PROTOCOL);
         return;
     }
-    const int2 *req = reinterpret_cast<const int2 *>(ws + hdr->off_req);
+    const int4 *req = reinterpret_cast<const int4 *>(ws + hdr->off_req);
     const int2 *tok = reinterpret_cast<const int2 *>(ws + hdr->off_tok);
     const float *part_lse = reinterpret_cast<const float *>(ws + hdr->off_part_lse);
     const float *part_o = reinterpret_cast<const float *>(ws + hdr->off_part_o);
@@ -615,7 +730,7 @@ __global__ void __launch_bounds__(256) combine_kernel(__nv_bfloat16 *out, const 
     const int h = static_cast<int>(row % num_q_heads);
     const int2 ti = tok[t];
     if (ti.x < 0) return;
-    const int2 info = req[ti.x];
+    const int4 info = req[ti.x];
     const int n = info.x;
     if (n <= 1) return;
     const int64_t base = info.y + (static_cast<int64_t>(ti.y) * num_q_heads + h) * n;

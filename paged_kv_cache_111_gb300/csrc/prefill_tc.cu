@@ -53,8 +53,8 @@ struct PrefillCfg {
     static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 };
 
-enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kVFull0, kVFull1, kKVEmpty0, kKVEmpty1, kSFull0, kSFull1,
-                  kSFree0, kSFree1, kPFull, kODone, kVFix, kVote, kNumBars };
+enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1,
+                  kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kODone, kVFix, kVote, kNumBars };
 
 // A row whose weights in a KV tile are concentrated (sum of squared weights
 // of the tile above this fraction of the squared running sum) needs P's bf16
@@ -132,30 +132,50 @@ __global__ void __launch_bounds__(256, 1)
                             qs + row0 / G);
         }
         const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks_per_seq;
+        // block ids in windows of 32 pages (4 KV tiles), one lane per page; the
+        // next window is loaded a window ahead.  Pages past the sequence are -1
+        // and load as zeros (outside the tensor map).
+        constexpr int kPagesPerTile = kPrefillKeys / kBlock;
+        auto load_window = [&](int w) -> int {
+            const int page = w * 32 + lane;
+            const int b = page < n_pages ? __ldg(bt + page) : -1;
+            if (page < n_pages && (b < 0 || b >= p.num_blocks))
+                set_status(status, PKV_ERR_DEVICE_INDEX);   // loaded as zeros by the bounded TMA, reported
+            return b;
+        };
+        int win_cur = load_window(0);
+        int win_next = load_window(1);
         for (int j = 0; j < n_kv && ok; ++j) {
             const int st = j & 1;
-            if (j >= 2) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKVEmpty0 + st], ((j - 2) >> 1) & 1, status));
+            if (j > 0 && (j * kPagesPerTile) % 32 == 0) {
+                win_cur = win_next;
+                win_next = load_window(j * kPagesPerTile / 32 + 1);
+            }
+            const int wofs = (j * kPagesPerTile) % 32;
+            int pb[kPagesPerTile];
+#pragma unroll
+            for (int pg = 0; pg < kPagesPerTile; ++pg) pb[pg] = __shfl_sync(0xffffffffu, win_cur, wofs + pg);
+            // K of tile j once S of tile j-2 has read its stage
+            if (j >= 2) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKEmpty0 + st], ((j - 2) >> 1) & 1, status));
             if (!ok) break;
-            const int page = j * (kPrefillKeys / kBlock) + lane;
-            // pages past the sequence load as zeros (block -1 is outside the tensor map)
-            const int blk = (lane < kPrefillKeys / kBlock && page < n_pages) ? __ldg(bt + page) : -1;
-            if (lane < kPrefillKeys / kBlock && page < n_pages && (blk < 0 || blk >= p.num_blocks))
-                set_status(status, PKV_ERR_DEVICE_INDEX);   // loaded as zeros by the bounded TMA, reported
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars[kKFull0 + st], Cfg::kKVBytes);
-                mbar_arrive_expect_tx(&bars[kVFull0 + st], Cfg::kKVBytes);
+#pragma unroll
+                for (int pg = 0; pg < kPagesPerTile; ++pg)
+                    for (int h = 0; h < Cfg::kHalves; ++h)
+                        tma_load_5d(smem + Cfg::kOffK + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
+                                    &kv_map, &bars[kKFull0 + st], h * 64, 0, 0, g, pb[pg]);
             }
-#pragma unroll 1
-            for (int pg = 0; pg < kPrefillKeys / kBlock; ++pg) {
-                const int b = __shfl_sync(0xffffffffu, blk, pg);
-                if (lane == 0) {
-                    for (int h = 0; h < Cfg::kHalves; ++h) {
-                        uint8_t *kd = smem + Cfg::kOffK + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048;
-                        uint8_t *vd = smem + Cfg::kOffV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048;
-                        tma_load_5d(kd, &kv_map, &bars[kKFull0 + st], h * 64, 0, 0, g, b);
-                        tma_load_5d(vd, &kv_map, &bars[kVFull0 + st], h * 64, 0, 1, g, b);
-                    }
-                }
+            // V of tile j once P V of tile j-2 has read its stage
+            if (j >= 2) ok = __all_sync(0xffffffffu, pf_wait(&bars[kVEmpty0 + st], ((j - 2) >> 1) & 1, status));
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[kVFull0 + st], Cfg::kKVBytes);
+#pragma unroll
+                for (int pg = 0; pg < kPagesPerTile; ++pg)
+                    for (int h = 0; h < Cfg::kHalves; ++h)
+                        tma_load_5d(smem + Cfg::kOffV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
+                                    &kv_map, &bars[kVFull0 + st], h * 64, 0, 1, g, pb[pg]);
             }
             if (j == end_tile) {
                 // zero V rows past the sequence end in its last (partial) page
@@ -207,21 +227,17 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 umma_commit(&bars[kODone]);
             };
-            if (ok) ok = pf_wait(&bars[kKFull0], 0, status);
-            if (ok) {
+            // S of the first two tiles (two S buffers in tensor memory)
+            for (int j0 = 0; j0 < 2 && j0 < n_kv && ok; ++j0) {
+                ok = pf_wait(&bars[kKFull0 + j0], 0, status);
+                if (!ok) break;
                 tc_fence_after();
-                issue_s(0);
+                issue_s(j0);
+                umma_commit(&bars[kKEmpty0 + j0]);
             }
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int st = j & 1;
-                if (j + 1 < n_kv) {
-                    const int s1 = (j + 1) & 1;
-                    ok = pf_wait(&bars[kKFull0 + s1], ((j + 1) >> 1) & 1, status);
-                    if (ok && j + 1 >= 2) ok = pf_wait(&bars[kSFree0 + s1], ((j - 1) >> 1) & 1, status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(j + 1);
-                }
+                // O += P V of tile j as soon as its P is in shared memory
                 ok = pf_wait(&bars[kPFull], p_cnt & 1, status);
                 ++p_cnt;
                 if (ok) ok = pf_wait(&bars[kVFull0 + st], (j >> 1) & 1, status);
@@ -238,7 +254,16 @@ __global__ void __launch_bounds__(256, 1)
                     tc_fence_after();
                     issue_pv(j, 1);
                 }
-                umma_commit(&bars[kKVEmpty0 + st]);
+                umma_commit(&bars[kVEmpty0 + st]);
+                // then S of tile j+2 into the buffer softmax has read for tile j
+                if (j + 2 < n_kv) {
+                    ok = pf_wait(&bars[kKFull0 + st], ((j + 2) >> 1) & 1, status);
+                    if (ok) ok = pf_wait(&bars[kSFree0 + st], (j >> 1) & 1, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(j + 2);
+                    umma_commit(&bars[kKEmpty0 + st]);
+                }
             }
         }
         __syncwarp();
@@ -261,26 +286,69 @@ __global__ void __launch_bounds__(256, 1)
             if (!ok) break;
             tc_fence_after();
             float x[kPrefillKeys];
+            {
+                uint32_t v[4][32];
 #pragma unroll
-            for (int c = 0; c < kPrefillKeys / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(trow + (sb ? Cfg::kColS1 : Cfg::kColS0) + c * 32, v);
+                for (int c = 0; c < kPrefillKeys / 32; ++c)
+                    tmem_ld32(trow + (sb ? Cfg::kColS1 : Cfg::kColS0) + c * 32, v[c]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
+                for (int c = 0; c < kPrefillKeys / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kSFree0 + sb]);
 
+            // keys a row may not see become -inf; only tiles reaching some
+            // row's limit need the test (warp-uniform branch)
             const int key0 = j * kPrefillKeys;
-            float mx = NEG_INF;
+            if (__any_sync(0xffffffffu, key0 + kPrefillKeys > lim)) {
+#pragma unroll
+                for (int c = 0; c < kPrefillKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
+            }
+            // row max of the raw scores: 8 independent chains
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = x[e];
+#pragma unroll
+            for (int c = 8; c < kPrefillKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            // log2-domain max (scale > 0 keeps the order of scores)
+            const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+            // a row moves its reference max only when the max grew by more than
+            // 2^8 (its O is then rescaled by alpha)
+            const bool first = m_ref == NEG_INF;           // O holds nothing yet for this row
+            const bool grow = !first && m_new > m_ref + 8.f;
+            const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
+            if (first || grow) m_ref = m_new;
+            const float ref = (m_ref == NEG_INF) ? 0.f : m_ref;
+            float ps8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ps8[e] = 0.f;
 #pragma unroll
             for (int c = 0; c < kPrefillKeys; ++c) {
-                x[c] = (key0 + c < lim) ? x[c] * p.scale_log2 : NEG_INF;
-                mx = fmaxf(mx, x[c]);
+                x[c] = exp2f(fmaf(x[c], p.scale_log2, -ref));
+                ps8[c & 7] += x[c];
             }
-            const float m_new = fmaxf(m_ref, mx);
+            const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+            l = l * alpha + psum;
+            // CTA-wide vote: does any row need the remainder of P in this tile?
+            // sum p^2 <= max p * sum p, so a row whose largest weight times the
+            // tile's weight stays below the concentration bound never needs it
+            const float pmax = (mx == NEG_INF) ? 0.f : exp2f(fmaf(mx, p.scale_log2, -ref));
+            const bool need = j < p.lo_tiles || pmax * psum > kLoConcentration * l * l;
+            const uint32_t wvote = __any_sync(0xffffffffu, need) ? 1u : 0u;
+            if (lane == 0) {
+                votes[(j & 1) * 4 + (warp - 4)] = wvote;
+                mbar_arrive(&bars[kVote]);
+            }
+            ok = __all_sync(0xffffffffu, pf_wait(&bars[kVote], j & 1, status));
+            if (!ok) break;
+            const bool lo = (votes[(j & 1) * 4 + 0] | votes[(j & 1) * 4 + 1] | votes[(j & 1) * 4 + 2] |
+                             votes[(j & 1) * 4 + 3]) != 0u;
             // P V of the previous tile must be finished before O or the P buffer is touched
             if (j > 0) {
                 ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone], o_cnt & 1, status));
@@ -288,15 +356,10 @@ __global__ void __launch_bounds__(256, 1)
                 if (!ok) break;
                 tc_fence_after();
             }
-            // a row moves its reference max only when the max grew by more than
-            // 2^8 (its O is then rescaled); tensor-memory loads and stores are
-            // warp-wide, so the warp rescales when any of its rows needs it
-            const bool first = m_ref == NEG_INF;           // O holds nothing yet for this row
-            const bool grow = !first && m_new > m_ref + 8.f;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
-                l *= alpha;
-#pragma unroll
+            // tensor-memory loads and stores are warp-wide: the warp rescales
+            // when any of its rows moved its reference max
+            if (__any_sync(0xffffffffu, grow)) {               // rare: one 32-column chunk at a time
+#pragma unroll 1
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32(trow + Cfg::kColO + c * 32, v);
@@ -307,27 +370,6 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 tmem_st_wait();
             }
-            if (first || grow) m_ref = m_new;
-            const float ref = (m_ref == NEG_INF) ? 0.f : m_ref;
-            float psum = 0.f, psq = 0.f;
-#pragma unroll
-            for (int c = 0; c < kPrefillKeys; ++c) {
-                x[c] = exp2f(x[c] - ref);
-                psum += x[c];
-                psq += x[c] * x[c];
-            }
-            l += psum;
-            // CTA-wide vote: does any row need the remainder of P in this tile?
-            const bool need = j < p.lo_tiles || psq > kLoConcentration * l * l;
-            const uint32_t wvote = __any_sync(0xffffffffu, need) ? 1u : 0u;
-            if (lane == 0) {
-                votes[(j & 1) * 4 + (warp - 4)] = wvote;
-                mbar_arrive(&bars[kVote]);
-            }
-            ok = __all_sync(0xffffffffu, pf_wait(&bars[kVote], j & 1, status));
-            if (!ok) break;
-            const bool lo = (votes[(j & 1) * 4 + 0] | votes[(j & 1) * 4 + 1] | votes[(j & 1) * 4 + 2] |
-                             votes[(j & 1) * 4 + 3]) != 0u;
             // P (bf16) into the K-major, 128-byte-swizzled A tile: row `row`,
             // keys in two 64-key halves, 16-byte chunk c at c ^ (row & 7)
 #pragma unroll
@@ -380,22 +422,22 @@ __global__ void __launch_bounds__(256, 1)
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int i = rrow / G, hh = rrow % G;
             __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(qs + i) * p.num_q_heads + g * G + hh) * HD;
+            uint32_t v[HD / 32][32];
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(trow + Cfg::kColO + c * 32, v);
-                tmem_ld_wait();
-                if (valid) {
+            for (int c = 0; c < HD / 32; ++c) tmem_ld32(trow + Cfg::kColO + c * 32, v[c]);
+            tmem_ld_wait();
+            if (valid) {
+#pragma unroll
+                for (int c = 0; c < HD / 32; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[e + 0]) * inv, __uint_as_float(v[e + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+                        w.x = pack_bf16x2(__uint_as_float(v[c][e + 0]) * inv, __uint_as_float(v[c][e + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(v[c][e + 2]) * inv, __uint_as_float(v[c][e + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(v[c][e + 4]) * inv, __uint_as_float(v[c][e + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(v[c][e + 6]) * inv, __uint_as_float(v[c][e + 7]) * inv);
                         *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
                     }
-                }
             }
         }
     }
