@@ -602,12 +602,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
             const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
             const float ref0 = mn0 == NEG_INF ? 0.f : mn0;
             const float ref1 = mn1 == NEG_INF ? 0.f : mn1;
-            const float a0 = exp2f(m0 - ref0), a1 = exp2f(m1 - ref1);
+            const float a0 = fast_exp2(m0 - ref0), a1 = fast_exp2(m1 - ref1);
             m0 = mn0;
             m1 = mn1;
             float pr[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) pr[e] = exp2f(x[e] - (((e >> 1) & 1) ? ref1 : ref0));
+            for (int e = 0; e < 8; ++e) pr[e] = fast_exp2(x[e] - (((e >> 1) & 1) ? ref1 : ref0));
             l0 = l0 * a0 + (pr[0] + pr[1] + pr[4] + pr[5]);
             l1 = l1 * a1 + (pr[2] + pr[3] + pr[6] + pr[7]);
 #pragma unroll

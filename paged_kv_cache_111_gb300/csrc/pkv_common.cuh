@@ -133,6 +133,14 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &big, ui
     rest = *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// 2^x on the special-function unit (ex2.approx, flush-to-zero): a few ulp,
+// 2^-inf = +0.  Softmax weights below 2^-126 become 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Record an error code in a device status word (first error wins).
 __device__ __forceinline__ void set_status(int32_t *status, int32_t code) {
     if (status) atomicCAS(status, 0, code);

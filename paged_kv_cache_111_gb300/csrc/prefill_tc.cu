@@ -322,24 +322,23 @@ __global__ void __launch_bounds__(256, 1)
             // 2^8 (its O is then rescaled by alpha)
             const bool first = m_ref == NEG_INF;           // O holds nothing yet for this row
             const bool grow = !first && m_new > m_ref + 8.f;
-            const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
+            const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
             if (first || grow) m_ref = m_new;
             const float ref = (m_ref == NEG_INF) ? 0.f : m_ref;
-            float ps8[8];
+            float ps8[8], pq8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ps8[e] = 0.f;
+            for (int e = 0; e < 8; ++e) ps8[e] = pq8[e] = 0.f;
 #pragma unroll
             for (int c = 0; c < kPrefillKeys; ++c) {
-                x[c] = exp2f(fmaf(x[c], p.scale_log2, -ref));
+                x[c] = fast_exp2(fmaf(x[c], p.scale_log2, -ref));
                 ps8[c & 7] += x[c];
+                pq8[c & 7] = fmaf(x[c], x[c], pq8[c & 7]);
             }
             const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+            const float psq = ((pq8[0] + pq8[1]) + (pq8[2] + pq8[3])) + ((pq8[4] + pq8[5]) + (pq8[6] + pq8[7]));
             l = l * alpha + psum;
             // CTA-wide vote: does any row need the remainder of P in this tile?
-            // sum p^2 <= max p * sum p, so a row whose largest weight times the
-            // tile's weight stays below the concentration bound never needs it
-            const float pmax = (mx == NEG_INF) ? 0.f : exp2f(fmaf(mx, p.scale_log2, -ref));
-            const bool need = j < p.lo_tiles || pmax * psum > kLoConcentration * l * l;
+            const bool need = j < p.lo_tiles || psq > kLoConcentration * l * l;
             const uint32_t wvote = __any_sync(0xffffffffu, need) ? 1u : 0u;
             if (lane == 0) {
                 votes[(j & 1) * 4 + (warp - 4)] = wvote;
