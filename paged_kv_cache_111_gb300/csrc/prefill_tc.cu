@@ -39,22 +39,21 @@ namespace pkv {
 template <int HD>
 struct PrefillCfg {
     static constexpr int kHalves = HD / 64;
-    static constexpr int kHalfQ = kPrefillRows * 128;       // bytes of one 64-column half of a 128-row tile
-    static constexpr int kQBytes = kHalves * kHalfQ;
+    static constexpr int kStages = 3;                        // K and V ring depth
     static constexpr int kKVBytes = kHalves * kPrefillKeys * 128;   // one K (or V) tile
-    static constexpr int kPBytes = 2 * kPrefillRows * 128;  // 128 x 128 bf16
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;
-    static constexpr int kOffV = kOffK + 2 * kKVBytes;
-    static constexpr int kOffP = kOffV + 2 * kKVBytes;
-    static constexpr int kOffBar = kOffP + kPBytes;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kStages * kKVBytes;
+    static constexpr int kOffBar = kOffV + kStages * kKVBytes;
     static constexpr int kSmem = kOffBar + 256 + 1024;      // + barriers + alignment slack
-    static constexpr uint32_t kTmemCols = 512;              // S0 | S1 | O
-    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+    // tensor memory: two S buffers (each later holding that tile's P and its
+    // bf16 remainder), O, and Q as the A operand of S = Q K^T
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColQ = 384;
+    static constexpr uint32_t kPLo = 64;                     // remainder's columns within an S buffer
 };
 
-enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1,
-                  kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kODone, kVFix, kVote, kNumBars };
+enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kKFull2, kVFull0, kVFull1, kVFull2, kKEmpty0, kKEmpty1, kKEmpty2,
+                  kVEmpty0, kVEmpty1, kVEmpty2, kSFull0, kSFull1, kPFull, kODone0, kODone1, kVFix, kNumBars };
 
 // A row whose weights in a KV tile are concentrated (sum of squared weights
 // of the tile above this fraction of the squared running sum) needs P's bf16
@@ -72,18 +71,17 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t 
 
 template <int HD>
 __global__ void __launch_bounds__(256, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap kv_map,
-                   const PrefillParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16 *__restrict__ query,
+                   const int64_t q_stride, const PrefillParams p) {
     using Cfg = PrefillCfg<HD>;
+    constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile uint32_t *votes = tmem_slot + 4;          // [2 tiles in flight][4 softmax warps]
-    const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
     const uint32_t sK = smem_u32(smem + Cfg::kOffK);
     const uint32_t sV = smem_u32(smem + Cfg::kOffV);
-    const uint32_t sP = smem_u32(smem + Cfg::kOffP);
 
     const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
@@ -104,9 +102,7 @@ __global__ void __launch_bounds__(256, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < kNumBars; ++b)
-            mbar_init(&bars[b], (b == kSFree0 || b == kSFree1 || b == kPFull || b == kVote) ? 4 : 1);
-        tma_prefetch_desc(&q_map);
+        for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], (b == kPFull || b == kQFull) ? 4 : 1);
         tma_prefetch_desc(&kv_map);
     }
     if (warp == 2) {
@@ -123,14 +119,8 @@ __global__ void __launch_bounds__(256, 1)
     const int end_tile = (L % kBlock) ? (L - 1) / kPrefillKeys : -1;
 
     if (warp == 0) {
-        // ---------------- producer ----------------
+        // ---------------- producer: K and V pages through the block table ----------------
         bool ok = true;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[kQFull], Cfg::kQBytes);
-            for (int h = 0; h < Cfg::kHalves; ++h)
-                tma_load_3d(smem + Cfg::kOffQ + h * Cfg::kHalfQ, &q_map, &bars[kQFull], h * 64, g * G,
-                            qs + row0 / G);
-        }
         const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks_per_seq;
         // block ids in windows of 32 pages (4 KV tiles), one lane per page; the
         // next window is loaded a window ahead.  Pages past the sequence are -1
@@ -146,7 +136,7 @@ __global__ void __launch_bounds__(256, 1)
         int win_cur = load_window(0);
         int win_next = load_window(1);
         for (int j = 0; j < n_kv && ok; ++j) {
-            const int st = j & 1;
+            const int st = j % S;
             if (j > 0 && (j * kPagesPerTile) % 32 == 0) {
                 win_cur = win_next;
                 win_next = load_window(j * kPagesPerTile / 32 + 1);
@@ -155,8 +145,8 @@ __global__ void __launch_bounds__(256, 1)
             int pb[kPagesPerTile];
 #pragma unroll
             for (int pg = 0; pg < kPagesPerTile; ++pg) pb[pg] = __shfl_sync(0xffffffffu, win_cur, wofs + pg);
-            // K of tile j once S of tile j-2 has read its stage
-            if (j >= 2) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKEmpty0 + st], ((j - 2) >> 1) & 1, status));
+            // K of tile j once S of tile j-S has read its stage
+            if (j >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKEmpty0 + st], ((j - S) / S) & 1, status));
             if (!ok) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars[kKFull0 + st], Cfg::kKVBytes);
@@ -166,8 +156,8 @@ __global__ void __launch_bounds__(256, 1)
                         tma_load_5d(smem + Cfg::kOffK + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
                                     &kv_map, &bars[kKFull0 + st], h * 64, 0, 0, g, pb[pg]);
             }
-            // V of tile j once P V of tile j-2 has read its stage
-            if (j >= 2) ok = __all_sync(0xffffffffu, pf_wait(&bars[kVEmpty0 + st], ((j - 2) >> 1) & 1, status));
+            // V of tile j once P V of tile j-S has read its stage
+            if (j >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kVEmpty0 + st], ((j - S) / S) & 1, status));
             if (!ok) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars[kVFull0 + st], Cfg::kKVBytes);
@@ -179,9 +169,9 @@ __global__ void __launch_bounds__(256, 1)
             }
             if (j == end_tile) {
                 // zero V rows past the sequence end in its last (partial) page
-                ok = __all_sync(0xffffffffu, pf_wait(&bars[kVFull0 + st], (j >> 1) & 1, status));
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kVFull0 + st], (j / S) & 1, status));
                 if (!ok) break;
-                const int lp = (L - 1) / kBlock - j * (kPrefillKeys / kBlock);   // page within the tile
+                const int lp = (L - 1) / kBlock - j * kPagesPerTile;   // page within the tile
                 const int first = L % kBlock;
                 const int nrows = kBlock - first;
                 for (int e = lane; e < Cfg::kHalves * nrows * 8; e += 32) {
@@ -202,67 +192,56 @@ __global__ void __launch_bounds__(256, 1)
             constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillRows, kPrefillKeys, 0, 0);
             constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillRows, HD, 0, 1);
             bool ok = pf_wait(&bars[kQFull], 0, status);
-            uint32_t p_cnt = 0;
+            // S(j) = Q K^T into S buffer j & 1; A = Q in tensor memory
             auto issue_s = [&](int j) {
-                const int st = j & 1;
-                const uint32_t d = tmem + (st ? Cfg::kColS1 : Cfg::kColS0);
+                const int st = j % S;
+                const uint32_t d = tmem + ((j & 1) ? Cfg::kColS1 : Cfg::kColS0);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kPrefillRows * 128) + (kk & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(sQ + off, 16, 1024);
                     const uint64_t b = smem_desc_sw128(sK + st * Cfg::kKVBytes + (kk >> 2) * (kPrefillKeys * 128) +
                                                            (kk & 3) * 32,
                                                        16, 1024);
-                    umma_bf16_ss(d, a, b, kIdescS, kk > 0);
+                    umma_bf16_ts(d, tmem + Cfg::kColQ + kk * 8, b, kIdescS, kk > 0);
                 }
-                umma_commit(&bars[kSFull0 + st]);
+                umma_commit(&bars[kSFull0 + (j & 1)]);
+                umma_commit(&bars[kKEmpty0 + st]);
             };
-            auto issue_pv = [&](int j, uint32_t accumulate) {
-                const int st = j & 1;
+            // O (+)= P V; A = P (or its remainder) in S buffer j & 1
+            auto issue_pv = [&](int j, uint32_t pcol, uint32_t accumulate) {
+                const int st = j % S;
 #pragma unroll
                 for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
-                    const uint64_t a = smem_desc_sw128(sP + (kk >> 2) * (kPrefillRows * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = smem_desc_sw128(sV + st * Cfg::kKVBytes + kk * 2048, kPrefillKeys * 128, 1024);
-                    umma_bf16_ss(tmem + Cfg::kColO, a, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + Cfg::kColO, pcol + kk * 8, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(&bars[kODone]);
             };
-            // S of the first two tiles (two S buffers in tensor memory)
             for (int j0 = 0; j0 < 2 && j0 < n_kv && ok; ++j0) {
                 ok = pf_wait(&bars[kKFull0 + j0], 0, status);
                 if (!ok) break;
                 tc_fence_after();
                 issue_s(j0);
-                umma_commit(&bars[kKEmpty0 + j0]);
             }
             for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j & 1;
-                // O += P V of tile j as soon as its P is in shared memory
-                ok = pf_wait(&bars[kPFull], p_cnt & 1, status);
-                ++p_cnt;
-                if (ok) ok = pf_wait(&bars[kVFull0 + st], (j >> 1) & 1, status);
+                const int st = j % S;
+                ok = pf_wait(&bars[kPFull], j & 1, status);
+                if (ok) ok = pf_wait(&bars[kVFull0 + st], (j / S) & 1, status);
                 if (ok && j == end_tile) ok = pf_wait(&bars[kVFix], 0, status);
                 if (!ok) break;
                 tc_fence_after();
+                const uint32_t pbuf = tmem + ((j & 1) ? Cfg::kColS1 : Cfg::kColS0);
                 const bool lo = (votes[(j & 1) * 4 + 0] | votes[(j & 1) * 4 + 1] | votes[(j & 1) * 4 + 2] |
                                  votes[(j & 1) * 4 + 3]) != 0u;
-                issue_pv(j, j > 0);
-                if (lo) {
-                    ok = pf_wait(&bars[kPFull], p_cnt & 1, status);
-                    ++p_cnt;
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(j, 1);
-                }
+                issue_pv(j, pbuf, j > 0);
+                if (lo) issue_pv(j, pbuf + Cfg::kPLo, 1);
+                umma_commit(&bars[kODone0 + (j & 1)]);
                 umma_commit(&bars[kVEmpty0 + st]);
-                // then S of tile j+2 into the buffer softmax has read for tile j
+                // S of tile j+2 reuses S buffer j & 1: issued after P V of tile j
+                // (tensor-core operations of one thread run in issue order)
                 if (j + 2 < n_kv) {
-                    ok = pf_wait(&bars[kKFull0 + st], ((j + 2) >> 1) & 1, status);
-                    if (ok) ok = pf_wait(&bars[kSFree0 + st], (j >> 1) & 1, status);
+                    ok = pf_wait(&bars[kKFull0 + (j + 2) % S], ((j + 2) / S) & 1, status);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(j + 2);
-                    umma_commit(&bars[kKEmpty0 + st]);
                 }
             }
         }
@@ -275,13 +254,38 @@ __global__ void __launch_bounds__(256, 1)
         const bool valid = rrow < rows_total;
         const int lim = valid ? ctx + rrow / G + 1 : 0;    // keys [0, lim) visible
         const float NEG_INF = -__int_as_float(0x7f800000);
-        float m_ref = NEG_INF, l = 0.f;
-        uint32_t o_cnt = 0;
-        bool ok = true;
         const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
+        bool ok = true;
 
+        // Q row -> tensor memory (A operand of S = Q K^T), zeros past the request
+        {
+            uint32_t qv[HD / 2];
+            const __nv_bfloat16 *qp =
+                query + static_cast<int64_t>(qs + (valid ? rrow / G : 0)) * q_stride +
+                static_cast<int64_t>(g * G + (valid ? rrow % G : 0)) * HD;
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c) {
+                const uint4 w = valid ? __ldg(reinterpret_cast<const uint4 *>(qp) + c) : make_uint4(0, 0, 0, 0);
+                qv[4 * c + 0] = w.x;
+                qv[4 * c + 1] = w.y;
+                qv[4 * c + 2] = w.z;
+                qv[4 * c + 3] = w.w;
+            }
+#pragma unroll
+            for (int c = 0; c < HD / 64; ++c) {
+                uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(&qv[c * 32]);
+                tmem_st32(trow + Cfg::kColQ + c * 32, part);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kQFull]);
+        }
+
+        float m_ref = NEG_INF, l = 0.f;
         for (int j = 0; j < n_kv && ok; ++j) {
             const int sb = j & 1;
+            const uint32_t sbuf = trow + (sb ? Cfg::kColS1 : Cfg::kColS0);
             ok = __all_sync(0xffffffffu, pf_wait(&bars[kSFull0 + sb], (j >> 1) & 1, status));
             if (!ok) break;
             tc_fence_after();
@@ -289,18 +293,13 @@ __global__ void __launch_bounds__(256, 1)
             {
                 uint32_t v[4][32];
 #pragma unroll
-                for (int c = 0; c < kPrefillKeys / 32; ++c)
-                    tmem_ld32(trow + (sb ? Cfg::kColS1 : Cfg::kColS0) + c * 32, v[c]);
+                for (int c = 0; c < kPrefillKeys / 32; ++c) tmem_ld32(sbuf + c * 32, v[c]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < kPrefillKeys / 32; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kSFree0 + sb]);
-
             // keys a row may not see become -inf; only tiles reaching some
             // row's limit need the test (warp-uniform branch)
             const int key0 = j * kPrefillKeys;
@@ -337,27 +336,22 @@ __global__ void __launch_bounds__(256, 1)
             const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
             const float psq = ((pq8[0] + pq8[1]) + (pq8[2] + pq8[3])) + ((pq8[4] + pq8[5]) + (pq8[6] + pq8[7]));
             l = l * alpha + psum;
-            // CTA-wide vote: does any row need the remainder of P in this tile?
+            // this warp's vote: does any of its rows need the remainder of P?
             const bool need = j < p.lo_tiles || psq > kLoConcentration * l * l;
-            const uint32_t wvote = __any_sync(0xffffffffu, need) ? 1u : 0u;
-            if (lane == 0) {
-                votes[(j & 1) * 4 + (warp - 4)] = wvote;
-                mbar_arrive(&bars[kVote]);
-            }
-            ok = __all_sync(0xffffffffu, pf_wait(&bars[kVote], j & 1, status));
-            if (!ok) break;
-            const bool lo = (votes[(j & 1) * 4 + 0] | votes[(j & 1) * 4 + 1] | votes[(j & 1) * 4 + 2] |
-                             votes[(j & 1) * 4 + 3]) != 0u;
-            // P V of the previous tile must be finished before O or the P buffer is touched
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone], o_cnt & 1, status));
-                ++o_cnt;
+            const bool wneed = __any_sync(0xffffffffu, need);
+            // P V of tile j-1 must be done before O is rescaled; the barrier of
+            // tile j-2 (same parity) is waited every tile, which keeps each
+            // barrier at most one phase ahead of this thread
+            if (j >= 2) {
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + sb], ((j - 2) >> 1) & 1, status));
                 if (!ok) break;
-                tc_fence_after();
             }
-            // tensor-memory loads and stores are warp-wide: the warp rescales
-            // when any of its rows moved its reference max
-            if (__any_sync(0xffffffffu, grow)) {               // rare: one 32-column chunk at a time
+            if (__any_sync(0xffffffffu, grow)) {              // rare: O rescale, one chunk at a time
+                if (j >= 1) {
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + (sb ^ 1)], ((j - 1) >> 1) & 1, status));
+                    if (!ok) break;
+                }
+                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t v[32];
@@ -367,54 +361,44 @@ __global__ void __launch_bounds__(256, 1)
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
                     tmem_st32(trow + Cfg::kColO + c * 32, v);
                 }
-                tmem_st_wait();
             }
-            // P (bf16) into the K-major, 128-byte-swizzled A tile: row `row`,
-            // keys in two 64-key halves, 16-byte chunk c at c ^ (row & 7)
+            // P (bf16 pairs) into this tile's S buffer; the remainder too when
+            // this warp asks for it, zeros otherwise (another warp may)
 #pragma unroll
-            for (int c = 0; c < kPrefillKeys / 8; ++c) {
-                uint32_t w[4];
+            for (int c = 0; c < 2; ++c) {
+                uint32_t w[32];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(x[c * 8 + 2 * e], x[c * 8 + 2 * e + 1]);
-                const uint32_t a = sP + (c >> 3) * (kPrefillRows * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                             "r"(w[3])
-                             : "memory");
+                for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1]);
+                tmem_st32(sbuf + c * 32, w);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kPFull]);
-            if (lo) {
-                // the remainder of P once the first P V has read the buffer
-                ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone], o_cnt & 1, status));
-                ++o_cnt;
-                if (!ok) break;
-                tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < kPrefillKeys / 8; ++c) {
-                    uint32_t w[4];
+            for (int c = 0; c < 2; ++c) {
+                uint32_t w[32];
+                if (wneed) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float a0 = x[c * 8 + 2 * e], a1 = x[c * 8 + 2 * e + 1];
+                    for (int e = 0; e < 32; ++e) {
+                        const float a0 = x[c * 64 + 2 * e], a1 = x[c * 64 + 2 * e + 1];
                         const float2 hb = __bfloat1622float2(__floats2bfloat162_rn(a0, a1));
                         w[e] = pack_bf16x2(a0 - hb.x, a1 - hb.y);
                     }
-                    const uint32_t a = sP + (c >> 3) * (kPrefillRows * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                                 "r"(w[3])
-                                 : "memory");
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] = 0u;
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kPFull]);
+                tmem_st32(sbuf + Cfg::kPLo + c * 32, w);
             }
+            tmem_st_wait();
+            if (lane == 0) votes[(j & 1) * 4 + (warp - 4)] = wneed ? 1u : 0u;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kPFull]);
         }
         if (ok) {
-            // epilogue: the last P V, then O / l to bf16
-            ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone], o_cnt & 1, status));
-            ++o_cnt;
+            // epilogue: the last two P V, then O / l to bf16
+            if (n_kv >= 2) ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + (n_kv & 1)], ((n_kv - 2) >> 1) & 1,
+                                                                status));
+            if (ok) ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + ((n_kv - 1) & 1)], ((n_kv - 1) >> 1) & 1,
+                                                         status));
         }
         if (ok) {
             tc_fence_after();
@@ -471,8 +455,8 @@ static EncodeTiledFn encode_fn() {
 }
 
 template <int HD>
-static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &qm, const CUtensorMap &kvm, int64_t grid,
-                             int dev, cudaStream_t stream) {
+static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, const void *query, int64_t q_stride,
+                             int64_t grid, int dev, cudaStream_t stream) {
     using Cfg = PrefillCfg<HD>;
     static std::mutex mu;
     static uint64_t done_mask = 0;
@@ -486,30 +470,19 @@ static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &qm, cons
             done_mask |= bit;
         }
     }
-    prefill_kernel<HD><<<static_cast<unsigned>(grid), 256, Cfg::kSmem, stream>>>(qm, kvm, p);
+    prefill_kernel<HD><<<static_cast<unsigned>(grid), 256, Cfg::kSmem, stream>>>(
+        kvm, static_cast<const __nv_bfloat16 *>(query), q_stride, p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
                    const void *kv_cache, int64_t num_blocks, int32_t head_size, int64_t grid, int dev,
                    cudaStream_t stream) {
+    (void)num_tokens;
     if (grid <= 0) return PKV_OK;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PKV_ERR_CUDA;
-    const int G = p.G;
-    // query as {head_size, q heads, tokens}; box = one tile: 64 columns x G heads x 128/G tokens
-    CUtensorMap qm, kvm;
-    {
-        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_size), static_cast<cuuint64_t>(p.num_q_heads),
-                                    static_cast<cuuint64_t>(num_tokens)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_size) * 2, static_cast<cuuint64_t>(q_stride) * 2};
-        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kPrefillRows / G)};
-        const cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(query), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return PKV_ERR_CUDA;
-    }
+    CUtensorMap kvm;
     {
         // cache as {head_size, 16, 2, kv heads, blocks}; box = K or V rows of one page, 64 columns
         const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2,
@@ -523,8 +496,8 @@ int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, 
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PKV_ERR_CUDA;
     }
-    if (head_size == 64) return launch_prefill_hd<64>(p, qm, kvm, grid, dev, stream);
-    return launch_prefill_hd<128>(p, qm, kvm, grid, dev, stream);
+    if (head_size == 64) return launch_prefill_hd<64>(p, kvm, query, q_stride, grid, dev, stream);
+    return launch_prefill_hd<128>(p, kvm, query, q_stride, grid, dev, stream);
 }
 
 }  // namespace pkv
