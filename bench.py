@@ -39,11 +39,11 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per algorithmic byte of the attention launch, from
 # the ncu capture summarised in profiles/decode_kernel_llama13b-decode-64req.md
-# (64-request case of the 13B batch: 1.0510 GB of traffic for 1.0339 GB of
+# (64-request case of the 13B batch: 1.0509 GB of traffic for 1.0339 GB of
 # algorithmic bytes).  Traffic grows with the KV bytes read, so the full
 # launch's traffic is this ratio times its algorithmic bytes.  It holds only
 # for the kernel sources it was measured on (hash below); otherwise null.
-DECODE_TRAFFIC = {"sources_sha256_16": "d8d9cfae647e79d4", "ratio": 1.051008 / 1.033885,
+DECODE_TRAFFIC = {"sources_sha256_16": "035123e956697127", "ratio": (1.042628 + 0.008228) / 1.033885,
                   "profile": "profiles/decode_kernel_llama13b-decode-64req.md"}
 
 
@@ -84,8 +84,17 @@ def algorithmic_bytes(step: wl.Step) -> dict:
     tables = sum((int(l) + B - 1) // B for l in step.seq_lens.tolist()) * 4
     attn = kv_unique + 2 * T * H * d * 2 + tables + 4 * S + 4 * (S + 1)
     kvw = 2 * (T * per_token_kv) + 8 * T
+    # flops: every query row of every head sees keys 0 .. its position; one
+    # multiply-add each in Q K^T and in P V (4 flops per key per dimension)
+    ql = step.query_lens.to(torch.float64)
+    ctx = step.context_lens.to(torch.float64)
+    visible = float((ql * ctx + ql * (ql + 1) / 2).sum())
+    flops = 4.0 * d * H * visible
     return {"attention": attn, "kv_write": kvw, "kv_unique": kv_unique, "kv_logical": kv_logical,
-            "step": attn + kvw}
+            "step": attn + kvw, "flops": flops}
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def peaks() -> dict:
@@ -93,9 +102,10 @@ def peaks() -> dict:
     try:
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json, burst copy)"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured (MEASURED_PEAKS.json: burst copy, burst cuBLAS bf16)"}
     except Exception:
-        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
 
 
 # ---------------------------------------------------------------------------
@@ -155,6 +165,26 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 
+def replica_seed(workload: str, rank: int) -> int:
+    """Each rank runs its own replica of the batch: same shape, its own draws."""
+    return wl.seed_of(workload) + 1000 * rank
+
+
+def max_over_ranks(values, world: int, device=None):
+    """Element-wise max of per-rank timings (the job takes as long as its
+    slowest rank); the only cross-rank exchange of the benchmark."""
+    if world <= 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(bytes_per_step_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank moved its replica's bytes in the slowest rank's time."""
+    return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def run_gpu(args, rank: int, world: int) -> dict:
     import paged_kv_cache_111_gb300 as pkv
     from paged_kv_cache_111_gb300 import _build
@@ -162,7 +192,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    step = wl.make_workload(args.workload, seed=wl.seed_of(args.workload) + 1000 * rank)
+    step = wl.make_workload(args.workload, seed=replica_seed(args.workload, rank))
     if args.subset:
         # the first `subset` requests with a compact pool (profiling-size case)
         step = step.subset(list(range(min(args.subset, step.num_seqs))), name=f"{args.workload}[:{args.subset}]")
@@ -363,6 +393,27 @@ def run_reference(args, rank: int, world: int) -> None:
 
 # ---------------------------------------------------------------------------
 
+def roofline(ab: dict, attn_ms: float, pk: dict) -> dict:
+    """Roofline of the paged_attn call: HBM-bound (decode) unless its
+    algorithmic flops at the tensor peak take longer than its bytes at the
+    HBM peak (a prefill chunk), then tensor-bound."""
+    t = attn_ms * 1e-3
+    hbm_s = ab["attention"] / (pk["hbm_gbs"] * 1e9)
+    tensor_s = ab["flops"] / (pk["bf16_tflops"] * 1e12)
+    if tensor_s > hbm_s:
+        ach = ab["flops"] / t / 1e12
+        return {"bound": "tensor", "kernel": "paged_attn (plan + decode + tcgen05 prefill kernels)",
+                "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],
+                "peak_source": pk["source"], "algorithmic_flops_per_launch": ab["flops"], "traffic": None}
+    ach = ab["attention"] / t / 1e9
+    return {"bound": "hbm", "kernel": "paged_attn (plan + decode kernels)",
+            "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+            "peak_source": pk["source"], "algorithmic_bytes_per_launch": ab["attention"],
+            "traffic": (DECODE_TRAFFIC["ratio"] * ab["attention"]
+                        if decode_sources_hash() == DECODE_TRAFFIC["sources_sha256_16"] else None),
+            "traffic_source": DECODE_TRAFFIC["profile"] + " (scaled by algorithmic bytes)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -390,17 +441,13 @@ def main():
     step = r["step"]
     ab = algorithmic_bytes(step)
     ms_per_step = r["total_ms"] / args.steps
-    if world > 1:
-        t = torch.tensor([ms_per_step, r["attn_ms"], r["e2e_ms"]], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step, attn_max, e2e_max = (float(x) for x in t.tolist())
-    else:
-        attn_max, e2e_max = r["attn_ms"], r["e2e_ms"]
+    ms_per_step, attn_max, e2e_max = max_over_ranks([ms_per_step, r["attn_ms"], r["e2e_ms"]], world,
+                                                    device="cuda" if world > 1 else None)
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
     pk = peaks()
-    value = world * ab["step"] / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput(ab["step"], world, ms_per_step)
     attn_gbs = ab["attention"] / (r["attn_ms"] * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -427,15 +474,9 @@ def main():
         "tokens_per_s": world * step.num_tokens / (ms_per_step * 1e-3),
         "us_per_step": {"kv_write": r["kvw_ms"] * 1e3, "paged_attn": r["attn_ms"] * 1e3,
                         "combine": r["comb_ms"] * 1e3, "total": ms_per_step * 1e3},
-        "roofline": {"bound": "hbm", "kernel": "paged_attn (plan + decode kernels)",
-                     "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": attn_gbs / pk["hbm_gbs"], "peak_source": pk["source"],
-                     "algorithmic_bytes_per_launch": ab["attention"],
-                     "traffic": (DECODE_TRAFFIC["ratio"] * ab["attention"]
-                                 if decode_sources_hash() == DECODE_TRAFFIC["sources_sha256_16"] else None),
-                     "traffic_source": DECODE_TRAFFIC["profile"] + " (scaled by algorithmic bytes)"},
+        "roofline": roofline(ab, r["attn_ms"], pk),
         "copy_probe_gbs": r["probe_gbs"],
-        "e2e": ({"value": world * ab["step"] / (e2e_max * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": ({"value": job_throughput(ab["step"], world, e2e_max), "unit": "GB/s",
                  "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": e2e_max}
                 if e2e_max == e2e_max else None),
         "gpu_launches": 4 * args.steps,
