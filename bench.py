@@ -234,6 +234,17 @@ def run_gpu(args, rank: int, world: int) -> dict:
     if status != 0:
         raise RuntimeError(f"device status {pkv.STATUS_NAMES.get(status, status)}")
 
+    graph = None
+    if args.graph:
+        # the whole layer-step captured once and replayed: no host work per step
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        stream = torch.cuda.current_stream(dev)
+
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
@@ -243,15 +254,23 @@ def run_gpu(args, rank: int, world: int) -> dict:
     with ClockSampler(dev.index) as clk:
         start.record(stream)
         for i in range(args.steps):
-            one_step(events[i])
+            if graph is not None:
+                graph.replay()
+            else:
+                one_step(events[i])
         stop.record(stream)
         torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     total_ms = start.elapsed_time(stop)
-    kvw_ms = sum(e[0].elapsed_time(e[1]) for e in events) / args.steps
-    attn_ms = sum(e[1].elapsed_time(e[2]) for e in events) / args.steps
-    comb_ms = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps
+    if graph is None:
+        kvw_ms = sum(e[0].elapsed_time(e[1]) for e in events) / args.steps
+        attn_ms = sum(e[1].elapsed_time(e[2]) for e in events) / args.steps
+        comb_ms = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps
+    else:
+        # one graph per step: the phases are not separable; attribute the step
+        kvw_ms = comb_ms = float("nan")
+        attn_ms = total_ms / args.steps
     status = pkv.workspace_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {pkv.STATUS_NAMES.get(status, status)}")
@@ -424,6 +443,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-copy-probe", dest="copy_probe", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the layer-step in a CUDA graph once and time its replays")
     ap.add_argument("--subset", type=int, default=0,
                     help="keep only the first N requests, with a compact pool (small profiling case)")
     args = ap.parse_args()
@@ -467,13 +488,15 @@ def main():
             "num_q_heads": step.num_q_heads, "num_kv_heads": step.num_kv_heads, "head_size": step.head_size,
             "block_size": step.block_size, "num_blocks": step.num_blocks,
             "kv_bytes_per_step": ab["kv_unique"], "parallelism": f"replicas x{world}",
+            "launch": "cuda graph replay" if args.graph else "eager",
             "l2": "inputs larger than L2 (KV read per step above 129 MB), no flush"
             if ab["kv_unique"] > 129e6 else "inputs fit in L2; no flush (small workload)",
         },
         "pct_of_peak": value / pk["hbm_gbs"],
         "tokens_per_s": world * step.num_tokens / (ms_per_step * 1e-3),
-        "us_per_step": {"kv_write": r["kvw_ms"] * 1e3, "paged_attn": r["attn_ms"] * 1e3,
-                        "combine": r["comb_ms"] * 1e3, "total": ms_per_step * 1e3},
+        "us_per_step": {k: (v * 1e3 if v == v else None) for k, v in
+                        (("kv_write", r["kvw_ms"]), ("paged_attn", r["attn_ms"]), ("combine", r["comb_ms"]),
+                         ("total", ms_per_step))},
         "roofline": roofline(ab, r["attn_ms"], pk),
         "copy_probe_gbs": r["probe_gbs"],
         "e2e": ({"value": job_throughput(ab["step"], world, e2e_max), "unit": "GB/s",
@@ -482,6 +505,9 @@ def main():
         "gpu_launches": 4 * args.steps,
         "clocks": r["clocks"],
     }
+    if args.graph:
+        line["roofline"]["kernel"] = "whole layer-step (kv_write + paged_attn + combine), CUDA-graph replay"
+        line["roofline"]["traffic"] = None
     if ab["kv_logical"] != ab["kv_unique"]:
         line["logical_kv_gbs_incl_l2_reuse"] = ab["kv_logical"] / (r["attn_ms"] * 1e-3) / 1e9
     if not args.no_cpu_baseline:

@@ -184,6 +184,30 @@ int pkv_paged_attn_combine(void *out, const void *workspace, size_t workspace_by
                            void *stream);
 
 /*
+ * pkv_copy_blocks — copy-on-write of shared blocks.
+ *
+ * "continuous batching and PagedAttention" tutorial, section 3.8 "COW and
+ * reference counting" (and "vLLM internals: managing the KV cache like an OS
+ * manages memory", section 2.2): a request about to write into a block that
+ * other requests still share gets a fresh block holding a copy of the
+ * shared one; its block table then points at the copy.  This call makes the
+ * copies: for every pair p,
+ *     kv_cache[block_mapping[2p+1]][h][k_or_v][:][:] =
+ *         kv_cache[block_mapping[2p]][h][k_or_v][:][:]     for every kv head h,
+ * a bit copy of all 2*16*head_size*2 bytes per kv head.  Pairs with a source
+ * or destination outside [0, num_blocks) are skipped and PKV_ERR_DEVICE_INDEX
+ * is stored in *device_status (when not NULL; never cleared by the library).
+ * A block that is the destination of one pair and the source of another in
+ * the same call has no defined result.
+ *
+ *  block_mapping   int64 [num_pairs][2]: {source block, destination block}.
+ */
+int pkv_copy_blocks(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                    int32_t head_size, int32_t block_size,
+                    const int64_t *block_mapping, int32_t num_pairs,
+                    int32_t *device_status, void *stream);
+
+/*
  * pkv_paged_attn_noalloc — paged attention that allocates nothing.
  *
  * The pages have no counterpart to this call; it exists for callers that

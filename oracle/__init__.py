@@ -68,6 +68,8 @@ def _load():
             lib.oracle_attn_row.restype = ctypes.c_int
             lib.oracle_lse_combine.argtypes = [P, P, P, P, i32, i32]
             lib.oracle_lse_combine.restype = ctypes.c_int
+            lib.oracle_copy_blocks.argtypes = [P, i64, i32, i32, i32, P, i32]
+            lib.oracle_copy_blocks.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -88,7 +90,7 @@ class use_library:
         self.saved = _load()
         lib = ctypes.CDLL(self.path)
         for name in ("oracle_max_threads", "oracle_kv_write", "oracle_paged_attn",
-                     "oracle_attn_row", "oracle_lse_combine"):
+                     "oracle_attn_row", "oracle_lse_combine", "oracle_copy_blocks"):
             src, dst = getattr(self.saved, name), getattr(lib, name)
             dst.restype = src.restype
             if src.argtypes is not None:
@@ -148,6 +150,14 @@ def kv_write(cache: np.ndarray, key, value, slot_mapping) -> None:
     assert k.shape == (T, hkv, d) and v.shape == (T, hkv, d)
     _check(_load().oracle_kv_write(_ptr(cache), nb, hkv, d, bs, _ptr(k), _ptr(v), _ptr(s), T),
            "oracle_kv_write")
+
+
+def copy_blocks(cache: np.ndarray, mapping) -> None:
+    """In-place copy-on-write block copies; mapping int64 [n, 2] of {source, destination}."""
+    nb, hkv, _, bs, d = cache.shape
+    m = _np(mapping, np.int64).reshape(-1, 2)
+    _check(_load().oracle_copy_blocks(_ptr(cache), nb, hkv, d, bs, _ptr(m), int(m.shape[0])),
+           "oracle_copy_blocks")
 
 
 def paged_attn(cache: np.ndarray, query, block_tables, seq_lens, query_start_loc,

@@ -136,6 +136,36 @@ int oracle_kv_write(uint16_t *cache, int64_t num_blocks, int32_t num_kv_heads,
     return 0;
 }
 
+/*
+ * Copy-on-write block copies ("continuous batching and PagedAttention"
+ * tutorial, section 3.8): for every pair, the destination block receives a
+ * bit copy of the source block (every kv head, K and V).  mapping: int64
+ * [num_pairs][2] = {source, destination}.  Out-of-range ids are rejected.
+ */
+int oracle_copy_blocks(uint16_t *cache, int64_t num_blocks, int32_t num_kv_heads, int32_t head_size,
+                       int32_t block_size, const int64_t *mapping, int32_t num_pairs)
+{
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0)
+        return ORACLE_EINVAL;
+    if (num_pairs == 0)
+        return 0;
+    if (!cache || !mapping)
+        return ORACLE_EINVAL;
+    for (int32_t i = 0; i < num_pairs; ++i)
+        if (mapping[2 * i] < 0 || mapping[2 * i] >= num_blocks || mapping[2 * i + 1] < 0 ||
+            mapping[2 * i + 1] >= num_blocks)
+            return ORACLE_ERANGE;
+    const size_t block_elems = cache_offset(1, 0, 0, 0, num_kv_heads, block_size, head_size);
+    for (int32_t i = 0; i < num_pairs; ++i) {
+        const int64_t src = mapping[2 * i], dst = mapping[2 * i + 1];
+        if (src == dst)
+            continue;
+        memcpy(cache + (size_t)dst * block_elems, cache + (size_t)src * block_elems,
+               block_elems * sizeof(uint16_t));
+    }
+    return 0;
+}
+
 typedef struct {
     const uint16_t *query;
     const uint16_t *cache;

@@ -12,6 +12,7 @@ Calls (same names as the C ABI without the ``pkv_`` prefix):
 * ``paged_attn(out, query, kv_cache, block_tables, seq_lens, query_start_loc,
   max_query_len, max_seq_len, scale, workspace, num_splits=0)``
 * ``paged_attn_combine(out, workspace)``
+* ``copy_blocks(kv_cache, block_mapping)`` (copy-on-write of shared blocks)
 
 plus ``paged_attn_workspace_size(...)`` (the C call's size query) and
 ``workspace_status(workspace)`` (reads the device status word).
@@ -30,7 +31,8 @@ from . import _build
 
 __all__ = [
     "BLOCK_SIZE", "PagedKVError", "load", "kv_write", "paged_attn", "paged_attn_combine",
-    "paged_attn_workspace_size", "workspace_status", "STATUS_NAMES", "library_path",
+    "paged_attn_workspace_size", "workspace_status", "STATUS_NAMES", "library_path", "copy_blocks",
+    "paged_attn_noalloc",
 ]
 
 BLOCK_SIZE = 16
@@ -72,6 +74,8 @@ def load():
         lib.pkv_paged_attn.restype = ctypes.c_int
         lib.pkv_paged_attn_combine.argtypes = [P, P, ctypes.c_size_t, i32, i32, i32, P]
         lib.pkv_paged_attn_combine.restype = ctypes.c_int
+        lib.pkv_copy_blocks.argtypes = [P, i64, i32, i32, i32, P, i32, P, P]
+        lib.pkv_copy_blocks.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -109,6 +113,18 @@ def kv_write(kv_cache: torch.Tensor, key: torch.Tensor, value: torch.Tensor, slo
     rc = load().pkv_kv_write(_ptr(kv_cache), nb, hkv, d, bs, _ptr(key), key.stride(0), _ptr(value),
                              value.stride(0), _ptr(slot_mapping), T, _ptr(device_status), _stream(kv_cache, stream))
     _check(rc, "pkv_kv_write")
+
+
+def copy_blocks(kv_cache: torch.Tensor, block_mapping: torch.Tensor, device_status: Optional[torch.Tensor] = None,
+                stream=None) -> None:
+    """Copy-on-write: block_mapping int64 [num_pairs, 2] of {source, destination} block ids."""
+    _need_cuda(kv_cache, block_mapping, device_status)
+    nb, hkv, _, bs, d = kv_cache.shape
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2 or not block_mapping.is_contiguous():
+        raise ValueError("block_mapping must be a contiguous [num_pairs, 2] int64 tensor")
+    rc = load().pkv_copy_blocks(_ptr(kv_cache), nb, hkv, d, bs, _ptr(block_mapping), int(block_mapping.shape[0]),
+                                _ptr(device_status), _stream(kv_cache, stream))
+    _check(rc, "pkv_copy_blocks")
 
 
 def paged_attn_workspace_size(num_seqs: int, num_tokens: int, max_query_len: int, max_seq_len: int,

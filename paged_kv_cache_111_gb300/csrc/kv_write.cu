@@ -1,4 +1,5 @@
-// Cache write ("reshape_and_cache"): scatter new K/V tokens into their slots.
+// Cache write ("reshape_and_cache"): scatter new K/V tokens into their slots;
+// and the copy-on-write block copy.
 //
 // "vLLM internals: managing the KV cache like an OS manages memory", section
 // 2.1 (the fused write op puts each new token's K/V into its physical block);
@@ -56,7 +57,46 @@ __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
     }
 }
 
+// Copy-on-write block copies: one CTA per (pair, kv head); the K and V pages
+// of one kv head are one contiguous run of 2*16*head_size bf16.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *cache, int64_t num_blocks, int32_t num_kv_heads,
+                                                          int32_t vec_per_page, const int64_t *mapping,
+                                                          int32_t num_pairs, int32_t *status) {
+    const int64_t unit = blockIdx.x;
+    const int64_t pair = unit / num_kv_heads;
+    const int64_t h = unit - pair * num_kv_heads;
+    if (pair >= num_pairs) return;
+    const int64_t src = __ldg(mapping + 2 * pair), dst = __ldg(mapping + 2 * pair + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && h == 0) set_status(status, PKV_ERR_DEVICE_INDEX);
+        return;
+    }
+    if (src == dst) return;
+    const uint4 *s = cache + (src * num_kv_heads + h) * vec_per_page;
+    uint4 *d = cache + (dst * num_kv_heads + h) * vec_per_page;
+    for (int v = threadIdx.x; v < vec_per_page; v += blockDim.x) d[v] = __ldg(s + v);
+}
+
 }  // namespace pkv
+
+extern "C" int pkv_copy_blocks(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads, int32_t head_size,
+                               int32_t block_size, const int64_t *block_mapping, int32_t num_pairs,
+                               int32_t *device_status, void *stream) {
+    using namespace pkv;
+    if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_SHAPE;
+    if (block_size != kBlock || (head_size != 64 && head_size != 128)) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PKV_OK;
+    if (!kv_cache || !block_mapping) return PKV_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(kv_cache) & 15u) || (reinterpret_cast<uintptr_t>(block_mapping) & 7u))
+        return PKV_ERR_ALIGNMENT;
+    const int64_t units = static_cast<int64_t>(num_pairs) * num_kv_heads;
+    if (units > 0x7fffffffLL) return PKV_ERR_SHAPE;
+    const int32_t vec_per_page = 2 * kBlock * head_size / 8;
+    copy_blocks_kernel<<<static_cast<unsigned>(units), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(kv_cache), num_blocks, num_kv_heads, vec_per_page, block_mapping, num_pairs,
+        device_status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 extern "C" int pkv_kv_write(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads, int32_t head_size,
                             int32_t block_size, const void *key, int64_t key_token_stride, const void *value,

@@ -35,6 +35,8 @@ MUTANTS = [
     ("cache write K/V swapped", "memcpy(cache + cache_offset(block, h, 0, off, num_kv_heads, block_size, head_size),\n                   key + src",
      "memcpy(cache + cache_offset(block, h, 0, off, num_kv_heads, block_size, head_size),\n                   value + src"),
     ("combine ignores weights", "const double w = exp(part_lse[s] - m);", "const double w = 1.0;"),
+    ("block copy covers one kv head", "const size_t block_elems = cache_offset(1, 0, 0, 0, num_kv_heads, block_size, head_size);",
+     "const size_t block_elems = cache_offset(0, 1, 0, 0, num_kv_heads, block_size, head_size);"),
     ("layout heads and k/v swapped", "idx = idx * (size_t)num_kv_heads + (size_t)kv_head;\n    idx = idx * 2u + (size_t)which;",
      "idx = idx * 2u + (size_t)which;\n    idx = idx * (size_t)num_kv_heads + (size_t)kv_head;"),
 ]
@@ -50,7 +52,8 @@ tests = [lambda: [pins.test_oracle_matches_torch_sdpa_on_contiguous_kv(c) for c 
          pins.test_two_keys_closed_form,
          pins.test_uniform_keys_and_zero_scale_give_the_mean_of_values,
          pins.test_split_key_range_merges_to_the_full_row,
-         pins.test_kv_write_round_trip_and_untouched_slots]
+         pins.test_kv_write_round_trip_and_untouched_slots,
+         pins.test_copy_on_write_copy_gives_the_fork_the_parents_view]
 caught = 0
 with oracle.use_library({so!r}):
     for t in tests:

@@ -377,3 +377,23 @@ def test_wrong_metadata_is_rejected():
     with pytest.raises(oracle.OracleError):          # q heads not a multiple of kv heads
         oracle.paged_attn(cache2, torch.zeros(2, 3, 64, dtype=torch.bfloat16), step.block_tables,
                           step.seq_lens, step.query_start_loc, 3, 1.0)
+
+
+def test_copy_on_write_copy_gives_the_fork_the_parents_view():
+    """The COW walk-through of the pages: block 2 copied into block 7; the fork's
+    table [0, 1, 7] then reads exactly what the parent's [0, 1, 2] reads."""
+    g = golden("cow_example.json")
+    d, hkv, H = 64, 2, 4
+    step = wl.build_step("cow2", [wl.RequestSpec(3 * 16 - 2, 1)], H, hkv, d, 16, 31, permute_blocks=False)
+    assert step.block_tables[0].tolist() == g["prompt_blocks"]
+    cache, out, _ = oracle.run_step(step)
+    oracle.copy_blocks(cache, torch.tensor([[g["prompt_blocks"][2], g["sample0_new_block"]]]))
+    assert (cache[g["sample0_new_block"]] == cache[g["prompt_blocks"][2]]).all()
+    fork_table = torch.tensor([g["sample0_table_after_write"]], dtype=torch.int32)
+    out2, _ = oracle.paged_attn(cache, step.query, fork_table, step.seq_lens, step.query_start_loc, H, step.scale)
+    assert (out2 == out).all()
+    # other blocks untouched, out-of-range pairs refused
+    before = cache.copy()
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(cache, torch.tensor([[0, 16]]))
+    assert (cache == before).all()
