@@ -31,6 +31,7 @@ struct KvWriteParams {
 // One token per CTA iteration; the CTA's threads cover that token's K and V
 // rows of every kv head, 16 bytes each.
 __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
+    pdl_trigger();                                         // the attention plan may start (it reads no cache)
     const int vpr = 1 << p.vec_shift;                      // vectors per head row
     const int per_kv = p.num_kv_heads * vpr;               // vectors of K (or V) per token
     const int per_tok = 2 * per_kv;

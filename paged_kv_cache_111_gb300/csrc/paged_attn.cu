@@ -8,7 +8,8 @@
 // Each request only sees its own tokens ("Inside vLLM: Anatomy of a
 // High-Throughput LLM Inference System", "Executing the forward pass").
 //
-// How it runs on sm_103a (three kernels, enqueued by two calls):
+// How it runs on sm_103a (kernels enqueued by two calls, back to back with
+// programmatic dependent launch):
 //  1. plan_kernel (one CTA) reads seq_lens / query_start_loc, checks them,
 //     and lists work chunks in the workspace, largest first.  A request whose
 //     query rows for one kv head fit one 16-row tile (q_r * G <= 16: decode,
@@ -274,6 +275,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int G = p.num_q_heads / p.num_kv_heads;
+    pdl_wait();       // the previous kernel on the stream may still read this workspace
+    pdl_trigger();
 
     for (int i = tid; i < kSizeBins; i += nthr) {
         bin_count[i] = 0;
@@ -451,6 +454,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * DEPTH * Cfg::kPageBytes) + warp * DEPTH;
     const uint32_t ring_u32 = smem_u32(ring);
 
+    if (lane == 0) {
+        for (int s = 0; s < DEPTH; ++s) mbar_init(&bars[s], 1);
+        if (warp == 0) tma_prefetch_desc(&kv_map);
+    }
+    fence_barrier_init();
+    __syncwarp();
+    pdl_wait();       // the plan (and the cache write before it) are complete
+    pdl_trigger();
     const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
     const int4 *req = reinterpret_cast<const int4 *>(p.ws + hdr->off_req);
@@ -458,13 +469,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
     float *part_lse = reinterpret_cast<float *>(p.ws + hdr->off_part_lse);
     float *part_o = reinterpret_cast<float *>(p.ws + hdr->off_part_o);
     const int n_items = hdr->n_chunks * p.num_kv_heads;
-
-    if (lane == 0) {
-        for (int s = 0; s < DEPTH; ++s) mbar_init(&bars[s], 1);
-        if (warp == 0) tma_prefetch_desc(&kv_map);
-    }
-    fence_barrier_init();
-    __syncwarp();
 
     const int W = gridDim.x * NW;
     const int wid = blockIdx.x * NW + warp;
@@ -712,6 +716,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 template <int HD>
 __global__ void __launch_bounds__(256) combine_kernel(__nv_bfloat16 *out, const uint8_t *ws, int32_t num_tokens,
                                                       int32_t num_q_heads) {
+    pdl_wait();       // every partial of the attention kernels is written
     const WsHeader *hdr = reinterpret_cast<const WsHeader *>(ws);
     if (hdr->magic != kMagic || hdr->num_tokens != num_tokens || hdr->num_q_heads != num_q_heads ||
         hdr->head_size != HD) {
@@ -822,8 +827,9 @@ static int launch_decode(const CUtensorMap &map, const AttnParams &p, int grid, 
             done_mask |= bit;
         }
     }
-    decode_kernel<HD, NW, DEPTH><<<grid, NW * 32, Cfg::kSmem, stream>>>(map, p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    if (launch_pdl(decode_kernel<HD, NW, DEPTH>, dim3(grid), dim3(NW * 32), Cfg::kSmem, stream, map, p) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
 }
 
 // decode tiling per head size: warps per CTA, ring stages per warp, CTAs per SM
@@ -904,8 +910,7 @@ extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_
     const bool may_prefill = prefill_ok && static_cast<int64_t>(max_query_len) * G > kDecodeTileMaxRows;
     pp.prefill_ok = prefill_ok ? 1 : 0;
     pp.lay = lay;
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(pp);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess) return PKV_ERR_CUDA;
 
     AttnParams ap;
     ap.out = static_cast<__nv_bfloat16 *>(out);
@@ -956,11 +961,12 @@ extern "C" int pkv_paged_attn_combine(void *out, const void *workspace, size_t w
     const int64_t rows = static_cast<int64_t>(num_tokens) * num_q_heads;
     const int64_t grid = (rows + 7) / 8;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (head_size == 64)
-        combine_kernel<64><<<static_cast<unsigned>(grid), 256, 0, st>>>(
-            static_cast<__nv_bfloat16 *>(out), static_cast<const uint8_t *>(workspace), num_tokens, num_q_heads);
-    else
-        combine_kernel<128><<<static_cast<unsigned>(grid), 256, 0, st>>>(
-            static_cast<__nv_bfloat16 *>(out), static_cast<const uint8_t *>(workspace), num_tokens, num_q_heads);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
+    const uint8_t *w = static_cast<const uint8_t *>(workspace);
+    const cudaError_t e =
+        head_size == 64 ? launch_pdl(combine_kernel<64>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, o, w,
+                                     num_tokens, num_q_heads)
+                        : launch_pdl(combine_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, o, w,
+                                     num_tokens, num_q_heads);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

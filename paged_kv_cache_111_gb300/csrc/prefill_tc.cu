@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t sK = smem_u32(smem + Cfg::kOffK);
     const uint32_t sV = smem_u32(smem + Cfg::kOffV);
 
+    pdl_wait();       // the plan, the cache write and the decode kernel are complete
+    pdl_trigger();
     const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
     const int n_items = hdr->n_ptiles * p.num_kv_heads;
@@ -470,9 +472,10 @@ static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, con
             done_mask |= bit;
         }
     }
-    prefill_kernel<HD><<<static_cast<unsigned>(grid), 256, Cfg::kSmem, stream>>>(
-        kvm, static_cast<const __nv_bfloat16 *>(query), q_stride, p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    if (launch_pdl(prefill_kernel<HD>, dim3(static_cast<unsigned>(grid)), dim3(256), Cfg::kSmem, stream, kvm,
+                   static_cast<const __nv_bfloat16 *>(query), q_stride, p) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
 }
 
 int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
