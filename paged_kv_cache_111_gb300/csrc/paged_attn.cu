@@ -300,9 +300,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if ((tid & 31) == 0 && mine) atomicAdd(&total_pages, mine);
     __syncthreads();
     if (tid == 0) {
-        // about 8 chunks per warp of the decode grid, 4..64 pages each
+        // about 3 chunks per warp of the decode grid, 4..64 pages each
         const unsigned long long work = total_pages * (unsigned long long)p.num_kv_heads;
-        const unsigned long long target = 8ull * (unsigned long long)max(p.total_warps, 1);
+        const unsigned long long target = 3ull * (unsigned long long)max(p.total_warps, 1);
         const unsigned long long per = (work + target - 1) / target;
         pages_per_split = (int)min(64ull, max(4ull, per));
     }
