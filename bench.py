@@ -94,6 +94,35 @@ def algorithmic_bytes(step: wl.Step) -> dict:
             "step": attn + kvw, "flops": flops}
 
 
+def shared_prefix_blocks(step: wl.Step) -> int:
+    """Leading table blocks every request shares with request 0 (what a prefix
+    cache knows when it hands out the blocks), bounded by every request's
+    context; 0 when fewer than two requests or nothing is shared."""
+    if step.num_seqs < 2:
+        return 0
+    t = step.block_tables
+    same = (t == t[0:1]).all(dim=0).tolist()
+    k = 0
+    while k < len(same) and same[k]:
+        k += 1
+    ctx_min = int(step.context_lens.min())
+    return min(k, ctx_min // step.block_size)
+
+
+def launches_per_step(step: wl.Step, prefix_blocks: int) -> int:
+    """Kernels of one layer-step: kv_write, plan, decode, combine; the prefill
+    kernel when some request has more than 64 rows (q_r * G) and the head
+    layout has a tensor-core tile; the shared-prefix kernel when asked for."""
+    G = step.num_q_heads // step.num_kv_heads
+    tile_ok = step.head_size in (64, 128) and 128 % G == 0
+    n = 4
+    if tile_ok and step.max_query_len * G > 64:
+        n += 1
+    if tile_ok and prefix_blocks > 0:
+        n += 1
+    return n
+
+
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -206,12 +235,23 @@ def run_gpu(args, rank: int, world: int) -> dict:
         b = min(hs.numel(), a + chunk)
         pkv.kv_write(pool, hk[a:b].to(dev), hv[a:b].to(dev), hs[a:b].to(dev))
     del hk, hv
-    ws_bytes = pkv.paged_attn_workspace_size(step.num_seqs, T, step.max_query_len, step.max_seq_len, H,
-                                             step.num_kv_heads, d)
+    K = shared_prefix_blocks(step) if args.shared_prefix_blocks < 0 else args.shared_prefix_blocks
+    if K:
+        ws_bytes = pkv.paged_attn_shared_prefix_workspace_size(step.num_seqs, T, step.max_query_len,
+                                                               step.max_seq_len, H, step.num_kv_heads, d, K)
+    else:
+        ws_bytes = pkv.paged_attn_workspace_size(step.num_seqs, T, step.max_query_len, step.max_seq_len, H,
+                                                 step.num_kv_heads, d)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     maxq, maxs = step.max_query_len, step.max_seq_len
+
+    def attention(q, tables, lens, qsl):
+        if K:
+            pkv.paged_attn_shared_prefix(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, K, ws)
+        else:
+            pkv.paged_attn(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, ws)
 
     def one_step(ev=None):
         if ev is not None:
@@ -219,8 +259,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         pkv.kv_write(pool, to["key"], to["value"], to["slot_mapping"])
         if ev is not None:
             ev[1].record(stream)
-        pkv.paged_attn(out, to["query"], pool, to["block_tables"], to["seq_lens"], to["query_start_loc"],
-                       maxq, maxs, step.scale, ws)
+        attention(to["query"], to["block_tables"], to["seq_lens"], to["query_start_loc"])
         if ev is not None:
             ev[2].record(stream)
         pkv.paged_attn_combine(out, ws)
@@ -288,8 +327,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         for f, t in host_in.items():
             dev_in[f].copy_(t, non_blocking=True)
         pkv.kv_write(pool, dev_in["key"], dev_in["value"], dev_in["slot_mapping"])
-        pkv.paged_attn(out, dev_in["query"], pool, dev_in["block_tables"], dev_in["seq_lens"],
-                       dev_in["query_start_loc"], maxq, maxs, step.scale, ws)
+        attention(dev_in["query"], dev_in["block_tables"], dev_in["seq_lens"], dev_in["query_start_loc"])
         pkv.paged_attn_combine(out, ws)
         host_out.copy_(out, non_blocking=True)
 
@@ -327,7 +365,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
         probe_gbs = 2 * n * 2 / (best * 1e-3) / 1e9
         del a, b
 
-    return {"step": step, "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
+    return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K),
+            "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
             "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "probe_gbs": probe_gbs}
 
 
@@ -445,6 +484,9 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--graph", action="store_true",
                     help="capture the layer-step in a CUDA graph once and time its replays")
+    ap.add_argument("--shared-prefix-blocks", type=int, default=-1,
+                    help="cascade over this many shared leading table blocks (pkv_paged_attn_shared_prefix); "
+                         "-1: the prefix every request's table shares with request 0's, 0: plain paged_attn")
     ap.add_argument("--subset", type=int, default=0,
                     help="keep only the first N requests, with a compact pool (small profiling case)")
     args = ap.parse_args()
@@ -489,6 +531,7 @@ def main():
             "block_size": step.block_size, "num_blocks": step.num_blocks,
             "kv_bytes_per_step": ab["kv_unique"], "parallelism": f"replicas x{world}",
             "launch": "cuda graph replay" if args.graph else "eager",
+            "shared_prefix_blocks": r["shared_prefix_blocks"],
             "l2": "inputs larger than L2 (KV read per step above 129 MB), no flush"
             if ab["kv_unique"] > 129e6 else "inputs fit in L2; no flush (small workload)",
         },
@@ -502,7 +545,7 @@ def main():
         "e2e": ({"value": job_throughput(ab["step"], world, e2e_max), "unit": "GB/s",
                  "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": e2e_max}
                 if e2e_max == e2e_max else None),
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
     }
     if args.graph:

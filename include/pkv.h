@@ -163,6 +163,42 @@ int pkv_paged_attn(void *out, const void *query, int64_t query_token_stride,
                    void *stream);
 
 /*
+ * pkv_paged_attn_shared_prefix — pkv_paged_attn for a batch whose requests
+ * share a prefix of their block tables (cascade attention).
+ *
+ * Requests that share a prefix keep one physical copy of its blocks, each
+ * block referenced from every sharer's table ("vLLM internals: managing the
+ * KV cache like an OS manages memory", section 2.2: shared blocks with
+ * reference counts; "continuous batching and PagedAttention" tutorial,
+ * sections 3.5 and 5.2: parallel sampling, beam search and prefix caching
+ * share the prompt's blocks).  This call computes exactly the result of
+ * pkv_paged_attn (same arguments, same formula, same combine afterwards),
+ * but reads the shared blocks once per kv head for all sharers: the keys of
+ * the first `shared_prefix_blocks` table entries are attended by every
+ * sharing row together on tensor-core tiles, cut into a few key ranges that
+ * become splits of that row, and merged with the row's own keys by the
+ * log-sum-exp combine (at most 32 splits per row in all).
+ *
+ * A request takes this path when its first shared_prefix_blocks table entries
+ * equal request 0's, its query rows fit one decode tile (q_r * G <= 16) and
+ * its context covers the prefix (L_r - q_r >= 16 * shared_prefix_blocks;
+ * request 0's must too).  Other requests are computed as by pkv_paged_attn.
+ * shared_prefix_blocks = 0 is pkv_paged_attn.  The workspace size depends on
+ * shared_prefix_blocks being zero or not.
+ */
+int pkv_paged_attn_shared_prefix(void *out, const void *query, int64_t query_token_stride,
+                                 const void *kv_cache, int64_t num_blocks,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *seq_lens, const int32_t *query_start_loc,
+                                 int32_t num_seqs, int32_t num_tokens,
+                                 int32_t max_query_len, int32_t max_seq_len,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                 int32_t block_size, float scale, int32_t num_splits,
+                                 int32_t shared_prefix_blocks,
+                                 void *workspace, size_t workspace_bytes, size_t *workspace_needed,
+                                 void *stream);
+
+/*
  * pkv_paged_attn_combine — the log-sum-exp merge of split rows.
  *
  * For every row (t, h) that pkv_paged_attn split into n parts with partial

@@ -13,6 +13,8 @@ Calls (same names as the C ABI without the ``pkv_`` prefix):
   max_query_len, max_seq_len, scale, workspace, num_splits=0)``
 * ``paged_attn_combine(out, workspace)``
 * ``copy_blocks(kv_cache, block_mapping)`` (copy-on-write of shared blocks)
+* ``paged_attn_shared_prefix(..., shared_prefix_blocks, workspace)`` (cascade:
+  a batch sharing a table prefix reads the shared blocks once)
 
 plus ``paged_attn_workspace_size(...)`` (the C call's size query) and
 ``workspace_status(workspace)`` (reads the device status word).
@@ -32,7 +34,7 @@ from . import _build
 __all__ = [
     "BLOCK_SIZE", "PagedKVError", "load", "kv_write", "paged_attn", "paged_attn_combine",
     "paged_attn_workspace_size", "workspace_status", "STATUS_NAMES", "library_path", "copy_blocks",
-    "paged_attn_noalloc",
+    "paged_attn_noalloc", "paged_attn_shared_prefix", "paged_attn_shared_prefix_workspace_size",
 ]
 
 BLOCK_SIZE = 16
@@ -76,6 +78,10 @@ def load():
         lib.pkv_paged_attn_combine.restype = ctypes.c_int
         lib.pkv_copy_blocks.argtypes = [P, i64, i32, i32, i32, P, i32, P, P]
         lib.pkv_copy_blocks.restype = ctypes.c_int
+        lib.pkv_paged_attn_shared_prefix.argtypes = [P, P, i64, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                                     i32, i32, ctypes.c_float, i32, i32, P, ctypes.c_size_t,
+                                                     ctypes.POINTER(ctypes.c_size_t), P]
+        lib.pkv_paged_attn_shared_prefix.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -161,6 +167,44 @@ def paged_attn(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Tensor, b
                                int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                ctypes.byref(need), _stream(out, stream))
     _check(rc, "pkv_paged_attn")
+
+
+def paged_attn_shared_prefix_workspace_size(num_seqs: int, num_tokens: int, max_query_len: int, max_seq_len: int,
+                                            num_q_heads: int, num_kv_heads: int, head_size: int,
+                                            shared_prefix_blocks: int) -> int:
+    """Bytes of workspace pkv_paged_attn_shared_prefix needs (no GPU work)."""
+    need = ctypes.c_size_t(0)
+    max_blocks = max((max_seq_len + BLOCK_SIZE - 1) // BLOCK_SIZE, shared_prefix_blocks)
+    rc = load().pkv_paged_attn_shared_prefix(None, None, num_q_heads * head_size, None, 1, None, max_blocks, None,
+                                             None, num_seqs, num_tokens, max_query_len, max_seq_len, num_q_heads,
+                                             num_kv_heads, head_size, BLOCK_SIZE, ctypes.c_float(1.0), 0,
+                                             shared_prefix_blocks, None, 0, ctypes.byref(need), None)
+    if rc not in (0, 1, 5):
+        _check(rc, "pkv_paged_attn_shared_prefix (size query)")
+    return int(need.value)
+
+
+def paged_attn_shared_prefix(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Tensor,
+                             block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                             max_query_len: int, max_seq_len: int, scale: float, shared_prefix_blocks: int,
+                             workspace: torch.Tensor, num_splits: int = 0, stream=None) -> None:
+    """paged_attn with the first shared_prefix_blocks table entries shared by the batch (cascade)."""
+    _need_cuda(out, query, kv_cache, block_tables, seq_lens, query_start_loc, workspace)
+    nb, hkv, _, bs, d = kv_cache.shape
+    T, H = int(query.shape[0]), int(query.shape[1])
+    if query.stride(2) != 1 or query.stride(1) != d:
+        raise ValueError("query must be [T, H, d] with contiguous heads")
+    if not out.is_contiguous() or tuple(out.shape) != (T, H, d):
+        raise ValueError("out must be a contiguous [T, H, d] tensor")
+    if block_tables.dim() != 2 or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous [num_seqs, max_blocks] tensor")
+    need = ctypes.c_size_t(0)
+    rc = load().pkv_paged_attn_shared_prefix(
+        _ptr(out), _ptr(query), query.stride(0), _ptr(kv_cache), nb, _ptr(block_tables), int(block_tables.shape[1]),
+        _ptr(seq_lens), _ptr(query_start_loc), int(seq_lens.shape[0]), T, int(max_query_len), int(max_seq_len), H,
+        hkv, d, bs, ctypes.c_float(scale), int(num_splits), int(shared_prefix_blocks), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), ctypes.byref(need), _stream(out, stream))
+    _check(rc, "pkv_paged_attn_shared_prefix")
 
 
 def paged_attn_combine(out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:

@@ -10,7 +10,7 @@ constexpr int kMaxSplits = 32;        // key ranges per split row, at most
 constexpr int kDecodeTileMaxRows = 64;  // longer requests go to the tensor-core prefill kernel
 constexpr int kPrefillRows = 128;     // rows of one prefill tile (M of the MMA)
 constexpr int kPrefillKeys = 128;     // keys of one prefill KV tile (N of S = Q K^T)
-constexpr int32_t kMagic = 0x504B5632;  // "PKV2"
+constexpr int32_t kMagic = 0x504B5633;  // "PKV3"
 
 struct WsHeader {
     int32_t status;          // device status word (first 4 bytes)
@@ -22,24 +22,34 @@ struct WsHeader {
     int32_t num_seqs;
     int32_t pages_per_split;
     int32_t n_ptiles;        // prefill-kernel tiles
-    int32_t pad_;
+    int32_t n_crows;         // rows of the shared-prefix (cascade) pass, per kv head
+    int32_t prefix_blocks;   // shared prefix in blocks (0: no cascade)
+    int32_t prefix_parts;    // the prefix keys are cut into this many splits (KV-tile ranges)
+    int32_t pad_[2];
     int64_t off_req;         // int4 [num_seqs]: {splits (0: refused), partial row base, first chunk, chunks}
     int64_t off_tok;         // int2 [num_tokens]: {request, index in request} (-1 if none)
     int64_t off_chunks;      // int4 [max_chunks]: {request, split or tile, page begin, page end}
     int64_t off_ptiles;      // int4 [max_ptiles]: {request, q tile, kv tiles, 0}
+    int64_t off_crows;       // int4 [max_crows]: {token, request, query index, q head in group}
     int64_t off_part_lse;    // float [max_prow]
     int64_t off_part_o;      // float [max_prow][head_size]
     int64_t max_chunks;
     int64_t max_ptiles;
+    int64_t max_crows;
     int64_t max_prow;
     int64_t prow_used;
 };
 static_assert(sizeof(WsHeader) <= 256, "header must fit its 256-byte slot");
 
 struct WsLayout {
-    int64_t off_req, off_tok, off_chunks, off_ptiles, off_part_lse, off_part_o, total;
-    int64_t max_chunks, max_ptiles, max_prow;
+    int64_t off_req, off_tok, off_chunks, off_ptiles, off_crows, off_part_lse, off_part_o, total;
+    int64_t max_chunks, max_ptiles, max_crows, max_prow;
+    int32_t prefix_parts;     // splits of the shared prefix (0: no cascade)
 };
+
+// CTAs the shared-prefix pass aims for: one per SM of a 152-SM part (the
+// kernel holds all of an SM's tensor memory).  Only the balance depends on it.
+constexpr int kPrefixTargetCtas = 152;
 
 struct PrefillParams {
     __nv_bfloat16 *out;
@@ -53,6 +63,13 @@ struct PrefillParams {
     int32_t lo_tiles;         // leading KV tiles whose P always enters P V as a bf16 pair
     uint8_t *ws;
 };
+
+// The shared-prefix (cascade) pass on the same kernel: rows of every request
+// that shares the first `prefix_blocks` blocks of its table with request 0
+// attend once to those blocks' keys, cut into `prefix_parts` ranges of KV
+// tiles; range i is split i of each row.
+int launch_prefix(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
+                  int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream);
 
 // Is the tensor-core prefill kernel available for this head layout?
 inline bool prefill_supported(int num_q_heads, int num_kv_heads, int head_size) {

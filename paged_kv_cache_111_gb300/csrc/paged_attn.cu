@@ -44,7 +44,7 @@ constexpr int kSizeBins = 256;      // counting-sort bins for chunk sizes (pages
 static inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_query_len, int64_t max_seq_len,
-                          int64_t num_q_heads, int64_t num_kv_heads, int64_t head_size) {
+                          int64_t num_q_heads, int64_t num_kv_heads, int64_t head_size, int64_t prefix_blocks) {
     const int64_t G = num_q_heads / num_kv_heads;
     WsLayout w;
     // split rows: requests with q_r * G <= 16, so q_r <= 16 / G
@@ -53,7 +53,22 @@ static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_quer
     if (split_tokens > num_tokens) split_tokens = num_tokens;
     const int64_t max_pages = (max_seq_len + kBlock - 1) / kBlock;
     const int64_t splits = max_pages < kMaxSplits ? (max_pages > 0 ? max_pages : 1) : kMaxSplits;
-    w.max_prow = split_tokens * num_q_heads * splits;
+    // the shared prefix is cut into prefix_parts KV-tile ranges so that its
+    // tiles (row tiles x kv heads x parts) about fill the GPU; every range is
+    // non-empty
+    w.max_crows = prefix_blocks > 0 ? split_tokens * G : 0;
+    w.prefix_parts = 0;
+    if (prefix_blocks > 0) {
+        const int64_t kv_tiles = (prefix_blocks * kBlock + kPrefillKeys - 1) / kPrefillKeys;
+        const int64_t row_tiles = (w.max_crows + kPrefillRows - 1) / kPrefillRows;
+        int64_t parts = kPrefixTargetCtas / (row_tiles * num_kv_heads > 0 ? row_tiles * num_kv_heads : 1);
+        parts = parts < 1 ? 1 : (parts > 8 ? 8 : parts);
+        parts = parts > kv_tiles ? kv_tiles : parts;
+        const int64_t per = (kv_tiles + parts - 1) / parts;
+        w.prefix_parts = static_cast<int32_t>((kv_tiles + per - 1) / per);
+    }
+    // a cascade request's splits are its prefix ranges plus its own chunks
+    w.max_prow = split_tokens * num_q_heads * (splits + w.prefix_parts);
     (void)max_query_len;
     // chunks: split requests give <= splits each; tiled ones ceil(q_r G / 16) <= q_r G / 16 + 1
     w.max_chunks = num_seqs * splits + (num_tokens * G + 15) / 16 + num_seqs;
@@ -68,6 +83,8 @@ static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_quer
     off = align256(off + 16 * w.max_chunks);
     w.off_ptiles = off;
     off = align256(off + 16 * w.max_ptiles);
+    w.off_crows = off;
+    off = align256(off + 16 * w.max_crows);
     w.off_part_lse = off;
     off = align256(off + 4 * w.max_prow);
     w.off_part_o = off;
@@ -87,6 +104,8 @@ struct PlanParams {
     int32_t num_splits;       // 0 = auto
     int32_t total_warps;      // warps of the decode grid (for the automatic split size)
     int32_t prefill_ok;       // long requests go to the tensor-core prefill kernel
+    int32_t prefix_blocks;    // shared prefix of the tables in blocks (0: no cascade)
+    const int32_t *block_tables;
     WsLayout lay;
 };
 
@@ -119,10 +138,23 @@ struct ReqPlan {
     int n_chunks;     // decode-kernel chunks (modes 0, 1) or prefill tiles (mode 2)
     int pages;        // key pages of the request (mode 0)
     int per_split;    // pages per split (mode 0)
+    int first;        // first page of the decode chunks (mode 0): the shared prefix is split 0
 };
 
-__device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split) {
-    ReqPlan rp{0, 0, 0, 0, 0, 0, 0, 0};
+// Mode 0 request r may take the cascade path: its table starts with request
+// 0's first prefix_blocks blocks (`differs`: it does not), and every one of
+// its rows sees all of them.
+__device__ bool cascade_eligible(const PlanParams &p, int r, bool differs) {
+    const int K = p.prefix_blocks;
+    if (K <= 0 || differs) return false;
+    const int q = p.qsl[r + 1] - p.qsl[r];
+    const int G = p.num_q_heads / p.num_kv_heads;
+    if (q <= 0 || q * G > 16 || p.seq_lens[0] - (p.qsl[1] - p.qsl[0]) < K * kBlock) return false;
+    return p.seq_lens[r] - q >= K * kBlock && K <= p.max_blocks_per_seq;
+}
+
+__device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split, bool cascade = false) {
+    ReqPlan rp{0, 0, 0, 0, 0, 0, 0, 0, 0};
     const int G = p.num_q_heads / p.num_kv_heads;
     const int q0 = p.qsl[r], q1 = p.qsl[r + 1];
     const int q = q1 - q0;
@@ -138,15 +170,19 @@ __device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split)
     if (rp.rows <= 16) {
         rp.mode = 0;
         rp.pages = div_up(L, kBlock);
+        rp.first = cascade ? p.prefix_blocks : 0;
+        const int span = rp.pages - rp.first;            // >= 1: a cascade row sees a key past the prefix
         int n;
+        // at most kMaxSplits splits in all (the combine's limit), prefix ranges included
+        const int cap = cascade ? kMaxSplits - p.lay.prefix_parts : kMaxSplits;
         if (p.num_splits > 0) {
-            n = min(min(p.num_splits, kMaxSplits), rp.pages);
+            n = min(min(p.num_splits, cap), span);
         } else {
-            const int per = max(pages_per_split, div_up(rp.pages, kMaxSplits));
-            n = div_up(rp.pages, per);
+            const int per = max(pages_per_split, div_up(span, cap));
+            n = div_up(span, per);
         }
-        rp.per_split = div_up(rp.pages, n);
-        rp.n_chunks = div_up(rp.pages, rp.per_split);   // no empty split
+        rp.per_split = div_up(span, n);
+        rp.n_chunks = div_up(span, rp.per_split);        // no empty split
     } else if (p.prefill_ok && rp.rows > kDecodeTileMaxRows) {
         rp.mode = 2;
         rp.n_chunks = div_up(rp.rows, kPrefillRows);
@@ -161,7 +197,7 @@ __device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split)
 // ending before request row `row_end` sees keys 0 .. ctx + last_row / G.
 __device__ __forceinline__ int2 chunk_pages(const ReqPlan &rp, int G, int k) {
     if (rp.mode == 0) {
-        const int b = k * rp.per_split;
+        const int b = rp.first + k * rp.per_split;
         return make_int2(b, min(rp.pages, b + rp.per_split));
     }
     const int row_end = rp.mode == 1 ? 16 * k + 16 : kPrefillRows * (k + 1);
@@ -272,9 +308,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     int2 *tok = reinterpret_cast<int2 *>(p.ws + p.lay.off_tok);
     int4 *chunks = reinterpret_cast<int4 *>(p.ws + p.lay.off_chunks);
     int4 *ptiles = reinterpret_cast<int4 *>(p.ws + p.lay.off_ptiles);
+    int4 *crows = reinterpret_cast<int4 *>(p.ws + p.lay.off_crows);
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int G = p.num_q_heads / p.num_kv_heads;
+    __shared__ int2 ctotals;
     pdl_wait();       // the previous kernel on the stream may still read this workspace
     pdl_trigger();
 
@@ -287,14 +325,42 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         bad = p.qsl[0] != 0;
     }
     for (int t = tid; t < p.num_tokens; t += nthr) tok[t] = make_int2(-1, -1);
+    // req[r].x is first the flag "table differs from request 0's in the prefix"
+    if (p.prefix_blocks > 0)
+        for (int r = tid; r < p.num_seqs; r += nthr) req[r] = make_int4(0, 0, 0, 0);
     __syncthreads();
+    if (p.prefix_blocks > 0 && p.prefix_blocks <= p.max_blocks_per_seq) {
+        // every (request, prefix block) pair at once, four loads in flight per thread
+        const int K = p.prefix_blocks;
+        const int64_t pairs = static_cast<int64_t>(p.num_seqs - 1) * K;
+        for (int64_t i0 = tid; i0 < pairs; i0 += 4 * static_cast<int64_t>(nthr)) {
+            int32_t a[4], b[4];
+            int rr[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t i = i0 + static_cast<int64_t>(u) * nthr;
+                rr[u] = i < pairs ? 1 + static_cast<int>(i / K) : 0;
+                const int blk = i < pairs ? static_cast<int>(i % K) : 0;
+                a[u] = __ldg(p.block_tables + static_cast<int64_t>(rr[u]) * p.max_blocks_per_seq + blk);
+                b[u] = __ldg(p.block_tables + blk);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (rr[u] > 0 && a[u] != b[u]) req[rr[u]].x = 1;
+        }
+        __syncthreads();                                 // uniform: prefix_blocks is a kernel parameter
+    }
 
     // pass 1: total key pages of split requests (sets the automatic split size)
     unsigned long long mine = 0;
     for (int r = tid; r < p.num_seqs; r += nthr) {
         const int q = p.qsl[r + 1] - p.qsl[r];
         const int L = p.seq_lens[r];
-        if (q > 0 && q * G <= 16 && L >= q) mine += (unsigned long long)div_up(L, kBlock);
+        if (q > 0 && q * G <= 16 && L >= q) {
+            // a cascade request's prefix pages are not decode-kernel work
+            const bool casc = cascade_eligible(p, r, p.prefix_blocks > 0 && req[r].x != 0);
+            mine += (unsigned long long)(div_up(L, kBlock) - (casc ? p.prefix_blocks : 0));
+        }
     }
     mine = warp_sum_u64(mine);
     if ((tid & 31) == 0 && mine) atomicAdd(&total_pages, mine);
@@ -313,32 +379,51 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     // a contiguous range of requests so one block scan gives every base
     const int per_thr = div_up(max(p.num_seqs, 1), nthr);
     const int r_begin = min(p.num_seqs, tid * per_thr), r_end = min(p.num_seqs, r_begin + per_thr);
-    int my_chunks = 0, my_prows = 0;
+    // (a cascade request's splits are its suffix chunks plus the shared prefix)
+    int my_chunks = 0, my_prows = 0, my_crows = 0;
+    unsigned my_casc = 0;                            // bit k: request r_begin + k takes the cascade path
     for (int r = r_begin; r < r_end; ++r) {
-        const ReqPlan rp = plan_request(p, r, pps);
+        const bool casc = cascade_eligible(p, r, p.prefix_blocks > 0 && req[r].x != 0);
+        if (casc && r - r_begin < 32) my_casc |= 1u << (r - r_begin);
+        const ReqPlan rp = plan_request(p, r, pps, casc && r - r_begin < 32);
         if (!rp.valid) {
             bad = 1;
             continue;
         }
         my_chunks += rp.n_chunks;
-        if (rp.mode == 0 && rp.n_chunks > 1) my_prows += rp.q * p.num_q_heads * rp.n_chunks;
+        const int nsplit = rp.n_chunks + (rp.first > 0 ? p.lay.prefix_parts : 0);
+        if (rp.mode == 0 && nsplit > 1) my_prows += rp.q * p.num_q_heads * nsplit;
+        if (rp.first > 0) my_crows += rp.rows;
     }
     const int2 pre = block_scan2(my_chunks, my_prows, warp_tot, &totals);
+    const int2 cpre = block_scan2(my_crows, 0, warp_tot, &ctotals);
     const int n_total = totals.x;
-    const bool fits = n_total <= p.lay.max_chunks + p.lay.max_ptiles && totals.y <= p.lay.max_prow;
+    const bool fits = n_total <= p.lay.max_chunks + p.lay.max_ptiles && totals.y <= p.lay.max_prow &&
+                      ctotals.x <= p.lay.max_crows;
     {
-        int cb = pre.x, pbase = pre.y;
+        int cb = pre.x, pbase = pre.y, crow = cpre.x;
         for (int r = r_begin; r < r_end; ++r) {
-            const ReqPlan rp = plan_request(p, r, pps);
+            const bool casc = (my_casc >> (r - r_begin)) & 1u;
+            const ReqPlan rp = plan_request(p, r, pps, casc);
             const int n = (rp.valid && fits) ? rp.n_chunks : 0;
-            const bool split = rp.valid && fits && rp.mode == 0 && rp.n_chunks > 1;
-            // {splits (0: request refused), partial row base, first chunk, chunks}
-            req[r] = make_int4(rp.valid && fits ? (split ? rp.n_chunks : 1) : 0, split ? pbase : 0, cb, n);
+            const int nsplit = rp.n_chunks + (rp.first > 0 ? p.lay.prefix_parts : 0);
+            const bool split = rp.valid && fits && rp.mode == 0 && nsplit > 1;
+            // {splits (0: request refused), partial row base, first chunk, chunks};
+            // a cascade request has splits = chunks + prefix_parts (>= 1), which
+            // no other request has
+            req[r] = make_int4(rp.valid && fits ? (split ? nsplit : 1) : 0, split ? pbase : 0, cb, n);
+            if (rp.valid && fits && rp.first > 0) {
+                const int q0 = p.qsl[r];
+                for (int row = 0; row < rp.rows; ++row) crows[crow + row] = make_int4(q0 + row / G, r, row / G, row % G);
+                crow += rp.rows;
+            }
             cb += n;
-            if (split) pbase += rp.q * p.num_q_heads * rp.n_chunks;
+            if (split) pbase += rp.q * p.num_q_heads * nsplit;
         }
     }
     __syncthreads();
+
+    auto is_cascade = [&](const int4 &ri) { return p.lay.prefix_parts > 0 && ri.x == ri.w + p.lay.prefix_parts; };
 
     // pass 3: per chunk, its size bin (request found by binary search on the bases)
     auto owner = [&](int c) {
@@ -355,7 +440,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     for (int c = tid; c < n_emit; c += nthr) {
         const int r = owner(c);
         const int4 ri = req[r];
-        const ReqPlan rp = plan_request(p, r, pps);
+        const ReqPlan rp = plan_request(p, r, pps, is_cascade(ri));
         const int2 pg = chunk_pages(rp, G, c - ri.z);
         if (rp.mode == 2) agg_inc(pbin_count, min(pg.y, kSizeBins - 1));
         else agg_inc(bin_count, min(pg.y - pg.x, kSizeBins - 1));
@@ -377,15 +462,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     for (int c = tid; c < n_emit; c += nthr) {
         const int r = owner(c);
         const int4 ri = req[r];
-        const ReqPlan rp = plan_request(p, r, pps);
+        const bool casc = is_cascade(ri);
+        const ReqPlan rp = plan_request(p, r, pps, casc);
         const int k = c - ri.z;
         const int2 pg = chunk_pages(rp, G, k);
         if (rp.mode == 2) {
             const int pos = agg_inc(pbin_cursor, min(pg.y, kSizeBins - 1));
             if (pos < p.lay.max_ptiles) ptiles[pos] = make_int4(r, k, pg.y, 0);
         } else {
+            // chunk {request, split index (cascade: after the prefix ranges), pages}
             const int pos = agg_inc(bin_cursor, min(pg.y - pg.x, kSizeBins - 1));
-            if (pos < p.lay.max_chunks) chunks[pos] = make_int4(r, k, pg.x, pg.y);
+            if (pos < p.lay.max_chunks) chunks[pos] = make_int4(r, k + (casc ? p.lay.prefix_parts : 0), pg.x, pg.y);
         }
     }
     // token owners, one thread per token: the last request starting at or
@@ -415,8 +502,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         hdr->off_ptiles = p.lay.off_ptiles;
         hdr->off_part_lse = p.lay.off_part_lse;
         hdr->off_part_o = p.lay.off_part_o;
+        hdr->off_crows = p.lay.off_crows;
+        hdr->n_crows = fits ? ctotals.x : 0;
+        hdr->prefix_blocks = p.prefix_blocks;
+        hdr->prefix_parts = p.lay.prefix_parts;
         hdr->max_chunks = p.lay.max_chunks;
         hdr->max_ptiles = p.lay.max_ptiles;
+        hdr->max_crows = p.lay.max_crows;
         hdr->max_prow = p.lay.max_prow;
         hdr->prow_used = totals.y;
     }
@@ -839,18 +931,20 @@ template <> struct DecodeTiling<128> { static constexpr int NW = 4, DEPTH = 3, C
 
 }  // namespace pkv
 
-extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_stride, const void *kv_cache,
-                              int64_t num_blocks, const int32_t *block_tables, int32_t max_blocks_per_seq,
-                              const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
-                              int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
-                              int32_t num_kv_heads, int32_t head_size, int32_t block_size, float scale,
-                              int32_t num_splits, void *workspace, size_t workspace_bytes, size_t *workspace_needed,
-                              void *stream) {
-    using namespace pkv;
+namespace pkv {
+
+static int paged_attn_impl(void *out, const void *query, int64_t query_token_stride, const void *kv_cache,
+                           int64_t num_blocks, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                           int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_size, int32_t block_size, float scale,
+                           int32_t num_splits, int32_t prefix_blocks, void *workspace, size_t workspace_bytes,
+                           size_t *workspace_needed, void *stream) {
     // ---- host-side validation: nothing is enqueued on error ----
     if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_query_len < 0 ||
-        max_seq_len < 0 || max_blocks_per_seq < 0 || num_splits < 0)
+        max_seq_len < 0 || max_blocks_per_seq < 0 || num_splits < 0 || prefix_blocks < 0)
         return PKV_ERR_SHAPE;
+    if (prefix_blocks > max_blocks_per_seq) return PKV_ERR_SHAPE;
     if (block_size != kBlock || (head_size != 64 && head_size != 128)) return PKV_ERR_UNSUPPORTED;
     if (num_q_heads % num_kv_heads) return PKV_ERR_SHAPE;
     if (num_tokens > 0 && num_seqs == 0) return PKV_ERR_SHAPE;
@@ -859,8 +953,10 @@ extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_
     if (num_blocks < 1 || num_blocks > INT32_MAX) return PKV_ERR_SHAPE;
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PKV_ERR_SHAPE;
 
-    const WsLayout lay =
-        ws_layout(num_seqs, num_tokens, max_query_len, max_seq_len, num_q_heads, num_kv_heads, head_size);
+    // the shared-prefix pass runs on the tensor-core tile kernel
+    if (!prefill_supported(num_q_heads, num_kv_heads, head_size)) prefix_blocks = 0;
+    const WsLayout lay = ws_layout(num_seqs, num_tokens, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
+                                   head_size, prefix_blocks);
     if (workspace_needed) *workspace_needed = static_cast<size_t>(lay.total);
     if (num_seqs == 0) return PKV_OK;
     if (!out || !query || !kv_cache || !block_tables || !seq_lens || !query_start_loc) return PKV_ERR_NULL;
@@ -909,6 +1005,8 @@ extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_
     const int G = num_q_heads / num_kv_heads;
     const bool may_prefill = prefill_ok && static_cast<int64_t>(max_query_len) * G > kDecodeTileMaxRows;
     pp.prefill_ok = prefill_ok ? 1 : 0;
+    pp.prefix_blocks = prefix_blocks;
+    pp.block_tables = block_tables;
     pp.lay = lay;
     if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess) return PKV_ERR_CUDA;
 
@@ -930,7 +1028,7 @@ extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_
              ? launch_decode<64, DecodeTiling<64>::NW, DecodeTiling<64>::DEPTH>(map, ap, static_cast<int>(grid), dev, st)
              : launch_decode<128, DecodeTiling<128>::NW, DecodeTiling<128>::DEPTH>(map, ap, static_cast<int>(grid), dev,
                                                                                    st);
-    if (rc || !may_prefill) return rc;
+    if (rc || (!may_prefill && prefix_blocks == 0)) return rc;
     PrefillParams fp;
     fp.out = ap.out;
     fp.block_tables = block_tables;
@@ -944,8 +1042,45 @@ extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_
     fp.scale_log2 = ap.scale_log2;
     fp.lo_tiles = 0;
     fp.ws = ap.ws;
+    if (prefix_blocks > 0) {
+        rc = launch_prefix(fp, query, query_token_stride, kv_cache, num_blocks, head_size,
+                           (lay.max_crows + kPrefillRows - 1) / kPrefillRows * num_kv_heads * lay.prefix_parts,
+                           dev, st);
+        if (rc) return rc;
+    }
+    if (!may_prefill) return PKV_OK;
     return launch_prefill(fp, query, query_token_stride, num_tokens, kv_cache, num_blocks, head_size,
                           lay.max_ptiles * num_kv_heads, dev, st);
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_paged_attn(void *out, const void *query, int64_t query_token_stride, const void *kv_cache,
+                              int64_t num_blocks, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                              int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_size, int32_t block_size, float scale,
+                              int32_t num_splits, void *workspace, size_t workspace_bytes, size_t *workspace_needed,
+                              void *stream) {
+    return pkv::paged_attn_impl(out, query, query_token_stride, kv_cache, num_blocks, block_tables,
+                                max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_tokens, max_query_len,
+                                max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale, num_splits, 0,
+                                workspace, workspace_bytes, workspace_needed, stream);
+}
+
+extern "C" int pkv_paged_attn_shared_prefix(void *out, const void *query, int64_t query_token_stride,
+                                            const void *kv_cache, int64_t num_blocks, const int32_t *block_tables,
+                                            int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                            const int32_t *query_start_loc, int32_t num_seqs, int32_t num_tokens,
+                                            int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                            float scale, int32_t num_splits, int32_t shared_prefix_blocks,
+                                            void *workspace, size_t workspace_bytes, size_t *workspace_needed,
+                                            void *stream) {
+    return pkv::paged_attn_impl(out, query, query_token_stride, kv_cache, num_blocks, block_tables,
+                                max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_tokens, max_query_len,
+                                max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale, num_splits,
+                                shared_prefix_blocks, workspace, workspace_bytes, workspace_needed, stream);
 }
 
 extern "C" int pkv_paged_attn_combine(void *out, const void *workspace, size_t workspace_bytes, int32_t num_tokens,

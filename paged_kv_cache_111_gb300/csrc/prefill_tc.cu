@@ -69,7 +69,14 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t 
     return false;
 }
 
-template <int HD>
+// CASCADE = false: one 128-row tile of one long request (a prefill chunk),
+// causal, written to `out`.  CASCADE = true: 128 rows taken from every
+// request that shares the first prefix_blocks blocks of its table with
+// request 0, against one range of those blocks' KV tiles (every key of the
+// prefix is visible to every such row); the result for range i is split i of
+// each row (normalised partial output and its log-sum-exp), merged with the
+// row's other splits by the combine.
+template <int HD, bool CASCADE>
 __global__ void __launch_bounds__(256, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16 *__restrict__ query,
                    const int64_t q_stride, const PrefillParams p) {
@@ -87,20 +94,39 @@ __global__ void __launch_bounds__(256, 1)
     pdl_trigger();
     const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
-    const int n_items = hdr->n_ptiles * p.num_kv_heads;
+    const int n_parts = CASCADE ? hdr->prefix_parts : 1;
+    const int n_tiles = CASCADE ? (hdr->n_crows + kPrefillRows - 1) / kPrefillRows : hdr->n_ptiles;
+    const int n_items = n_tiles * p.num_kv_heads * n_parts;
     const int item = blockIdx.x;
     if (item >= n_items) return;                       // uniform over the CTA
-    const int4 tile = reinterpret_cast<const int4 *>(p.ws + hdr->off_ptiles)[item / p.num_kv_heads];
     const int g = item % p.num_kv_heads;
-    const int r = tile.x, qt = tile.y, n_kv = tile.z;
-    const int L = p.seq_lens[r];
-    const int qs = p.qsl[r];
-    const int qlen = p.qsl[r + 1] - qs;
-    const int ctx = L - qlen;
     const int G = p.G;
-    const int rows_total = qlen * G;
-    const int row0 = qt * kPrefillRows;                // first request row of the tile
-    const int n_pages = (L + kBlock - 1) / kBlock;
+    // t0: first KV tile of this CTA's key range (cascade part; 0 otherwise)
+    int r, n_kv, L, qs, ctx, rows_total, row0, n_pages, part = 0, t0 = 0;
+    if constexpr (CASCADE) {
+        r = 0;                                         // the prefix blocks are read through request 0's table
+        L = hdr->prefix_blocks * kBlock;               // every row sees keys 0 .. L-1
+        const int kv_all = (L + kPrefillKeys - 1) / kPrefillKeys;
+        const int per = (kv_all + n_parts - 1) / n_parts;   // the plan makes every range non-empty
+        part = (item / p.num_kv_heads) % n_parts;
+        t0 = part * per;
+        n_kv = min(kv_all, t0 + per) - t0;
+        n_pages = hdr->prefix_blocks;
+        qs = ctx = 0;
+        rows_total = hdr->n_crows;
+        row0 = (item / (p.num_kv_heads * n_parts)) * kPrefillRows;
+    } else {
+        const int4 tile = reinterpret_cast<const int4 *>(p.ws + hdr->off_ptiles)[item / p.num_kv_heads];
+        r = tile.x;
+        n_kv = tile.z;
+        L = p.seq_lens[r];
+        qs = p.qsl[r];
+        const int qlen = p.qsl[r + 1] - qs;
+        ctx = L - qlen;
+        rows_total = qlen * G;
+        row0 = tile.y * kPrefillRows;                  // first request row of the tile
+        n_pages = (L + kBlock - 1) / kBlock;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -118,7 +144,7 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t tmem = *tmem_slot;
 
     // the KV tile holding the sequence's last key, when that page is partial
-    const int end_tile = (L % kBlock) ? (L - 1) / kPrefillKeys : -1;
+    const int end_tile = (!CASCADE && (L % kBlock)) ? (L - 1) / kPrefillKeys : -1;
 
     if (warp == 0) {
         // ---------------- producer: K and V pages through the block table ----------------
@@ -129,7 +155,7 @@ __global__ void __launch_bounds__(256, 1)
         // and load as zeros (outside the tensor map).
         constexpr int kPagesPerTile = kPrefillKeys / kBlock;
         auto load_window = [&](int w) -> int {
-            const int page = w * 32 + lane;
+            const int page = t0 * kPagesPerTile + w * 32 + lane;
             const int b = page < n_pages ? __ldg(bt + page) : -1;
             if (page < n_pages && (b < 0 || b >= p.num_blocks))
                 set_status(status, PKV_ERR_DEVICE_INDEX);   // loaded as zeros by the bounded TMA, reported
@@ -252,9 +278,23 @@ __global__ void __launch_bounds__(256, 1)
         // ---------------- softmax + epilogue: thread = row ----------------
         const int row = threadIdx.x - 128;
         const int lane_base = (warp - 4) * 32;
-        const int rrow = row0 + row;                       // request row
+        const int rrow = row0 + row;                       // request row (cascade: row of the prefix pass)
         const bool valid = rrow < rows_total;
-        const int lim = valid ? ctx + rrow / G + 1 : 0;    // keys [0, lim) visible
+        // the row's query token and q head within the group; keys [0, lim) visible
+        int tok = 0, hh = 0, lim = 0;
+        int4 crow = make_int4(0, 0, 0, 0);
+        if (valid) {
+            if constexpr (CASCADE) {
+                crow = reinterpret_cast<const int4 *>(p.ws + hdr->off_crows)[rrow];   // {token, request, index, head}
+                tok = crow.x;
+                hh = crow.w;
+                lim = L;
+            } else {
+                tok = qs + rrow / G;
+                hh = rrow % G;
+                lim = ctx + rrow / G + 1;
+            }
+        }
         const float NEG_INF = -__int_as_float(0x7f800000);
         const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
         bool ok = true;
@@ -263,8 +303,7 @@ __global__ void __launch_bounds__(256, 1)
         {
             uint32_t qv[HD / 2];
             const __nv_bfloat16 *qp =
-                query + static_cast<int64_t>(qs + (valid ? rrow / G : 0)) * q_stride +
-                static_cast<int64_t>(g * G + (valid ? rrow % G : 0)) * HD;
+                query + static_cast<int64_t>(tok) * q_stride + static_cast<int64_t>(g * G + hh) * HD;
 #pragma unroll
             for (int c = 0; c < HD / 8; ++c) {
                 const uint4 w = valid ? __ldg(reinterpret_cast<const uint4 *>(qp) + c) : make_uint4(0, 0, 0, 0);
@@ -304,7 +343,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             // keys a row may not see become -inf; only tiles reaching some
             // row's limit need the test (warp-uniform branch)
-            const int key0 = j * kPrefillKeys;
+            const int key0 = (t0 + j) * kPrefillKeys;
             if (__any_sync(0xffffffffu, key0 + kPrefillKeys > lim)) {
 #pragma unroll
                 for (int c = 0; c < kPrefillKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
@@ -405,13 +444,29 @@ __global__ void __launch_bounds__(256, 1)
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int i = rrow / G, hh = rrow % G;
-            __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(qs + i) * p.num_q_heads + g * G + hh) * HD;
             uint32_t v[HD / 32][32];
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) tmem_ld32(trow + Cfg::kColO + c * 32, v[c]);
             tmem_ld_wait();
-            if (valid) {
+            if constexpr (CASCADE) {
+                if (valid) {
+                    // split `part` of the row: normalised partial output and natural log-sum-exp
+                    const int4 ri = reinterpret_cast<const int4 *>(p.ws + hdr->off_req)[crow.y];
+                    const int64_t prow =
+                        ri.y + (static_cast<int64_t>(crow.z) * p.num_q_heads + g * G + hh) * ri.x + part;
+                    float *po = reinterpret_cast<float *>(p.ws + hdr->off_part_o) + prow * HD;
+#pragma unroll
+                    for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4 *>(po + c * 32 + e) =
+                                make_float4(__uint_as_float(v[c][e]) * inv, __uint_as_float(v[c][e + 1]) * inv,
+                                            __uint_as_float(v[c][e + 2]) * inv, __uint_as_float(v[c][e + 3]) * inv);
+                    reinterpret_cast<float *>(p.ws + hdr->off_part_lse)[prow] =
+                        l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+                }
+            } else if (valid) {
+                __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(tok) * p.num_q_heads + g * G + hh) * HD;
 #pragma unroll
                 for (int c = 0; c < HD / 32; ++c)
 #pragma unroll
@@ -456,7 +511,7 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int HD>
+template <int HD, bool CASCADE>
 static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, const void *query, int64_t q_stride,
                              int64_t grid, int dev, cudaStream_t stream) {
     using Cfg = PrefillCfg<HD>;
@@ -466,16 +521,29 @@ static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, con
         std::lock_guard<std::mutex> lock(mu);
         const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
         if (!bit || !(done_mask & bit)) {
-            if (cudaFuncSetAttribute(prefill_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem) !=
-                cudaSuccess)
+            if (cudaFuncSetAttribute(prefill_kernel<HD, CASCADE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::kSmem) != cudaSuccess)
                 return PKV_ERR_CUDA;
             done_mask |= bit;
         }
     }
-    if (launch_pdl(prefill_kernel<HD>, dim3(static_cast<unsigned>(grid)), dim3(256), Cfg::kSmem, stream, kvm,
-                   static_cast<const __nv_bfloat16 *>(query), q_stride, p) != cudaSuccess)
+    if (launch_pdl(prefill_kernel<HD, CASCADE>, dim3(static_cast<unsigned>(grid)), dim3(256), Cfg::kSmem, stream,
+                   kvm, static_cast<const __nv_bfloat16 *>(query), q_stride, p) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
+}
+
+static int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                         int32_t head_size);
+
+int launch_prefix(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
+                  int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream) {
+    if (grid <= 0) return PKV_OK;
+    CUtensorMap kvm;
+    const int rc = make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
+    if (rc) return rc;
+    if (head_size == 64) return launch_prefill_hd<64, true>(p, kvm, query, q_stride, grid, dev, stream);
+    return launch_prefill_hd<128, true>(p, kvm, query, q_stride, grid, dev, stream);
 }
 
 int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
@@ -483,24 +551,30 @@ int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, 
                    cudaStream_t stream) {
     (void)num_tokens;
     if (grid <= 0) return PKV_OK;
+    CUtensorMap kvm;
+    const int rc = make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
+    if (rc) return rc;
+    if (head_size == 64) return launch_prefill_hd<64, false>(p, kvm, query, q_stride, grid, dev, stream);
+    return launch_prefill_hd<128, false>(p, kvm, query, q_stride, grid, dev, stream);
+}
+
+// Tensor map of the cache as {head_size, 16, 2, kv heads, blocks}; a box is
+// the K (or V) rows of one page, 64 columns, 128-byte swizzle.
+static int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                         int32_t head_size) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PKV_ERR_CUDA;
-    CUtensorMap kvm;
-    {
-        // cache as {head_size, 16, 2, kv heads, blocks}; box = K or V rows of one page, 64 columns
-        const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2,
-                                    static_cast<cuuint64_t>(p.num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
-        const cuuint64_t row = static_cast<cuuint64_t>(head_size) * 2;
-        const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * p.num_kv_heads};
-        const cuuint32_t box[5] = {64, kBlock, 1, 1, 1};
-        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-        if (enc(&kvm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return PKV_ERR_CUDA;
-    }
-    if (head_size == 64) return launch_prefill_hd<64>(p, kvm, query, q_stride, grid, dev, stream);
-    return launch_prefill_hd<128>(p, kvm, query, q_stride, grid, dev, stream);
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2, static_cast<cuuint64_t>(num_kv_heads),
+                                static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t row = static_cast<cuuint64_t>(head_size) * 2;
+    const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * num_kv_heads};
+    const cuuint32_t box[5] = {64, kBlock, 1, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (enc(kvm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
 }
 
 }  // namespace pkv
