@@ -70,6 +70,15 @@ def _load():
             lib.oracle_lse_combine.restype = ctypes.c_int
             lib.oracle_copy_blocks.argtypes = [P, i64, i32, i32, i32, P, i32]
             lib.oracle_copy_blocks.restype = ctypes.c_int
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_decode.restype = ctypes.c_double
+            lib.oracle_e4m3_encode.argtypes = [f32]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_kv_write_fp8.argtypes = [P, i64, i32, i32, i32, P, P, P, i32, f32, f32]
+            lib.oracle_kv_write_fp8.restype = ctypes.c_int
+            lib.oracle_paged_attn_fp8.argtypes = [P, P, P, P, i64, P, i32, P, P, i32,
+                                                  i32, i32, i32, i32, f32, f32, f32, i32]
+            lib.oracle_paged_attn_fp8.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -90,7 +99,9 @@ class use_library:
         self.saved = _load()
         lib = ctypes.CDLL(self.path)
         for name in ("oracle_max_threads", "oracle_kv_write", "oracle_paged_attn",
-                     "oracle_attn_row", "oracle_lse_combine", "oracle_copy_blocks"):
+                     "oracle_attn_row", "oracle_lse_combine", "oracle_copy_blocks",
+                     "oracle_e4m3_decode", "oracle_e4m3_encode", "oracle_kv_write_fp8",
+                     "oracle_paged_attn_fp8"):
             src, dst = getattr(self.saved, name), getattr(lib, name)
             dst.restype = src.restype
             if src.argtypes is not None:
@@ -227,4 +238,71 @@ def run_step(step, num_threads: int = 0):
     kv_write(cache, step.key, step.value, step.slot_mapping)
     out, lse = paged_attn(cache, step.query, step.block_tables, step.seq_lens,
                           step.query_start_loc, step.num_q_heads, step.scale, num_threads)
+    return cache, out, lse
+
+
+# ---- FP8 (E4M3) cache ---------------------------------------------------------
+
+E4M3_NAN = 0x7F
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one E4M3 code (NaN for 0x7F / 0xFF)."""
+    return float(_load().oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code of the fp32 value x (ties to even, held at +-448)."""
+    return int(_load().oracle_e4m3_encode(ctypes.c_float(x)))
+
+
+def new_cache_fp8(num_blocks: int, num_kv_heads: int, head_size: int, block_size: int = 16) -> np.ndarray:
+    """An E4M3 cache of raw bytes, all NaN (0x7F)."""
+    return np.full((num_blocks, num_kv_heads, 2, block_size, head_size), E4M3_NAN, dtype=np.uint8)
+
+
+def kv_write_fp8(cache: np.ndarray, key, value, slot_mapping, k_scale: float, v_scale: float) -> None:
+    """In-place write of bf16 key/value [T, Hkv, d] into an E4M3 cache: code = E4M3(x / scale)."""
+    nb, hkv, two, bs, d = cache.shape
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and two == 2
+    k = _np(key, np.uint16)
+    v = _np(value, np.uint16)
+    s = _np(slot_mapping, np.int64)
+    T = int(s.shape[0])
+    assert k.shape == (T, hkv, d) and v.shape == (T, hkv, d)
+    _check(_load().oracle_kv_write_fp8(_ptr(cache), nb, hkv, d, bs, _ptr(k), _ptr(v), _ptr(s), T,
+                                       ctypes.c_float(k_scale), ctypes.c_float(v_scale)),
+           "oracle_kv_write_fp8")
+
+
+def paged_attn_fp8(cache: np.ndarray, query, block_tables, seq_lens, query_start_loc,
+                   num_q_heads: int, scale: float, k_scale: float, v_scale: float, num_threads: int = 0):
+    """Attention over an E4M3 cache (values code * scale); returns (out fp64, lse fp64)."""
+    nb, hkv, _, bs, d = cache.shape
+    assert cache.dtype == np.uint8
+    q = _np(query, np.uint16)
+    bt = _np(block_tables, np.int32)
+    sl = _np(seq_lens, np.int32)
+    qsl = _np(query_start_loc, np.int32)
+    S = int(sl.shape[0])
+    T = int(qsl[-1]) if S else 0
+    out = np.zeros((T, num_q_heads, d), dtype=np.float64)
+    lse = np.zeros((T, num_q_heads), dtype=np.float64)
+    maxb = int(bt.shape[1]) if bt.ndim == 2 else 0
+    _check(_load().oracle_paged_attn_fp8(_ptr(out), _ptr(lse), _ptr(q), _ptr(cache), nb, _ptr(bt), maxb,
+                                         _ptr(sl), _ptr(qsl), S, num_q_heads, hkv, d, bs,
+                                         ctypes.c_float(scale), ctypes.c_float(k_scale),
+                                         ctypes.c_float(v_scale), int(num_threads)),
+           "oracle_paged_attn_fp8")
+    return out, lse
+
+
+def run_step_fp8(step, k_scale: float, v_scale: float, num_threads: int = 0):
+    """run_step over an E4M3 cache: (cache uint8, out fp64 [T, H, d], lse fp64 [T, H])."""
+    cache = new_cache_fp8(step.num_blocks, step.num_kv_heads, step.head_size, step.block_size)
+    kv_write_fp8(cache, step.hist_key, step.hist_value, step.hist_slot_mapping, k_scale, v_scale)
+    kv_write_fp8(cache, step.key, step.value, step.slot_mapping, k_scale, v_scale)
+    out, lse = paged_attn_fp8(cache, step.query, step.block_tables, step.seq_lens,
+                              step.query_start_loc, step.num_q_heads, step.scale, k_scale, v_scale,
+                              num_threads)
     return cache, out, lse

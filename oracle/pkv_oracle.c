@@ -31,6 +31,19 @@
  * of the sequence, written before attention reads them).  Query head h reads
  * kv head h / (num_q_heads / num_kv_heads).
  *
+ * FP8 cache option ("vLLM internals: managing the KV cache like an OS manages
+ * memory", section 7.2, the KV cache itself can be stored in FP8; the
+ * "continuous batching and PagedAttention" tutorial, sections 8.8, 10.3 and
+ * the FAQ of 10.8: an FP8 KV cache halves its memory at almost no loss).  The
+ * pages fix neither the 8-bit format nor the scaling; the reading taken is
+ * the OCP E4M3 format (sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent 0 is subnormal; all-ones exponent and mantissa is NaN; no
+ * infinities; largest finite 448) with one fp32 scale for all K and one for
+ * all V: the stored code is E4M3(x / scale), the quotient an fp32 division
+ * rounded to nearest and the code the nearest E4M3 value (ties to the even
+ * code, magnitudes past 448 held at 448), and the cache then holds
+ * code_value * scale.  The same layout holds one byte per element.
+ *
  * Every function returns 0 on success and a negative code on invalid input.
  */
 
@@ -64,6 +77,58 @@ static size_t cache_offset(int64_t block, int32_t kv_head, int32_t which, int32_
     idx = idx * 2u + (size_t)which;
     idx = idx * (size_t)block_size + (size_t)off;
     return idx * (size_t)head_size;
+}
+
+/* ---- E4M3 ------------------------------------------------------------------ */
+
+/* The value of an E4M3 code, from the format's definition. */
+double oracle_e4m3_decode(uint8_t code)
+{
+    const int sign = code >> 7;
+    const int e = (code >> 3) & 15;
+    const int m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);               /* m/8 * 2^(1-7) */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/*
+ * The E4M3 code nearest to x (ties to the even code), magnitudes at or past
+ * 448 held at 448, NaN to 0x7F.  The sign is kept, also for results that
+ * round to zero.
+ */
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int code;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: multiples of 2^-9; code = that multiple (0..8) */
+        code = (int)nearbyint(ldexp(a, 9));     /* exact scaling; rounds half to even */
+    } else {
+        int ex;
+        const double fr = frexp(a, &ex);        /* a = fr * 2^ex, fr in [0.5, 1) */
+        const int e = ex - 1;                   /* a = (2 fr) * 2^e, 2 fr in [1, 2) */
+        const int m = (int)nearbyint((2.0 * fr - 1.0) * 8.0);
+        code = ((e + 7) << 3) + m;              /* m = 8 carries into the exponent */
+    }
+    return sign | (uint8_t)code;
+}
+
+/* fp32 quotient x / scale, rounded to nearest (the value that is encoded). */
+static float quotient_f32(float x, float scale)
+{
+    volatile float q = x / scale;               /* a single IEEE fp32 division */
+    return q;
 }
 
 int oracle_max_threads(void)
@@ -137,6 +202,67 @@ int oracle_kv_write(uint16_t *cache, int64_t num_blocks, int32_t num_kv_heads,
 }
 
 /*
+ * Cache write into an FP8 cache: the same slots as oracle_kv_write, each
+ * element stored as oracle_e4m3_encode(bf16 value / scale), k_scale for K
+ * and v_scale for V.  cache: uint8 [num_blocks][num_kv_heads][2][block_size][head_size].
+ */
+int oracle_kv_write_fp8(uint8_t *cache, int64_t num_blocks, int32_t num_kv_heads,
+                        int32_t head_size, int32_t block_size,
+                        const uint16_t *key, const uint16_t *value,
+                        const int64_t *slot_mapping, int32_t num_tokens,
+                        float k_scale, float v_scale)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks < 0)
+        return ORACLE_EINVAL;
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || isinf(k_scale) || isinf(v_scale))
+        return ORACLE_EINVAL;
+    if (num_tokens == 0)
+        return 0;
+    if (!cache || !key || !value || !slot_mapping)
+        return ORACLE_EINVAL;
+    const int64_t num_slots = num_blocks * (int64_t)block_size;
+    int64_t *sorted = (int64_t *)malloc(sizeof(int64_t) * (size_t)num_tokens);
+    if (!sorted)
+        return ORACLE_ENOMEM;
+    int32_t n = 0;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s >= num_slots) {
+            free(sorted);
+            return ORACLE_ERANGE;
+        }
+        if (s >= 0)
+            sorted[n++] = s;
+    }
+    qsort(sorted, (size_t)n, sizeof(int64_t), cmp_i64);
+    for (int32_t i = 1; i < n; ++i) {
+        if (sorted[i] == sorted[i - 1]) {
+            free(sorted);
+            return ORACLE_EDUP;
+        }
+    }
+    free(sorted);
+
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        const int64_t block = slot / block_size;
+        const int32_t off = (int32_t)(slot % block_size);
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            const size_t src = ((size_t)t * (size_t)num_kv_heads + (size_t)h) * (size_t)head_size;
+            uint8_t *kd = cache + cache_offset(block, h, 0, off, num_kv_heads, block_size, head_size);
+            uint8_t *vd = cache + cache_offset(block, h, 1, off, num_kv_heads, block_size, head_size);
+            for (int32_t e = 0; e < head_size; ++e) {
+                kd[e] = oracle_e4m3_encode(quotient_f32((float)bf16_bits_to_double(key[src + e]), k_scale));
+                vd[e] = oracle_e4m3_encode(quotient_f32((float)bf16_bits_to_double(value[src + e]), v_scale));
+            }
+        }
+    }
+    return 0;
+}
+
+/*
  * Copy-on-write block copies ("continuous batching and PagedAttention"
  * tutorial, section 3.8): for every pair, the destination block receives a
  * bit copy of the source block (every kv head, K and V).  mapping: int64
@@ -168,7 +294,7 @@ int oracle_copy_blocks(uint16_t *cache, int64_t num_blocks, int32_t num_kv_heads
 
 typedef struct {
     const uint16_t *query;
-    const uint16_t *cache;
+    const void *cache;          /* bf16 elements, or E4M3 bytes when fp8 */
     int64_t num_blocks;
     const int32_t *block_tables;
     int32_t max_blocks_per_seq;
@@ -177,7 +303,20 @@ typedef struct {
     int32_t num_seqs;
     int32_t num_q_heads, num_kv_heads, head_size, block_size;
     double scale;
+    int fp8;                    /* 0: bf16 cache; 1: E4M3 cache */
+    double k_scale, v_scale;    /* fp8 only: the value is code_value * scale */
 } problem_t;
+
+/* Element e of the K (which = 0) or V (which = 1) row at (block, kv head, offset). */
+static double cache_elem(const problem_t *p, int64_t block, int32_t kv_head, int32_t which, int32_t off,
+                         int32_t e)
+{
+    const size_t i = cache_offset(block, kv_head, which, off, p->num_kv_heads, p->block_size, p->head_size) +
+                     (size_t)e;
+    if (p->fp8)
+        return oracle_e4m3_decode(((const uint8_t *)p->cache)[i]) * (which ? p->v_scale : p->k_scale);
+    return bf16_bits_to_double(((const uint16_t *)p->cache)[i]);
+}
 
 static int check_problem(const problem_t *p)
 {
@@ -248,11 +387,9 @@ static void attend_row(const problem_t *p, int32_t r, int32_t i, int32_t h,
     double m = -INFINITY;
     for (int64_t j = j0; j < j1; ++j) {
         const int32_t phys = table[j / B];
-        const uint16_t *k = p->cache + cache_offset(phys, g, 0, (int32_t)(j % B),
-                                                    p->num_kv_heads, B, d);
         double dot = 0.0;
         for (int32_t e = 0; e < d; ++e)
-            dot += bf16_bits_to_double(q[e]) * bf16_bits_to_double(k[e]);
+            dot += bf16_bits_to_double(q[e]) * cache_elem(p, phys, g, 0, (int32_t)(j % B), e);
         const double s = p->scale * dot;
         scores[j - j0] = s;
         if (s > m)
@@ -265,10 +402,8 @@ static void attend_row(const problem_t *p, int32_t r, int32_t i, int32_t h,
         scores[j - j0] = w;
         z += w;
         const int32_t phys = table[j / B];
-        const uint16_t *v = p->cache + cache_offset(phys, g, 1, (int32_t)(j % B),
-                                                    p->num_kv_heads, B, d);
         for (int32_t e = 0; e < d; ++e)
-            out[e] += w * bf16_bits_to_double(v[e]);
+            out[e] += w * cache_elem(p, phys, g, 1, (int32_t)(j % B), e);
     }
     for (int32_t e = 0; e < d; ++e)
         out[e] /= z;
@@ -292,6 +427,8 @@ static int64_t longest_seq(const problem_t *p)
  * lse: double [num_tokens][num_q_heads] (may be NULL).  Rows are
  * independent; num_threads <= 0 uses every available thread.
  */
+static int paged_attn_all(const problem_t *pp, double *out, double *lse, int32_t num_threads);
+
 int oracle_paged_attn(double *out, double *lse, const uint16_t *query,
                       const uint16_t *cache, int64_t num_blocks,
                       const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -301,7 +438,33 @@ int oracle_paged_attn(double *out, double *lse, const uint16_t *query,
 {
     problem_t p = {query, cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                    query_start_loc, num_seqs, num_q_heads, num_kv_heads, head_size,
-                   block_size, (double)scale};
+                   block_size, (double)scale, 0, 1.0, 1.0};
+    return paged_attn_all(&p, out, lse, num_threads);
+}
+
+/* The same attention over an E4M3 cache: K and V values are code_value * scale. */
+int oracle_paged_attn_fp8(double *out, double *lse, const uint16_t *query,
+                          const uint8_t *cache, int64_t num_blocks,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                          int32_t block_size, float scale, float k_scale, float v_scale,
+                          int32_t num_threads)
+{
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || isinf(k_scale) || isinf(v_scale))
+        return ORACLE_EINVAL;
+    problem_t p = {query, cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
+                   query_start_loc, num_seqs, num_q_heads, num_kv_heads, head_size,
+                   block_size, (double)scale, 1, (double)k_scale, (double)v_scale};
+    return paged_attn_all(&p, out, lse, num_threads);
+}
+
+static int paged_attn_all(const problem_t *pp, double *out, double *lse, int32_t num_threads)
+{
+    const problem_t p = *pp;
+    const int32_t num_seqs = p.num_seqs, num_q_heads = p.num_q_heads, head_size = p.head_size;
+    const int32_t *query_start_loc = p.query_start_loc, *seq_lens = p.seq_lens;
+    const uint16_t *query = p.query;
     int rc = check_problem(&p);
     if (rc)
         return rc;
@@ -372,7 +535,7 @@ int oracle_attn_row(double *out, double *lse, double *weights, const uint16_t *q
 {
     problem_t p = {query, cache, num_blocks, block_tables, max_blocks_per_seq, seq_lens,
                    query_start_loc, num_seqs, num_q_heads, num_kv_heads, head_size,
-                   block_size, (double)scale};
+                   block_size, (double)scale, 0, 1.0, 1.0};
     int rc = check_problem(&p);
     if (rc)
         return rc;

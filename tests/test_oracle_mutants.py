@@ -2,7 +2,8 @@
 
 Every mutant is a one-expression edit of ``oracle/pkv_oracle.c`` compiled
 into a temporary library; the committed oracle is never modified.  For each
-one, at least one of the pin tests in ``test_oracle_pins`` must fail.
+one, at least one of the pin tests in ``test_oracle_pins`` or
+``test_oracle_fp8_pins`` must fail.
 """
 
 import os
@@ -21,22 +22,37 @@ MUTANTS = [
     ("causal limit one too far", "int64_t j1 = key_end < pos + 1 ? key_end : pos + 1;\n    for (int32_t e",
      "int64_t j1 = key_end < pos + 2 ? key_end : pos + 2;\n    for (int32_t e"),
     ("position ignores context", "const int64_t pos = context + i;", "const int64_t pos = i;"),
-    ("keys read from the V half", "const uint16_t *k = p->cache + cache_offset(phys, g, 0,",
-     "const uint16_t *k = p->cache + cache_offset(phys, g, 1,"),
-    ("table indexed by offset", "const int32_t phys = table[j / B];\n        const uint16_t *k",
-     "const int32_t phys = table[j % B];\n        const uint16_t *k"),
-    ("offset taken as block index", "cache_offset(phys, g, 1, (int32_t)(j % B),",
-     "cache_offset(phys, g, 1, (int32_t)((j / B) % B),"),
+    ("keys read from the V half", "* cache_elem(p, phys, g, 0, (int32_t)(j % B), e)",
+     "* cache_elem(p, phys, g, 1, (int32_t)(j % B), e)"),
+    ("table indexed by offset", "const int32_t phys = table[j / B];\n        double dot",
+     "const int32_t phys = table[j % B];\n        double dot"),
+    ("offset taken as block index", "cache_elem(p, phys, g, 1, (int32_t)(j % B), e)",
+     "cache_elem(p, phys, g, 1, (int32_t)((j / B) % B), e)"),
     ("scale dropped", "const double s = p->scale * dot;", "const double s = dot;"),
     ("no normalisation", "        out[e] /= z;\n    *lse = m + log(z);", "        out[e] /= 1.0;\n    *lse = m + log(z);"),
     ("lse without the maximum", "*lse = m + log(z);\n    if (weights)", "*lse = log(z);\n    if (weights)"),
-    ("cache write offset", "const int32_t off = (int32_t)(slot % block_size);",
-     "const int32_t off = (int32_t)((slot + 1) % block_size);"),
+    ("cache write offset", "/* padding token */\n        const int64_t block = slot / block_size;\n"
+     "        const int32_t off = (int32_t)(slot % block_size);",
+     "/* padding token */\n        const int64_t block = slot / block_size;\n"
+     "        const int32_t off = (int32_t)((slot + 1) % block_size);"),
+    ("fp8 cache write offset", "continue;\n        const int64_t block = slot / block_size;\n"
+     "        const int32_t off = (int32_t)(slot % block_size);",
+     "continue;\n        const int64_t block = slot / block_size;\n"
+     "        const int32_t off = (int32_t)((slot + 1) % block_size);"),
     ("cache write K/V swapped", "memcpy(cache + cache_offset(block, h, 0, off, num_kv_heads, block_size, head_size),\n                   key + src",
      "memcpy(cache + cache_offset(block, h, 0, off, num_kv_heads, block_size, head_size),\n                   value + src"),
     ("combine ignores weights", "const double w = exp(part_lse[s] - m);", "const double w = 1.0;"),
     ("block copy covers one kv head", "const size_t block_elems = cache_offset(1, 0, 0, 0, num_kv_heads, block_size, head_size);",
      "const size_t block_elems = cache_offset(0, 1, 0, 0, num_kv_heads, block_size, head_size);"),
+    ("e4m3 exponent bias", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("e4m3 mantissa truncated", "const int m = (int)nearbyint((2.0 * fr - 1.0) * 8.0);",
+     "const int m = (int)floor((2.0 * fr - 1.0) * 8.0);"),
+    ("e4m3 subnormal step", "code = (int)nearbyint(ldexp(a, 9));", "code = (int)nearbyint(ldexp(a, 8));"),
+    ("e4m3 zero loses its sign", "const uint8_t sign = signbit(x) ? 0x80 : 0x00;",
+     "const uint8_t sign = x < 0 ? 0x80 : 0x00;"),
+    ("fp8 write ignores the K scale", "quotient_f32((float)bf16_bits_to_double(key[src + e]), k_scale)",
+     "quotient_f32((float)bf16_bits_to_double(key[src + e]), 1.0f)"),
+    ("fp8 V read with the K scale", "(which ? p->v_scale : p->k_scale)", "(which ? p->k_scale : p->k_scale)"),
     ("layout heads and k/v swapped", "idx = idx * (size_t)num_kv_heads + (size_t)kv_head;\n    idx = idx * 2u + (size_t)which;",
      "idx = idx * 2u + (size_t)which;\n    idx = idx * (size_t)num_kv_heads + (size_t)kv_head;"),
 ]
@@ -44,8 +60,13 @@ MUTANTS = [
 BATTERY = r"""
 import sys
 sys.path.insert(0, {tests!r}); sys.path.insert(0, {root!r})
-import oracle, test_oracle_pins as pins
-tests = [lambda: [pins.test_oracle_matches_torch_sdpa_on_contiguous_kv(c) for c in range(len(pins.CASES))],
+import oracle, test_oracle_pins as pins, test_oracle_fp8_pins as f8
+tests = [f8.test_decode_matches_torch_on_all_codes,
+         f8.test_encode_matches_torch_rounding_inside_its_range,
+         f8.test_saturation_and_signed_zero,
+         lambda: f8.test_fp8_write_matches_torch_quotient_rounding(0.0173, 3.7),
+         lambda: f8.test_fp8_attention_matches_torch_sdpa_on_contiguous_dequantised_kv(0.0173, 3.7),
+lambda: [pins.test_oracle_matches_torch_sdpa_on_contiguous_kv(c) for c in range(len(pins.CASES))],
          pins.test_oracle_matches_sdpa_with_shared_prefix_and_forks,
          pins.test_index_example_from_the_pages,
          pins.test_single_key_returns_its_value_exactly,
