@@ -30,6 +30,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import workloads as wl  # noqa: E402
@@ -60,17 +61,18 @@ def decode_sources_hash() -> str:
 # algorithmic bytes
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(step: wl.Step) -> dict:
+def algorithmic_bytes(step: wl.Step, kv_elem_bytes: int = 2) -> dict:
     """Bytes the method must move per step (each byte once), by phase.
 
     attention: K and V of every key each request sees (a physical block
     shared by several requests counts once), Q in, out, the table entries
-    read and the per-request lengths.  kv_write: new K/V read and written,
-    and slot numbers.
+    read and the per-request lengths.  kv_write: new K/V read (bf16) and
+    written (kv_elem_bytes per element: 2 for bf16, 1 for E4M3), and slot
+    numbers.
     """
     H, Hkv, d, B = step.num_q_heads, step.num_kv_heads, step.head_size, step.block_size
     T, S = step.num_tokens, step.num_seqs
-    per_token_kv = 2 * Hkv * d * 2
+    per_token_kv = 2 * Hkv * d * kv_elem_bytes
     # unique (block, used tokens): a shared block is read once
     used = {}
     for r in range(S):
@@ -83,7 +85,7 @@ def algorithmic_bytes(step: wl.Step) -> dict:
     kv_logical = int(step.seq_lens.long().sum()) * per_token_kv
     tables = sum((int(l) + B - 1) // B for l in step.seq_lens.tolist()) * 4
     attn = kv_unique + 2 * T * H * d * 2 + tables + 4 * S + 4 * (S + 1)
-    kvw = 2 * (T * per_token_kv) + 8 * T
+    kvw = T * 2 * Hkv * d * 2 + T * per_token_kv + 8 * T
     # flops: every query row of every head sees keys 0 .. its position; one
     # multiply-add each in Q K^T and in P V (4 flops per key per dimension)
     ql = step.query_lens.to(torch.float64)
@@ -109,12 +111,13 @@ def shared_prefix_blocks(step: wl.Step) -> int:
     return min(k, ctx_min // step.block_size)
 
 
-def launches_per_step(step: wl.Step, prefix_blocks: int) -> int:
+def launches_per_step(step: wl.Step, prefix_blocks: int, fp8: bool = False) -> int:
     """Kernels of one layer-step: kv_write, plan, decode, combine; the prefill
     kernel when some request has more than 64 rows (q_r * G) and the head
-    layout has a tensor-core tile; the shared-prefix kernel when asked for."""
+    layout has a tensor-core tile; the shared-prefix kernel when asked for.
+    An E4M3 cache runs every row on the decode kernel."""
     G = step.num_q_heads // step.num_kv_heads
-    tile_ok = step.head_size in (64, 128) and 128 % G == 0
+    tile_ok = step.head_size in (64, 128) and 128 % G == 0 and not fp8
     n = 4
     if tile_ok and step.max_query_len * G > 64:
         n += 1
@@ -228,14 +231,28 @@ def run_gpu(args, rank: int, world: int) -> dict:
     T, H, d = step.num_tokens, step.num_q_heads, step.head_size
     to = {f: getattr(step, f).to(dev).contiguous() for f in
           ("seq_lens", "query_start_loc", "block_tables", "query", "key", "value", "slot_mapping")}
-    pool = wl.make_poisoned_pool_like(step, device=dev)
+    fp8 = args.kv_dtype == "fp8"
+    scales = fp8_scales(step) if fp8 else None
+    if fp8:
+        pool = torch.full(step.pool_shape(), 0x7F, dtype=torch.uint8, device=dev)   # E4M3 NaN
+    else:
+        pool = wl.make_poisoned_pool_like(step, device=dev)
+
+    def write(key, value, slots):
+        if fp8:
+            pkv.kv_write_fp8(pool, key, value, slots, scales[0], scales[1])
+        else:
+            pkv.kv_write(pool, key, value, slots)
+
     hk, hv, hs = step.hist_key, step.hist_value, step.hist_slot_mapping
     chunk = 1 << 16
     for a in range(0, hs.numel(), chunk):
         b = min(hs.numel(), a + chunk)
-        pkv.kv_write(pool, hk[a:b].to(dev), hv[a:b].to(dev), hs[a:b].to(dev))
+        write(hk[a:b].to(dev), hv[a:b].to(dev), hs[a:b].to(dev))
     del hk, hv
     K = shared_prefix_blocks(step) if args.shared_prefix_blocks < 0 else args.shared_prefix_blocks
+    if fp8:
+        K = 0                        # the shared-prefix pass reads bf16 pages only
     if K:
         ws_bytes = pkv.paged_attn_shared_prefix_workspace_size(step.num_seqs, T, step.max_query_len,
                                                                step.max_seq_len, H, step.num_kv_heads, d, K)
@@ -248,7 +265,9 @@ def run_gpu(args, rank: int, world: int) -> dict:
     maxq, maxs = step.max_query_len, step.max_seq_len
 
     def attention(q, tables, lens, qsl):
-        if K:
+        if fp8:
+            pkv.paged_attn_fp8(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, scales[0], scales[1], ws)
+        elif K:
             pkv.paged_attn_shared_prefix(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, K, ws)
         else:
             pkv.paged_attn(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, ws)
@@ -256,7 +275,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
     def one_step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        pkv.kv_write(pool, to["key"], to["value"], to["slot_mapping"])
+        write(to["key"], to["value"], to["slot_mapping"])
         if ev is not None:
             ev[1].record(stream)
         attention(to["query"], to["block_tables"], to["seq_lens"], to["query_start_loc"])
@@ -326,7 +345,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
     def e2e_step():
         for f, t in host_in.items():
             dev_in[f].copy_(t, non_blocking=True)
-        pkv.kv_write(pool, dev_in["key"], dev_in["value"], dev_in["slot_mapping"])
+        write(dev_in["key"], dev_in["value"], dev_in["slot_mapping"])
         attention(dev_in["query"], dev_in["block_tables"], dev_in["seq_lens"], dev_in["query_start_loc"])
         pkv.paged_attn_combine(out, ws)
         host_out.copy_(out, non_blocking=True)
@@ -365,7 +384,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
         probe_gbs = 2 * n * 2 / (best * 1e-3) / 1e9
         del a, b
 
-    return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K),
+    return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K, fp8),
+            "fp8_scales": scales,
             "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
             "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "probe_gbs": probe_gbs}
 
@@ -380,21 +400,42 @@ def oracle_sample(step: wl.Step, n_req: int, seed: int) -> wl.Step:
     return step.subset(sorted(idx.tolist()))
 
 
-def time_oracle_step(sub: wl.Step):
-    """One oracle step on ``sub``: cache write of the new tokens + attention.
+def time_oracle_step(sub: wl.Step, fp8_scales=None):
+    """One oracle step on ``sub``: cache write of the new tokens + attention
+    (over an E4M3 cache when fp8_scales = (k_scale, v_scale) is given).
     Returns (seconds, algorithmic bytes of the sample, threads)."""
     import oracle
-    cache = oracle.new_cache(sub.num_blocks, sub.num_kv_heads, sub.head_size)
-    oracle.kv_write(cache, sub.hist_key, sub.hist_value, sub.hist_slot_mapping)
+    if fp8_scales is None:
+        cache = oracle.new_cache(sub.num_blocks, sub.num_kv_heads, sub.head_size)
+        oracle.kv_write(cache, sub.hist_key, sub.hist_value, sub.hist_slot_mapping)
+        t0 = time.perf_counter()
+        oracle.kv_write(cache, sub.key, sub.value, sub.slot_mapping)
+        oracle.paged_attn(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
+                          sub.num_q_heads, sub.scale)
+        dt = time.perf_counter() - t0
+        return dt, algorithmic_bytes(sub)["step"], oracle.max_threads()
+    ks, vs = fp8_scales
+    cache = oracle.new_cache_fp8(sub.num_blocks, sub.num_kv_heads, sub.head_size)
+    oracle.kv_write_fp8(cache, sub.hist_key, sub.hist_value, sub.hist_slot_mapping, ks, vs)
     t0 = time.perf_counter()
-    oracle.kv_write(cache, sub.key, sub.value, sub.slot_mapping)
-    oracle.paged_attn(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
-                      sub.num_q_heads, sub.scale)
+    oracle.kv_write_fp8(cache, sub.key, sub.value, sub.slot_mapping, ks, vs)
+    oracle.paged_attn_fp8(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
+                          sub.num_q_heads, sub.scale, ks, vs)
     dt = time.perf_counter() - t0
-    return dt, algorithmic_bytes(sub)["step"], oracle.max_threads()
+    return dt, algorithmic_bytes(sub, 1)["step"], oracle.max_threads()
 
 
-def cpu_baseline(step: wl.Step, budget_s: float = 10.0) -> dict:
+def fp8_scales(step: wl.Step):
+    """Per-tensor E4M3 scales from the step's own K and V (largest magnitude / 448),
+    as a calibration pass would set them; rounded to fp32."""
+    def amax(*ts):
+        return max(float(t.float().abs().max()) if t.numel() else 0.0 for t in ts)
+    ks = max(amax(step.hist_key, step.key), 1e-30) / 448.0
+    vs = max(amax(step.hist_value, step.value), 1e-30) / 448.0
+    return float(np.float32(ks)), float(np.float32(vs))
+
+
+def cpu_baseline(step: wl.Step, budget_s: float = 10.0, scales=None) -> dict:
     import oracle
     oracle.build()
     n_req = max(1, step.num_seqs // 4)
@@ -402,7 +443,7 @@ def cpu_baseline(step: wl.Step, budget_s: float = 10.0) -> dict:
     times, nbytes, threads = [], 0, 1
     t_end = time.perf_counter() + budget_s
     while len(times) < 3 or time.perf_counter() < t_end:
-        dt, nbytes, threads = time_oracle_step(sub)
+        dt, nbytes, threads = time_oracle_step(sub, scales)
         times.append(dt)
         if len(times) >= 50:
             break
@@ -487,6 +528,8 @@ def main():
     ap.add_argument("--shared-prefix-blocks", type=int, default=-1,
                     help="cascade over this many shared leading table blocks (pkv_paged_attn_shared_prefix); "
                          "-1: the prefix every request's table shares with request 0's, 0: plain paged_attn")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="cache element type: bf16, or E4M3 with per-tensor K/V scales (pkv_*_fp8)")
     ap.add_argument("--subset", type=int, default=0,
                     help="keep only the first N requests, with a compact pool (small profiling case)")
     args = ap.parse_args()
@@ -502,7 +545,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ["LOCAL_RANK"])))
     r = run_gpu(args, rank, world)
     step = r["step"]
-    ab = algorithmic_bytes(step)
+    fp8 = args.kv_dtype == "fp8"
+    ab = algorithmic_bytes(step, 1 if fp8 else 2)
     ms_per_step = r["total_ms"] / args.steps
     ms_per_step, attn_max, e2e_max = max_over_ranks([ms_per_step, r["attn_ms"], r["e2e_ms"]], world,
                                                     device="cuda" if world > 1 else None)
@@ -523,7 +567,7 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic",
         "config": {
             "workload": step.name, "num_seqs": step.num_seqs, "num_tokens": step.num_tokens,
@@ -532,6 +576,8 @@ def main():
             "kv_bytes_per_step": ab["kv_unique"], "parallelism": f"replicas x{world}",
             "launch": "cuda graph replay" if args.graph else "eager",
             "shared_prefix_blocks": r["shared_prefix_blocks"],
+            "kv_cache": (f"e4m3, k_scale {r['fp8_scales'][0]:.6g}, v_scale {r['fp8_scales'][1]:.6g}"
+                         if fp8 else "bf16"),
             "l2": "inputs larger than L2 (KV read per step above 129 MB), no flush"
             if ab["kv_unique"] > 129e6 else "inputs fit in L2; no flush (small workload)",
         },
@@ -548,13 +594,17 @@ def main():
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
     }
+    if fp8:
+        # the profiled traffic ratio is the bf16 decode kernel's
+        line["roofline"]["traffic"] = None
+        line["roofline"]["kernel"] = "paged_attn (plan + E4M3 decode kernel; chunks on its 16-row tiles)"
     if args.graph:
         line["roofline"]["kernel"] = "whole layer-step (kv_write + paged_attn + combine), CUDA-graph replay"
         line["roofline"]["traffic"] = None
     if ab["kv_logical"] != ab["kv_unique"]:
         line["logical_kv_gbs_incl_l2_reuse"] = ab["kv_logical"] / (r["attn_ms"] * 1e-3) / 1e9
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(step)
+        line["cpu_baseline"] = cpu_baseline(step, scales=r["fp8_scales"])
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

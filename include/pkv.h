@@ -183,8 +183,8 @@ int pkv_paged_attn(void *out, const void *query, int64_t query_token_stride,
  * equal request 0's, its query rows fit one decode tile (q_r * G <= 16) and
  * its context covers the prefix (L_r - q_r >= 16 * shared_prefix_blocks;
  * request 0's must too).  Other requests are computed as by pkv_paged_attn.
- * shared_prefix_blocks = 0 is pkv_paged_attn.  The workspace size depends on
- * shared_prefix_blocks being zero or not.
+ * shared_prefix_blocks = 0 is pkv_paged_attn.  The workspace size also
+ * depends on shared_prefix_blocks.
  */
 int pkv_paged_attn_shared_prefix(void *out, const void *query, int64_t query_token_stride,
                                  const void *kv_cache, int64_t num_blocks,
@@ -197,6 +197,56 @@ int pkv_paged_attn_shared_prefix(void *out, const void *query, int64_t query_tok
                                  int32_t shared_prefix_blocks,
                                  void *workspace, size_t workspace_bytes, size_t *workspace_needed,
                                  void *stream);
+
+/*
+ * FP8 KV cache ("vLLM internals: managing the KV cache like an OS manages
+ * memory", section 7.2: the KV cache itself can be kept in FP8; "continuous
+ * batching and PagedAttention" tutorial, sections 8.8 and 10.3 and the FAQ
+ * of 10.8: an FP8 KV cache halves its memory at almost no loss).
+ *
+ * The cache has the bf16 layout with one byte per element:
+ *     uint8 [num_blocks][num_kv_heads][2][16][head_size]
+ * each byte an E4M3 code (OCP FP8: sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent 0 subnormal; 0x7F and 0xFF NaN; largest finite
+ * 448).  One fp32 scale covers all K (k_scale) and one all V (v_scale); a
+ * stored code c stands for value(c) * scale.
+ *
+ * pkv_kv_write_fp8 — pkv_kv_write into an E4M3 cache.  Element x (bf16) of
+ * a new K (V) row is stored as the E4M3 code nearest to the fp32 quotient
+ * x / k_scale (x / v_scale), computed with IEEE division rounded to nearest;
+ * ties go to the even code and magnitudes beyond 448 are held at 448, with
+ * the sign kept (a result that rounds to zero keeps its sign).  Arguments
+ * as pkv_kv_write; k_scale and v_scale must be positive and finite
+ * (PKV_ERR_SHAPE otherwise).
+ */
+int pkv_kv_write_fp8(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                     int32_t head_size, int32_t block_size,
+                     const void *key, int64_t key_token_stride,
+                     const void *value, int64_t value_token_stride,
+                     const int64_t *slot_mapping, int32_t num_tokens,
+                     float k_scale, float v_scale,
+                     int32_t *device_status, void *stream);
+
+/*
+ * pkv_paged_attn_fp8 — pkv_paged_attn over an E4M3 cache, with K_j and V_j
+ * taken as value(code) * k_scale and value(code) * v_scale; arguments,
+ * workspace and protocol (pkv_paged_attn_combine after it) as
+ * pkv_paged_attn.  Every row, chunks included, runs on the streaming decode
+ * kernel.  Scores, softmax and accumulation are fp32; the query enters the
+ * products as f16 after a per-row power-of-two scaling (exact for every
+ * query element not below 2^-24 of its row's largest).
+ */
+int pkv_paged_attn_fp8(void *out, const void *query, int64_t query_token_stride,
+                       const void *kv_cache, int64_t num_blocks,
+                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                       const int32_t *seq_lens, const int32_t *query_start_loc,
+                       int32_t num_seqs, int32_t num_tokens,
+                       int32_t max_query_len, int32_t max_seq_len,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                       int32_t block_size, float scale, float k_scale, float v_scale,
+                       int32_t num_splits,
+                       void *workspace, size_t workspace_bytes, size_t *workspace_needed,
+                       void *stream);
 
 /*
  * pkv_paged_attn_combine — the log-sum-exp merge of split rows.

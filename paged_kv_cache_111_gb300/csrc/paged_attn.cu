@@ -32,6 +32,9 @@
 // cache slots cannot reach an output.
 #include <mutex>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "attn_internal.cuh"
 
 namespace pkv {
@@ -120,6 +123,7 @@ struct AttnParams {
     int32_t num_q_heads, num_kv_heads, G;
     int64_t num_blocks;
     float scale_log2;         // scale * log2(e)
+    float k_scale, v_scale;   // E4M3 cache: stored code * scale is the value (1 for bf16)
     uint8_t *ws;
 };
 
@@ -523,18 +527,93 @@ __device__ __forceinline__ uint32_t swz(uint32_t box_base, int row, int chunk) {
     return box_base + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <int HD, int NW, int DEPTH>
+// KV8 = false: bf16 cache; ring stages hold pages in the 16-bit layout the
+// MMA loads read (128-byte swizzled 64-column boxes).  KV8 = true: E4M3
+// cache; ring stages hold the raw 8-bit page, which the warp widens to f16
+// into a private staging page of the 16-bit layout before the MMAs.
+template <int HD, int NW, int DEPTH, bool KV8>
 struct DecodeCfg {
     static constexpr int kBoxes = HD / 64;                 // 64-element boxes per row
     static constexpr int kBoxBytes = 2 * kBlock * 128;     // K and V rows of one box: 4 KiB
-    static constexpr int kPageBytes = kBoxes * kBoxBytes;  // one page of one kv head
-    static constexpr int kSmem = NW * DEPTH * kPageBytes + NW * DEPTH * 8 + 1024;
+    static constexpr int kPageBytes = kBoxes * kBoxBytes;  // one 16-bit page of one kv head
+    static constexpr int kStageBytes = KV8 ? 2 * kBlock * HD : kPageBytes;
+    static constexpr int kWarpBytes = DEPTH * kStageBytes + (KV8 ? kPageBytes : 0);
+    static constexpr int kSmem = NW * kWarpBytes + NW * DEPTH * 8 + 1024;
 };
 
-template <int HD, int NW, int DEPTH>
+// MMA element type of the decode kernel: bf16 for a bf16 cache; f16 for an
+// E4M3 cache (E4M3 widens to f16 exactly in one instruction per pair).
+template <bool F16> struct DecodeMath;
+template <> struct DecodeMath<false> {
+    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+        mma_bf16_16816(d, a, b0, b1);
+    }
+    static __device__ __forceinline__ void split(float x, float y, uint32_t &big, uint32_t &rest) {
+        split_bf16x2(x, y, big, rest);
+    }
+};
+template <> struct DecodeMath<true> {
+    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // (x, y) -> f16x2 pair plus its f16x2 remainder (about 22 bits together)
+    static __device__ __forceinline__ void split(float x, float y, uint32_t &big, uint32_t &rest) {
+        const __half2 b = __floats2half2_rn(x, y);
+        const float2 bf = __half22float2(b);
+        const __half2 r = __floats2half2_rn(x - bf.x, y - bf.y);
+        big = *reinterpret_cast<const uint32_t *>(&b);
+        rest = *reinterpret_cast<const uint32_t *>(&r);
+    }
+};
+
+// Widen one raw E4M3 page (linear [2][16][HD] bytes) into the 16-bit staging
+// page: f16 values, 128-byte swizzled 64-column boxes of 32 rows (K rows
+// 0..15, V rows 16..31).  Every lane converts 16-byte pieces.
+template <int HD>
+__device__ __forceinline__ void widen_e4m3_page(uint32_t src, uint32_t dst, int lane) {
+    constexpr int kChunks = 2 * kBlock * HD / 16;
+    constexpr int kBoxBytes = 2 * kBlock * 128;
+#pragma unroll
+    for (int c = lane; c < kChunks; c += 32) {
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(src + c * 16));
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu),
+                                                              __NV_E4M3);
+            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16),
+                                                              __NV_E4M3);
+            h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
+            h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+        }
+        const int e0 = c * 16;                 // first element of the piece
+        const int row = e0 / HD;               // K/V row of the 32-row box
+        const int col = e0 % HD;
+        const uint32_t box = dst + (col / 64) * kBoxBytes;
+        const int ch = (col % 64) / 8;
+        const uint32_t a0 = box + row * 128 + ((ch ^ (row & 7)) << 4);
+        const uint32_t a1 = box + row * 128 + (((ch + 1) ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                     "r"(h[3])
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(h[4]), "r"(h[5]), "r"(h[6]),
+                     "r"(h[7])
+                     : "memory");
+    }
+}
+
+template <int HD, int NW, int DEPTH, bool KV8>
 __global__ void __launch_bounds__(NW * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
-    using Cfg = DecodeCfg<HD, NW, DEPTH>;
+    using Cfg = DecodeCfg<HD, NW, DEPTH, KV8>;
+    using Math = DecodeMath<KV8>;
     constexpr int KSTEPS = HD / 16;       // k-steps of S = Q K^T
     constexpr int NTILES = HD / 8;        // n-tiles of O
     extern __shared__ uint8_t smem_raw[];
@@ -542,9 +621,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    uint8_t *ring = smem + warp * DEPTH * Cfg::kPageBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * DEPTH * Cfg::kPageBytes) + warp * DEPTH;
+    uint8_t *ring = smem + warp * Cfg::kWarpBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * Cfg::kWarpBytes) + warp * DEPTH;
     const uint32_t ring_u32 = smem_u32(ring);
+    const uint32_t staging_u32 = ring_u32 + DEPTH * Cfg::kStageBytes;   // KV8 only
 
     if (lane == 0) {
         for (int s = 0; s < DEPTH; ++s) mbar_init(&bars[s], 1);
@@ -606,11 +686,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
             if (lane == 0) {
                 if (blk < 0 || blk >= p.num_blocks) set_status(status, PKV_ERR_DEVICE_INDEX);
                 const uint32_t st = (seq + k) % DEPTH;
-                uint8_t *dst = ring + st * Cfg::kPageBytes;
-                mbar_arrive_expect_tx(&bars[st], Cfg::kPageBytes);
+                uint8_t *dst = ring + st * Cfg::kStageBytes;
+                mbar_arrive_expect_tx(&bars[st], Cfg::kStageBytes);
+                if constexpr (KV8) {
+                    tma_load_5d(dst, &kv_map, &bars[st], 0, 0, 0, g, blk);       // the whole 8-bit page
+                } else {
 #pragma unroll
-                for (int bx = 0; bx < Cfg::kBoxes; ++bx)
-                    tma_load_5d(dst + bx * Cfg::kBoxBytes, &kv_map, &bars[st], bx * 64, 0, 0, g, blk);
+                    for (int bx = 0; bx < Cfg::kBoxes; ++bx)
+                        tma_load_5d(dst + bx * Cfg::kBoxBytes, &kv_map, &bars[st], bx * 64, 0, 0, g, blk);
+                }
             }
         };
         int issued = min(DEPTH, npages);
@@ -632,6 +716,47 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 qf[kk][3] = R1 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q1p + c + 8)) : 0u;
             }
         }
+        // score factors of the two rows (log2 domain); for an E4M3 cache each
+        // Q row is scaled by a power of two 2^e into [2^14, 2^15) before it is
+        // rounded to f16 (exact but for parts below 2^-24 of the row's
+        // largest), and 2^-e and k_scale go into the factor
+        float sf0 = p.scale_log2, sf1 = p.scale_log2;
+        if constexpr (KV8) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                a0 = fmaxf(a0, fmaxf(fmaxf(fabsf(__uint_as_float(qf[kk][0] << 16)),
+                                           fabsf(__uint_as_float(qf[kk][0] & 0xFFFF0000u))),
+                                     fmaxf(fabsf(__uint_as_float(qf[kk][2] << 16)),
+                                           fabsf(__uint_as_float(qf[kk][2] & 0xFFFF0000u)))));
+                a1 = fmaxf(a1, fmaxf(fmaxf(fabsf(__uint_as_float(qf[kk][1] << 16)),
+                                           fabsf(__uint_as_float(qf[kk][1] & 0xFFFF0000u))),
+                                     fmaxf(fabsf(__uint_as_float(qf[kk][3] << 16)),
+                                           fabsf(__uint_as_float(qf[kk][3] & 0xFFFF0000u)))));
+            }
+            a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
+            a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
+            a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+            a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
+            // e = 14 - floor(log2 a), held in [-114, 126] so 2^e and 2^-e are normal
+            const int e0 = a0 > 0.f ? min(126, max(-114, 14 - ilogbf(a0))) : 0;
+            const int e1 = a1 > 0.f ? min(126, max(-114, 14 - ilogbf(a1))) : 0;
+            const float u0 = __int_as_float((e0 + 127) << 23), u1 = __int_as_float((e1 + 127) << 23);
+            auto to_f16 = [](uint32_t bf2, float u) {
+                const __half2 h = __floats2half2_rn(__uint_as_float(bf2 << 16) * u,
+                                                    __uint_as_float(bf2 & 0xFFFF0000u) * u);
+                return *reinterpret_cast<const uint32_t *>(&h);
+            };
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                qf[kk][0] = to_f16(qf[kk][0], u0);
+                qf[kk][1] = to_f16(qf[kk][1], u1);
+                qf[kk][2] = to_f16(qf[kk][2], u0);
+                qf[kk][3] = to_f16(qf[kk][3], u1);
+            }
+            sf0 = p.scale_log2 * p.k_scale * __int_as_float((127 - e0) << 23);
+            sf1 = p.scale_log2 * p.k_scale * __int_as_float((127 - e1) << 23);
+        }
 
         float o[NTILES][4];
 #pragma unroll
@@ -647,8 +772,24 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 failed_at = k;
                 break;
             }
-            const uint32_t page = ring_u32 + st * Cfg::kPageBytes;
+            uint32_t page = ring_u32 + st * Cfg::kStageBytes;
             const int j0 = (pb + k) * kBlock;       // first key of this page
+            if constexpr (KV8) {
+                // widen the 8-bit page, then hand its stage back to the copy engine
+                widen_e4m3_page<HD>(page, staging_u32, lane);
+                page = staging_u32;
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int nk = k + DEPTH;
+                if (nk < npages) {
+                    if (nk - wbase >= 32) {
+                        wbase += 32;
+                        win = wbase + lane < npages ? __ldg(bt + wbase + lane) : -1;
+                    }
+                    issue(nk);
+                    ++issued;
+                }
+            }
 
             // zero V rows past the end of the sequence (last page only)
             if (j0 + kBlock > L) {
@@ -674,21 +815,21 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 const int chunk = (kk % 4) * 2 + ((lane >> 3) & 1);
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(swz(page + bx * Cfg::kBoxBytes, tok, chunk), b0, b1, b2, b3);
-                mma_bf16_16816(s0, qf[kk], b0, b1);
-                mma_bf16_16816(s1, qf[kk], b2, b3);
+                Math::mma(s0, qf[kk], b0, b1);
+                Math::mma(s1, qf[kk], b2, b3);
             }
 
             // online softmax in the log2 domain; keys a row may not see get -inf
             const int c0 = j0 + 2 * t4, c1 = c0 + 1, c8 = c0 + 8, c9 = c0 + 9;
             float x[8];
-            x[0] = c0 < lim0 ? s0[0] * p.scale_log2 : NEG_INF;
-            x[1] = c1 < lim0 ? s0[1] * p.scale_log2 : NEG_INF;
-            x[2] = c0 < lim1 ? s0[2] * p.scale_log2 : NEG_INF;
-            x[3] = c1 < lim1 ? s0[3] * p.scale_log2 : NEG_INF;
-            x[4] = c8 < lim0 ? s1[0] * p.scale_log2 : NEG_INF;
-            x[5] = c9 < lim0 ? s1[1] * p.scale_log2 : NEG_INF;
-            x[6] = c8 < lim1 ? s1[2] * p.scale_log2 : NEG_INF;
-            x[7] = c9 < lim1 ? s1[3] * p.scale_log2 : NEG_INF;
+            x[0] = c0 < lim0 ? s0[0] * sf0 : NEG_INF;
+            x[1] = c1 < lim0 ? s0[1] * sf0 : NEG_INF;
+            x[2] = c0 < lim1 ? s0[2] * sf1 : NEG_INF;
+            x[3] = c1 < lim1 ? s0[3] * sf1 : NEG_INF;
+            x[4] = c8 < lim0 ? s1[0] * sf0 : NEG_INF;
+            x[5] = c9 < lim0 ? s1[1] * sf0 : NEG_INF;
+            x[6] = c8 < lim1 ? s1[2] * sf1 : NEG_INF;
+            x[7] = c9 < lim1 ? s1[3] * sf1 : NEG_INF;
             float mx0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[4], x[5]));
             float mx1 = fmaxf(fmaxf(x[2], x[3]), fmaxf(x[6], x[7]));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -713,13 +854,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 o[n][2] *= a1;
                 o[n][3] *= a1;
             }
-            // P as a bf16 pair (hi + remainder): the PV product keeps about
-            // 16 bits of each weight instead of bf16's 8
+            // P as a 16-bit pair (hi + remainder): the PV product keeps about
+            // 16 bits (bf16) or 22 bits (f16) of each weight
             uint32_t pa[4], pl[4];
-            split_bf16x2(pr[0], pr[1], pa[0], pl[0]);
-            split_bf16x2(pr[2], pr[3], pa[1], pl[1]);
-            split_bf16x2(pr[4], pr[5], pa[2], pl[2]);
-            split_bf16x2(pr[6], pr[7], pa[3], pl[3]);
+            Math::split(pr[0], pr[1], pa[0], pl[0]);
+            Math::split(pr[2], pr[3], pa[1], pl[1]);
+            Math::split(pr[4], pr[5], pa[2], pl[2]);
+            Math::split(pr[6], pr[7], pa[3], pl[3]);
 
             // O += P V (V rows are the page's tokens, read transposed)
 #pragma unroll
@@ -729,23 +870,27 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 const int chunk = (n % 8) + (lane >> 4);
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_trans(swz(page + bx * Cfg::kBoxBytes, kBlock + tok, chunk), b0, b1, b2, b3);
-                mma_bf16_16816(o[n], pa, b0, b1);
-                mma_bf16_16816(o[n + 1], pa, b2, b3);
-                mma_bf16_16816(o[n], pl, b0, b1);
-                mma_bf16_16816(o[n + 1], pl, b2, b3);
+                Math::mma(o[n], pa, b0, b1);
+                Math::mma(o[n + 1], pa, b2, b3);
+                Math::mma(o[n], pl, b0, b1);
+                Math::mma(o[n + 1], pl, b2, b3);
             }
 
-            // refill this stage with page k + DEPTH of the chunk
-            fence_proxy_async_smem();
-            __syncwarp();
-            const int nk = k + DEPTH;
-            if (nk < npages) {
-                if (nk - wbase >= 32) {
-                    wbase += 32;
-                    win = wbase + lane < npages ? __ldg(bt + wbase + lane) : -1;
+            if constexpr (!KV8) {
+                // refill this stage with page k + DEPTH of the chunk
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int nk = k + DEPTH;
+                if (nk < npages) {
+                    if (nk - wbase >= 32) {
+                        wbase += 32;
+                        win = wbase + lane < npages ? __ldg(bt + wbase + lane) : -1;
+                    }
+                    issue(nk);
+                    ++issued;
                 }
-                issue(nk);
-                ++issued;
+            } else {
+                __syncwarp();                    // the staging page is rewritten by the next page
             }
         }
 
@@ -765,8 +910,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
         l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-        const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        // (an E4M3 cache's V values are code * v_scale: the scale is applied once here)
+        const float inv0 = l0 > 0.f ? (KV8 ? p.v_scale / l0 : 1.f / l0) : 0.f;
+        const float inv1 = l1 > 0.f ? (KV8 ? p.v_scale / l1 : 1.f / l1) : 0.f;
         const int h0 = g * p.G + hh0, h1 = g * p.G + hh1;
         if (n_split <= 1) {
             if (R0 < rows) {
@@ -904,30 +1050,53 @@ static int make_kv_map(CUtensorMap *map, const void *kv_cache, int64_t num_block
     return rc == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <int HD, int NW, int DEPTH>
+// Tensor map of an E4M3 cache as a 5-D byte tensor {head_size, 16, 2, Hkv,
+// num_blocks}; one box is a whole page of one kv head (K and V rows, 2*16*d
+// bytes), unswizzled: the kernel widens it to f16 itself.
+static int make_kv_map_e4m3(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                            int32_t head_size) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return PKV_ERR_CUDA;
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2,
+                                static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t row = static_cast<cuuint64_t>(head_size);
+    const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * num_kv_heads};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(head_size), kBlock, 2, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult rc = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(kv_cache), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+template <int HD, int NW, int DEPTH, bool KV8>
 static int launch_decode(const CUtensorMap &map, const AttnParams &p, int grid, int dev, cudaStream_t stream) {
-    using Cfg = DecodeCfg<HD, NW, DEPTH>;
+    using Cfg = DecodeCfg<HD, NW, DEPTH, KV8>;
     static std::mutex mu;
     static uint64_t done_mask = 0;       // devices whose shared-memory limit is already raised
     {
         std::lock_guard<std::mutex> lock(mu);
         const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
         if (!bit || !(done_mask & bit)) {
-            if (cudaFuncSetAttribute(decode_kernel<HD, NW, DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(decode_kernel<HD, NW, DEPTH, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Cfg::kSmem) != cudaSuccess)
                 return PKV_ERR_CUDA;
             done_mask |= bit;
         }
     }
-    if (launch_pdl(decode_kernel<HD, NW, DEPTH>, dim3(grid), dim3(NW * 32), Cfg::kSmem, stream, map, p) != cudaSuccess)
+    if (launch_pdl(decode_kernel<HD, NW, DEPTH, KV8>, dim3(grid), dim3(NW * 32), Cfg::kSmem, stream, map, p) !=
+        cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }
 
 // decode tiling per head size: warps per CTA, ring stages per warp, CTAs per SM
-template <int HD> struct DecodeTiling;
+template <int HD, bool KV8 = false> struct DecodeTiling;
 template <> struct DecodeTiling<64> { static constexpr int NW = 4, DEPTH = 6, CTAS_PER_SM = 2; };
 template <> struct DecodeTiling<128> { static constexpr int NW = 4, DEPTH = 3, CTAS_PER_SM = 2; };
+// E4M3 pages are half the bytes: more stages in flight, plus one staging page per warp
+template <> struct DecodeTiling<64, true> { static constexpr int NW = 4, DEPTH = 8, CTAS_PER_SM = 2; };
+template <> struct DecodeTiling<128, true> { static constexpr int NW = 4, DEPTH = 4, CTAS_PER_SM = 2; };
 
 }  // namespace pkv
 
@@ -939,7 +1108,8 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
                            int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len, int32_t num_q_heads,
                            int32_t num_kv_heads, int32_t head_size, int32_t block_size, float scale,
                            int32_t num_splits, int32_t prefix_blocks, void *workspace, size_t workspace_bytes,
-                           size_t *workspace_needed, void *stream) {
+                           size_t *workspace_needed, void *stream, bool kv8 = false, float k_scale = 1.f,
+                           float v_scale = 1.f) {
     // ---- host-side validation: nothing is enqueued on error ----
     if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_query_len < 0 ||
         max_seq_len < 0 || max_blocks_per_seq < 0 || num_splits < 0 || prefix_blocks < 0)
@@ -952,9 +1122,12 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     if (static_cast<int64_t>(max_blocks_per_seq) * kBlock < max_seq_len) return PKV_ERR_SHAPE;
     if (num_blocks < 1 || num_blocks > INT32_MAX) return PKV_ERR_SHAPE;
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PKV_ERR_SHAPE;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale > 3.0e38f || v_scale > 3.0e38f) return PKV_ERR_SHAPE;
 
-    // the shared-prefix pass runs on the tensor-core tile kernel
-    if (!prefill_supported(num_q_heads, num_kv_heads, head_size)) prefix_blocks = 0;
+    // the tensor-core tile kernel (long chunks, the shared-prefix pass) reads
+    // bf16 pages only; with an E4M3 cache every row runs on the decode kernel
+    const bool prefill_ok = !kv8 && prefill_supported(num_q_heads, num_kv_heads, head_size);
+    if (!prefill_ok) prefix_blocks = 0;
     const WsLayout lay = ws_layout(num_seqs, num_tokens, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
                                    head_size, prefix_blocks);
     if (workspace_needed) *workspace_needed = static_cast<size_t>(lay.total);
@@ -977,10 +1150,11 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PKV_ERR_CUDA;
 
     CUtensorMap map;
-    int rc = make_kv_map(&map, kv_cache, num_blocks, num_kv_heads, head_size);
+    int rc = kv8 ? make_kv_map_e4m3(&map, kv_cache, num_blocks, num_kv_heads, head_size)
+                 : make_kv_map(&map, kv_cache, num_blocks, num_kv_heads, head_size);
     if (rc) return rc;
 
-    const int nw = head_size == 64 ? DecodeTiling<64>::NW : DecodeTiling<128>::NW;
+    const int nw = head_size == 64 ? DecodeTiling<64>::NW : DecodeTiling<128>::NW;   // 4 in every tiling
     const int per_sm = head_size == 64 ? DecodeTiling<64>::CTAS_PER_SM : DecodeTiling<128>::CTAS_PER_SM;
     int64_t grid = static_cast<int64_t>(sms) * per_sm;
     const int64_t max_items = lay.max_chunks * num_kv_heads;
@@ -1001,7 +1175,6 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     pp.max_seq_len = max_seq_len;
     pp.num_splits = num_splits;
     pp.total_warps = static_cast<int32_t>(grid * nw);
-    const bool prefill_ok = prefill_supported(num_q_heads, num_kv_heads, head_size);
     const int G = num_q_heads / num_kv_heads;
     const bool may_prefill = prefill_ok && static_cast<int64_t>(max_query_len) * G > kDecodeTileMaxRows;
     pp.prefill_ok = prefill_ok ? 1 : 0;
@@ -1023,11 +1196,21 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     ap.G = num_q_heads / num_kv_heads;
     ap.num_blocks = num_blocks;
     ap.scale_log2 = scale * 1.4426950408889634f;
+    ap.k_scale = k_scale;
+    ap.v_scale = v_scale;
     ap.ws = static_cast<uint8_t *>(workspace);
-    rc = head_size == 64
-             ? launch_decode<64, DecodeTiling<64>::NW, DecodeTiling<64>::DEPTH>(map, ap, static_cast<int>(grid), dev, st)
-             : launch_decode<128, DecodeTiling<128>::NW, DecodeTiling<128>::DEPTH>(map, ap, static_cast<int>(grid), dev,
-                                                                                   st);
+    if (kv8) {
+        using T64 = DecodeTiling<64, true>;
+        using T128 = DecodeTiling<128, true>;
+        rc = head_size == 64 ? launch_decode<64, T64::NW, T64::DEPTH, true>(map, ap, static_cast<int>(grid), dev, st)
+                             : launch_decode<128, T128::NW, T128::DEPTH, true>(map, ap, static_cast<int>(grid), dev, st);
+    } else {
+        using T64 = DecodeTiling<64>;
+        using T128 = DecodeTiling<128>;
+        rc = head_size == 64 ? launch_decode<64, T64::NW, T64::DEPTH, false>(map, ap, static_cast<int>(grid), dev, st)
+                             : launch_decode<128, T128::NW, T128::DEPTH, false>(map, ap, static_cast<int>(grid), dev,
+                                                                                 st);
+    }
     if (rc || (!may_prefill && prefix_blocks == 0)) return rc;
     PrefillParams fp;
     fp.out = ap.out;
@@ -1104,4 +1287,17 @@ extern "C" int pkv_paged_attn_combine(void *out, const void *workspace, size_t w
                         : launch_pdl(combine_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, o, w,
                                      num_tokens, num_q_heads);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_paged_attn_fp8(void *out, const void *query, int64_t query_token_stride, const void *kv_cache,
+                                  int64_t num_blocks, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_seqs,
+                                  int32_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                                  float scale, float k_scale, float v_scale, int32_t num_splits, void *workspace,
+                                  size_t workspace_bytes, size_t *workspace_needed, void *stream) {
+    return pkv::paged_attn_impl(out, query, query_token_stride, kv_cache, num_blocks, block_tables,
+                                max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_tokens, max_query_len,
+                                max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale, num_splits, 0,
+                                workspace, workspace_bytes, workspace_needed, stream, true, k_scale, v_scale);
 }
