@@ -570,32 +570,45 @@ template <> struct DecodeMath<true> {
     }
 };
 
+// Four E4M3 values (one 32-bit word, element 0 in the low byte) -> two f16x2
+// words (elements 0,1 and 2,3; the lower element in the low half).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &h01, uint32_t &h23) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w));
+}
+
 // Widen one raw E4M3 page (linear [2][16][HD] bytes) into the 16-bit staging
 // page: f16 values, 128-byte swizzled 64-column boxes of 32 rows (K rows
-// 0..15, V rows 16..31).  Every lane converts 16-byte pieces.
+// 0..15, V rows 16..31).  Every lane converts 16-byte pieces.  At HD = 128 a
+// quarter-warp takes two rows, half a row each, in alternating halves, so
+// that both its 8-bit reads and its 16-bit stores hit eight distinct bank
+// groups.
 template <int HD>
 __device__ __forceinline__ void widen_e4m3_page(uint32_t src, uint32_t dst, int lane) {
     constexpr int kChunks = 2 * kBlock * HD / 16;
     constexpr int kBoxBytes = 2 * kBlock * 128;
 #pragma unroll
-    for (int c = lane; c < kChunks; c += 32) {
+    for (int q = lane; q < kChunks; q += 32) {
+        int row, col;
+        if constexpr (HD == 128) {
+            const int ph = q >> 3, k = q & 7, sub = k >> 2;
+            row = 2 * (ph >> 1) + sub;
+            col = 16 * (4 * (sub ^ (ph & 1)) + (k & 3));
+        } else {
+            row = (q * 16) / HD;
+            col = (q * 16) % HD;
+        }
         uint32_t w[4];
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                     : "r"(src + c * 16));
+                     : "r"(src + row * HD + col));
         uint32_t h[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu),
-                                                              __NV_E4M3);
-            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16),
-                                                              __NV_E4M3);
-            h[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-            h[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-        }
-        const int e0 = c * 16;                 // first element of the piece
-        const int row = e0 / HD;               // K/V row of the 32-row box
-        const int col = e0 % HD;
+        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x4(w[i], h[2 * i], h[2 * i + 1]);
         const uint32_t box = dst + (col / 64) * kBoxBytes;
         const int ch = (col % 64) / 8;
         const uint32_t a0 = box + row * 128 + ((ch ^ (row & 7)) << 4);
@@ -836,24 +849,32 @@ __global__ void __launch_bounds__(NW * 32, 1)
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float ref0 = mn0 == NEG_INF ? 0.f : mn0;
-            const float ref1 = mn1 == NEG_INF ? 0.f : mn1;
-            const float a0 = fast_exp2(m0 - ref0), a1 = fast_exp2(m1 - ref1);
-            m0 = mn0;
-            m1 = mn1;
+            // a row's reference maximum moves only on its first visible key or
+            // when the page's maximum exceeds it by more than 2^8, so weights
+            // stay below 2^8 and O is rescaled (warp-uniformly) only then
+            const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;
+            if (__any_sync(0xffffffffu, up0 || up1)) {
+                const float a0 = up0 ? fast_exp2(m0 - mx0) : 1.f;   // 0 when m = -inf
+                const float a1 = up1 ? fast_exp2(m1 - mx1) : 1.f;
+                m0 = up0 ? mx0 : m0;
+                m1 = up1 ? mx1 : m1;
+                l0 *= a0;
+                l1 *= a1;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a0;
+                    o[n][2] *= a1;
+                    o[n][3] *= a1;
+                }
+            }
+            const float ref0 = m0 == NEG_INF ? 0.f : m0;
+            const float ref1 = m1 == NEG_INF ? 0.f : m1;
             float pr[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) pr[e] = fast_exp2(x[e] - (((e >> 1) & 1) ? ref1 : ref0));
-            l0 = l0 * a0 + (pr[0] + pr[1] + pr[4] + pr[5]);
-            l1 = l1 * a1 + (pr[2] + pr[3] + pr[6] + pr[7]);
-#pragma unroll
-            for (int n = 0; n < NTILES; ++n) {
-                o[n][0] *= a0;
-                o[n][1] *= a0;
-                o[n][2] *= a1;
-                o[n][3] *= a1;
-            }
+            l0 += (pr[0] + pr[1] + pr[4] + pr[5]);
+            l1 += (pr[2] + pr[3] + pr[6] + pr[7]);
             // P as a 16-bit pair (hi + remainder): the PV product keeps about
             // 16 bits (bf16) or 22 bits (f16) of each weight
             uint32_t pa[4], pl[4];

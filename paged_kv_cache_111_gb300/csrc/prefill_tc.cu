@@ -19,8 +19,8 @@
 //                  (bf16) to shared memory
 //   O += P V       tcgen05.mma, A = P (K-major), B = V (MN-major), D = O in
 //                  tensor memory
-// Warp roles: warp 0 loads (TMA: Q once, K and V pages through the block
-// table into a two-stage ring), warp 1 issues the MMAs, warp 2 owns the
+// Warp roles: warp 0 loads (TMA: K and V pages through the block table into
+// a three-stage ring), warp 1 issues the MMAs, warp 2 owns the
 // tensor-memory allocation, warps 4-7 do softmax and the epilogue.
 //
 // When any row of the tile puts a large share of its weight on few keys of
@@ -53,7 +53,12 @@ struct PrefillCfg {
 };
 
 enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kKFull2, kVFull0, kVFull1, kVFull2, kKEmpty0, kKEmpty1, kKEmpty2,
-                  kVEmpty0, kVEmpty1, kVEmpty2, kSFull0, kSFull1, kPFull, kODone0, kODone1, kVFix, kNumBars };
+                  kVEmpty0, kVEmpty1, kVEmpty2, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kVFix,
+                  kNumBars };
+static_assert(kNumBars * 8 + 48 <= 256, "barriers, the TMEM address slot and the votes fit their 256 bytes");
+// P of tile j is announced on kPFull0 + (j & 1): with one barrier per parity a
+// barrier never runs two phases ahead of the MMA thread's wait on it (the
+// softmax warps can finish tile j + 1 before the MMA thread looks at tile j).
 
 // A row whose weights in a KV tile are concentrated (sum of squared weights
 // of the tile above this fraction of the squared running sum) needs P's bf16
@@ -130,7 +135,8 @@ __global__ void __launch_bounds__(256, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], (b == kPFull || b == kQFull) ? 4 : 1);
+        for (int b = 0; b < kNumBars; ++b)
+            mbar_init(&bars[b], (b == kPFull0 || b == kPFull1 || b == kQFull) ? 4 : 1);
         tma_prefetch_desc(&kv_map);
     }
     if (warp == 2) {
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int st = j % S;
-                ok = pf_wait(&bars[kPFull], j & 1, status);
+                ok = pf_wait(&bars[kPFull0 + (j & 1)], (j >> 1) & 1, status);
                 if (ok) ok = pf_wait(&bars[kVFull0 + st], (j / S) & 1, status);
                 if (ok && j == end_tile) ok = pf_wait(&bars[kVFix], 0, status);
                 if (!ok) break;
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) votes[(j & 1) * 4 + (warp - 4)] = wneed ? 1u : 0u;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kPFull]);
+            if (lane == 0) mbar_arrive(&bars[kPFull0 + (j & 1)]);
         }
         if (ok) {
             // epilogue: the last two P V, then O / l to bf16
