@@ -224,7 +224,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    step = wl.make_workload(args.workload, seed=replica_seed(args.workload, rank))
+    step = wl.make_workload(args.workload, seed=replica_seed(args.workload, rank),
+                            permute_blocks=not args.contiguous_blocks)
     if args.subset:
         # the first `subset` requests with a compact pool (profiling-size case)
         step = step.subset(list(range(min(args.subset, step.num_seqs))), name=f"{args.workload}[:{args.subset}]")
@@ -528,6 +529,8 @@ def main():
     ap.add_argument("--shared-prefix-blocks", type=int, default=-1,
                     help="cascade over this many shared leading table blocks (pkv_paged_attn_shared_prefix); "
                          "-1: the prefix every request's table shares with request 0's, 0: plain paged_attn")
+    ap.add_argument("--contiguous-blocks", action="store_true",
+                    help="hand out physical blocks in order (no random permutation): the cost-of-paging comparison")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="cache element type: bf16, or E4M3 with per-tensor K/V scales (pkv_*_fp8)")
     ap.add_argument("--subset", type=int, default=0,
@@ -576,6 +579,7 @@ def main():
             "kv_bytes_per_step": ab["kv_unique"], "parallelism": f"replicas x{world}",
             "launch": "cuda graph replay" if args.graph else "eager",
             "shared_prefix_blocks": r["shared_prefix_blocks"],
+            "physical_blocks": "in order" if args.contiguous_blocks else "random permutation",
             "kv_cache": (f"e4m3, k_scale {r['fp8_scales'][0]:.6g}, v_scale {r['fp8_scales'][1]:.6g}"
                          if fp8 else "bf16"),
             "l2": "inputs larger than L2 (KV read per step above 129 MB), no flush"

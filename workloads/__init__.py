@@ -35,6 +35,7 @@ workload seed, a tag per tensor and the chunk index.
 from __future__ import annotations
 
 import dataclasses
+import functools
 import math
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -446,13 +447,19 @@ def seed_of(name: str) -> int:
     return 20260000 + WORKLOADS[name]["id"]
 
 
-def make_workload(name: str, seed: Optional[int] = None) -> Step:
-    """Build one of the named workloads (full size)."""
+def make_workload(name: str, seed: Optional[int] = None, permute_blocks: bool = True) -> Step:
+    """Build one of the named workloads (full size).
+
+    ``permute_blocks=False`` hands out physical blocks in order (each
+    request's pages contiguous in the pool), the same draws otherwise: the
+    contiguous-cache comparison point for the cost of paging.
+    """
     if name not in WORKLOADS:
         raise KeyError(f"unknown workload {name!r}; known: {sorted(WORKLOADS)}")
     seed = seed_of(name) if seed is None else seed
     gen = torch.Generator().manual_seed(seed)
     text = WORKLOADS[name]["text"]
+    build_step = functools.partial(_build_step_any, permute_blocks=permute_blocks)
     if name == "tiny-decode":
         L = torch.randint(1, 129, (4,), generator=gen).tolist()
         reqs = [RequestSpec(l - 1, 1) for l in L]
@@ -478,6 +485,10 @@ def make_workload(name: str, seed: Optional[int] = None) -> Step:
         return build_step(name, reqs, 64, 8, 128, 200000, seed, gen=gen,
                           shared_prefix_len=1024, forks=list(range(8)), description=text)
     raise AssertionError(name)
+
+
+def _build_step_any(*args, permute_blocks: bool = True, **kw) -> Step:
+    return build_step(*args, permute_blocks=permute_blocks, **kw)
 
 
 def make_poisoned_pool_like(step: Step, device=None) -> torch.Tensor:
