@@ -269,10 +269,12 @@ __global__ void __launch_bounds__(256, 1)
                 if (lo) issue_pv(j, pbuf + Cfg::kPLo, 1);
                 umma_commit(&bars[kODone0 + (j & 1)]);
                 umma_commit(&bars[kVEmpty0 + st]);
-                // S of tile j+2 reuses S buffer j & 1: issued after P V of tile j
-                // (tensor-core operations of one thread run in issue order)
+                // S of tile j+2 overwrites S buffer j & 1, where P V of tile j reads
+                // P: it is issued only once that product has completed (no
+                // overlap of a tensor-memory operand read with a later write)
                 if (j + 2 < n_kv) {
-                    ok = pf_wait(&bars[kKFull0 + (j + 2) % S], ((j + 2) / S) & 1, status);
+                    ok = pf_wait(&bars[kODone0 + (j & 1)], (j >> 1) & 1, status);
+                    if (ok) ok = pf_wait(&bars[kKFull0 + (j + 2) % S], ((j + 2) / S) & 1, status);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(j + 2);
