@@ -11,17 +11,22 @@
 // One CTA computes one 128-row tile for one kv head.  Rows are
 // (query token, q head of the GQA group) pairs, so one K/V tile in shared
 // memory serves every q head of the group.  Per 128-key KV tile:
-//   S = Q K^T      tcgen05.mma, A = Q and B = K from shared memory (K-major,
-//                  128-byte swizzle), D in tensor memory (two S buffers)
-//   softmax        one thread per row reads its S row from tensor memory,
-//                  masks, keeps a running max (rescaling O in tensor memory
-//                  only when the max grows by more than 2^8) and writes P
-//                  (bf16) to shared memory
-//   O += P V       tcgen05.mma, A = P (K-major), B = V (MN-major), D = O in
-//                  tensor memory
+//   S = Q K^T      tcgen05.mma, A = Q from tensor memory, B = K from shared
+//                  memory (K-major, 128-byte swizzle), D in tensor memory
+//                  (two S buffers)
+//   softmax        two threads per row, each with half of the tile's keys,
+//                  read S from tensor memory, mask, share their row maxima
+//                  through shared memory, keep a running max (rescaling
+//                  their half of O only when the max grows by more than 2^8)
+//                  and write P (bf16) over S
+//   O += P V       tcgen05.mma, A = P from tensor memory, B = V (MN-major)
+//                  from shared memory, D = O in tensor memory
+// Every product reads A from tensor memory: on this part a change between
+// shared-memory and tensor-memory A operands from one group of MMAs to the
+// next costs about a third of the tensor pipe's rate.
 // Warp roles: warp 0 loads (TMA: K and V pages through the block table into
 // a three-stage ring), warp 1 issues the MMAs, warp 2 owns the
-// tensor-memory allocation, warps 4-7 do softmax and the epilogue.
+// tensor-memory allocation, warps 4-11 do softmax and the epilogue.
 //
 // When any row of the tile puts a large share of its weight on few keys of
 // a KV tile (rows with few visible keys, or a peaked softmax), that tile's P
@@ -44,7 +49,8 @@ struct PrefillCfg {
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-    static constexpr int kSmem = kOffBar + 256 + 1024;      // + barriers + alignment slack
+    static constexpr int kOffXchg = kOffBar + 512;            // softmax halves' maxima and sums (3 KiB)
+    static constexpr int kSmem = kOffXchg + 3072 + 1024;    // + alignment slack
     // tensor memory: two S buffers (each later holding that tile's P and its
     // bf16 remainder), O, and Q as the A operand of S = Q K^T
     static constexpr uint32_t kTmemCols = 512;
@@ -54,8 +60,9 @@ struct PrefillCfg {
 
 enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kKFull2, kVFull0, kVFull1, kVFull2, kKEmpty0, kKEmpty1, kKEmpty2,
                   kVEmpty0, kVEmpty1, kVEmpty2, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kVFix,
+                  kXchg0, kXchg1, kXchg2, kXchg3,      // the two softmax warps of a lane quadrant
                   kNumBars };
-static_assert(kNumBars * 8 + 48 <= 256, "barriers, the TMEM address slot and the votes fit their 256 bytes");
+static_assert(kNumBars * 8 + 16 + 64 <= 512, "barriers, the TMEM address slot and the votes fit their 512 bytes");
 // P of tile j is announced on kPFull0 + (j & 1): with one barrier per parity a
 // barrier never runs two phases ahead of the MMA thread's wait on it (the
 // softmax warps can finish tile j + 1 before the MMA thread looks at tile j).
@@ -65,6 +72,62 @@ static_assert(kNumBars * 8 + 48 <= 256, "barriers, the TMEM address slot and the
 // remainder in P V: bf16 rounding of a few large weights would otherwise
 // exceed the output tolerance.
 constexpr float kLoConcentration = 0.01f;
+
+// ---- softmax arithmetic on fp32 pairs (Blackwell f32x2 instructions) ----------------
+
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 2^y for a pair, on the FMA pipe (the special-function unit runs one
+// exponential per lane every few cycles; part of a tile's exponentials go
+// here instead).  y is held at >= -125 (weights below 2^-125 of the row's
+// reference are negligible); y = n + f with n the nearest integer (found by
+// adding 1.5 * 2^23, whose low bits then hold n) and f in [-1/2, 1/2]; 2^f is
+// a degree-5 polynomial fitted here by least squares on Chebyshev nodes with
+// relative weights (relative error 2.3e-7 in fp32); 2^n enters as n added to
+// the exponent field.
+__device__ __forceinline__ uint64_t f2_exp2_poly(uint64_t y2) {
+    constexpr float kMagic = 12582912.0f;            // 1.5 * 2^23
+    float y0, y1;
+    f2_unpack(y2, y0, y1);
+    y0 = fmaxf(y0, -125.f);
+    y1 = fmaxf(y1, -125.f);
+    const uint64_t y = f2_pack(y0, y1);
+    const uint64_t ym = f2_add(y, f2_pack(kMagic, kMagic));            // n in the low mantissa bits
+    const uint64_t n = f2_add(ym, f2_pack(-kMagic, -kMagic));
+    const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), y);
+    uint64_t q = f2_fma(f, f2_pack(1.326744794e-3f, 1.326744794e-3f), f2_pack(9.675463662e-3f, 9.675463662e-3f));
+    q = f2_fma(q, f, f2_pack(5.550741032e-2f, 5.550741032e-2f));
+    q = f2_fma(q, f, f2_pack(2.402212173e-1f, 2.402212173e-1f));
+    q = f2_fma(q, f, f2_pack(6.931469440e-1f, 6.931469440e-1f));
+    q = f2_fma(q, f, f2_pack(1.000000119f, 1.000000119f));
+    float q0, q1, m0, m1;
+    f2_unpack(q, q0, q1);
+    f2_unpack(ym, m0, m1);
+    return f2_pack(__int_as_float(__float_as_int(q0) + (__float_as_int(m0) << 23)),
+                   __int_as_float(__float_as_int(q1) + (__float_as_int(m1) << 23)));
+}
 
 // Bounded wait shared by every role; on timeout records the error and
 // reports it so the role can stop.
@@ -82,7 +145,7 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t 
 // each row (normalised partial output and its log-sum-exp), merged with the
 // row's other splits by the combine.
 template <int HD, bool CASCADE>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16 *__restrict__ query,
                    const int64_t q_stride, const PrefillParams p) {
     using Cfg = PrefillCfg<HD>;
@@ -91,7 +154,7 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
-    volatile uint32_t *votes = tmem_slot + 4;          // [2 tiles in flight][4 softmax warps]
+    volatile uint32_t *votes = tmem_slot + 4;          // [2 tiles in flight][8 softmax warps]
     const uint32_t sK = smem_u32(smem + Cfg::kOffK);
     const uint32_t sV = smem_u32(smem + Cfg::kOffV);
 
@@ -136,7 +199,7 @@ __global__ void __launch_bounds__(256, 1)
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b)
-            mbar_init(&bars[b], (b == kPFull0 || b == kPFull1 || b == kQFull) ? 4 : 1);
+            mbar_init(&bars[b], (b == kPFull0 || b == kPFull1 || b == kQFull) ? 8 : (b >= kXchg0 ? 2 : 1));
         tma_prefetch_desc(&kv_map);
     }
     if (warp == 2) {
@@ -227,27 +290,37 @@ __global__ void __launch_bounds__(256, 1)
             constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillRows, HD, 0, 1);
             bool ok = pf_wait(&bars[kQFull], 0, status);
             // S(j) = Q K^T into S buffer j & 1; A = Q in tensor memory
+            // descriptors are built once per stage; a K step advances the
+            // start-address field (16-byte units, never carrying past its 14
+            // bits: shared-memory addresses are below 2^18)
+            uint64_t dk[S], dv[S];
+#pragma unroll
+            for (int st = 0; st < S; ++st) {
+                dk[st] = smem_desc_sw128(sK + st * Cfg::kKVBytes, 16, 1024);
+                dv[st] = smem_desc_sw128(sV + st * Cfg::kKVBytes, kPrefillKeys * 128, 1024);
+            }
             auto issue_s = [&](int j) {
                 const int st = j % S;
                 const uint32_t d = tmem + ((j & 1) ? Cfg::kColS1 : Cfg::kColS0);
+                const uint64_t b0 = dk[st];
+                umma_bf16_ts_c<false>(d, tmem + Cfg::kColQ, b0, kIdescS);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint64_t b = smem_desc_sw128(sK + st * Cfg::kKVBytes + (kk >> 2) * (kPrefillKeys * 128) +
-                                                           (kk & 3) * 32,
-                                                       16, 1024);
-                    umma_bf16_ts(d, tmem + Cfg::kColQ + kk * 8, b, kIdescS, kk > 0);
-                }
+                for (int kk = 1; kk < HD / 16; ++kk)
+                    umma_bf16_ts_c<true>(d, tmem + Cfg::kColQ + kk * 8, b0 + (((kk >> 2) * (kPrefillKeys * 128) +
+                                                                              (kk & 3) * 32) >> 4),
+                                         kIdescS);
                 umma_commit(&bars[kSFull0 + (j & 1)]);
                 umma_commit(&bars[kKEmpty0 + st]);
             };
             // O (+)= P V; A = P (or its remainder) in S buffer j & 1
-            auto issue_pv = [&](int j, uint32_t pcol, uint32_t accumulate) {
+            auto issue_pv = [&](int j, uint32_t pcol, bool accumulate) {
                 const int st = j % S;
+                const uint64_t b0 = dv[st];
+                if (accumulate) umma_bf16_ts_c<true>(tmem + Cfg::kColO, pcol, b0, kIdescO);
+                else umma_bf16_ts_c<false>(tmem + Cfg::kColO, pcol, b0, kIdescO);
 #pragma unroll
-                for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
-                    const uint64_t b = smem_desc_sw128(sV + st * Cfg::kKVBytes + kk * 2048, kPrefillKeys * 128, 1024);
-                    umma_bf16_ts(tmem + Cfg::kColO, pcol + kk * 8, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < kPrefillKeys / 16; ++kk)
+                    umma_bf16_ts_c<true>(tmem + Cfg::kColO, pcol + kk * 8, b0 + ((kk * 2048) >> 4), kIdescO);
             };
             for (int j0 = 0; j0 < 2 && j0 < n_kv && ok; ++j0) {
                 ok = pf_wait(&bars[kKFull0 + j0], 0, status);
@@ -263,10 +336,12 @@ __global__ void __launch_bounds__(256, 1)
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t pbuf = tmem + ((j & 1) ? Cfg::kColS1 : Cfg::kColS0);
-                const bool lo = (votes[(j & 1) * 4 + 0] | votes[(j & 1) * 4 + 1] | votes[(j & 1) * 4 + 2] |
-                                 votes[(j & 1) * 4 + 3]) != 0u;
+                uint32_t vote = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) vote |= votes[(j & 1) * 8 + w];
+                const bool lo = vote != 0u;
                 issue_pv(j, pbuf, j > 0);
-                if (lo) issue_pv(j, pbuf + Cfg::kPLo, 1);
+                if (lo) issue_pv(j, pbuf + Cfg::kPLo, true);
                 umma_commit(&bars[kODone0 + (j & 1)]);
                 umma_commit(&bars[kVEmpty0 + st]);
                 // S of tile j+2 overwrites S buffer j & 1, where P V of tile j reads
@@ -283,9 +358,13 @@ __global__ void __launch_bounds__(256, 1)
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ---------------- softmax + epilogue: thread = row ----------------
-        const int row = threadIdx.x - 128;
-        const int lane_base = (warp - 4) * 32;
+        // ---------------- softmax + epilogue: two threads per row ----------------
+        // warps 4-7 take keys (and output columns) of the first half of the tile,
+        // warps 8-11 the second half; warp w reads tensor-memory lanes of quadrant
+        // w % 4, so warps w and w + 4 share their 32 rows
+        const int quad = warp & 3;
+        const int half = (warp - 4) >> 2;
+        const int row = quad * 32 + lane;
         const int rrow = row0 + row;                       // request row (cascade: row of the prefix pass)
         const bool valid = rrow < rows_total;
         // the row's query token and q head within the group; keys [0, lim) visible
@@ -304,26 +383,42 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
         const float NEG_INF = -__int_as_float(0x7f800000);
-        const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        constexpr int kHalfKeys = kPrefillKeys / 2;        // keys of a tile per thread
+        constexpr int kHalfDims = HD / 2;                   // output columns per thread
+        // exchange of the two halves' row maxima (by tile parity) and final sums
+        float *xmax = reinterpret_cast<float *>(smem + Cfg::kOffXchg);          // [2][2][128]
+        float *xsum = xmax + 2 * 2 * kPrefillRows;                               // [2][128]
+        // the two warps of this quadrant meet on an mbarrier, one phase per
+        // tile plus one for the final sums (bounded waits, like every other)
+        uint64_t *xbar = &bars[kXchg0 + quad];
+        auto exchange = [&](int phase) -> bool {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xbar);
+            const bool done = __all_sync(0xffffffffu, pf_wait(xbar, phase & 1, status));
+            tc_fence_after();
+            return done;
+        };
         bool ok = true;
 
-        // Q row -> tensor memory (A operand of S = Q K^T), zeros past the request
+        // this half of the Q row -> tensor memory (A operand of S = Q K^T), zeros past the request
         {
-            uint32_t qv[HD / 2];
-            const __nv_bfloat16 *qp =
-                query + static_cast<int64_t>(tok) * q_stride + static_cast<int64_t>(g * G + hh) * HD;
+            uint32_t qv[kHalfDims / 2];
+            const __nv_bfloat16 *qp = query + static_cast<int64_t>(tok) * q_stride +
+                                      static_cast<int64_t>(g * G + hh) * HD + half * kHalfDims;
 #pragma unroll
-            for (int c = 0; c < HD / 8; ++c) {
+            for (int c = 0; c < kHalfDims / 8; ++c) {
                 const uint4 w = valid ? __ldg(reinterpret_cast<const uint4 *>(qp) + c) : make_uint4(0, 0, 0, 0);
                 qv[4 * c + 0] = w.x;
                 qv[4 * c + 1] = w.y;
                 qv[4 * c + 2] = w.z;
                 qv[4 * c + 3] = w.w;
             }
-#pragma unroll
-            for (int c = 0; c < HD / 64; ++c) {
-                uint32_t (&part)[32] = *reinterpret_cast<uint32_t(*)[32]>(&qv[c * 32]);
-                tmem_st32(trow + Cfg::kColQ + c * 32, part);
+            if constexpr (kHalfDims / 2 == 32) {
+                tmem_st32(trow + Cfg::kColQ + half * 32, qv);
+            } else {
+                tmem_st16(trow + Cfg::kColQ + half * 16, qv);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -331,61 +426,87 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) mbar_arrive(&bars[kQFull]);
         }
 
-        float m_ref = NEG_INF, l = 0.f;
+        float m_ref = NEG_INF, l = 0.f;                    // l: this half's sum
         for (int j = 0; j < n_kv && ok; ++j) {
             const int sb = j & 1;
             const uint32_t sbuf = trow + (sb ? Cfg::kColS1 : Cfg::kColS0);
             ok = __all_sync(0xffffffffu, pf_wait(&bars[kSFull0 + sb], (j >> 1) & 1, status));
             if (!ok) break;
             tc_fence_after();
-            float x[kPrefillKeys];
+            float x[kHalfKeys];
             {
-                uint32_t v[4][32];
+                uint32_t v[2][32];
 #pragma unroll
-                for (int c = 0; c < kPrefillKeys / 32; ++c) tmem_ld32(sbuf + c * 32, v[c]);
+                for (int c = 0; c < 2; ++c) tmem_ld32(sbuf + half * kHalfKeys + c * 32, v[c]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < kPrefillKeys / 32; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
             }
             // keys a row may not see become -inf; only tiles reaching some
             // row's limit need the test (warp-uniform branch)
-            const int key0 = (t0 + j) * kPrefillKeys;
-            if (__any_sync(0xffffffffu, key0 + kPrefillKeys > lim)) {
+            const int key0 = (t0 + j) * kPrefillKeys + half * kHalfKeys;
+            const bool masked = __any_sync(0xffffffffu, key0 + kHalfKeys > lim);
+            if (masked) {
 #pragma unroll
-                for (int c = 0; c < kPrefillKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
+                for (int c = 0; c < kHalfKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
             }
-            // row max of the raw scores: 8 independent chains
-            float mx8[8];
+            // this half's max (four chains of three-input maxima), then the row's
+            float mx4[4] = {fmaxf(x[0], x[1]), fmaxf(x[2], x[3]), fmaxf(x[4], x[5]), fmaxf(x[6], x[7])};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = x[e];
-#pragma unroll
-            for (int c = 8; c < kPrefillKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            // log2-domain max (scale > 0 keeps the order of scores)
+            for (int c = 8; c < kHalfKeys; c += 8) {
+                mx4[0] = fmax3(mx4[0], x[c], x[c + 1]);
+                mx4[1] = fmax3(mx4[1], x[c + 2], x[c + 3]);
+                mx4[2] = fmax3(mx4[2], x[c + 4], x[c + 5]);
+                mx4[3] = fmax3(mx4[3], x[c + 6], x[c + 7]);
+            }
+            float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            // the other half's max; both halves have read all of S (the barrier
+            // follows both tensor-memory loads), so P may overwrite S afterwards
+            xmax[(sb * 2 + half) * kPrefillRows + row] = mx;
+            ok = exchange(j);
+            if (!ok) break;
+            mx = fmaxf(mx, xmax[(sb * 2 + (half ^ 1)) * kPrefillRows + row]);
+            // log2-domain max (scale > 0 keeps the order of scores); both halves
+            // take the same decisions from the same values
             const float m_new = fmaxf(m_ref, mx * p.scale_log2);
-            // a row moves its reference max only when the max grew by more than
-            // 2^8 (its O is then rescaled by alpha)
             const bool first = m_ref == NEG_INF;           // O holds nothing yet for this row
             const bool grow = !first && m_new > m_ref + 8.f;
             const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
             if (first || grow) m_ref = m_new;
             const float ref = (m_ref == NEG_INF) ? 0.f : m_ref;
-            float ps8[8], pq8[8];
+            // weights p = 2^(x scale - ref) on pairs; in tiles with no masked key
+            // one pair in four takes the FMA-pipe exponential
+            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
+            uint64_t ps2[4] = {0, 0, 0, 0}, pq2[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ps8[e] = pq8[e] = 0.f;
-#pragma unroll
-            for (int c = 0; c < kPrefillKeys; ++c) {
-                x[c] = fast_exp2(fmaf(x[c], p.scale_log2, -ref));
-                ps8[c & 7] += x[c];
-                pq8[c & 7] = fmaf(x[c], x[c], pq8[c & 7]);
+            for (int c = 0; c < kHalfKeys; c += 2) {
+                const uint64_t y2 = f2_fma(f2_pack(x[c], x[c + 1]), sc2, nref2);
+                uint64_t p2;
+                if ((c & 7) == 6 && !masked) {
+                    p2 = f2_exp2_poly(y2);
+                } else {
+                    float y0, y1;
+                    f2_unpack(y2, y0, y1);
+                    p2 = f2_pack(fast_exp2(y0), fast_exp2(y1));
+                }
+                ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], p2);
+                pq2[(c >> 1) & 3] = f2_fma(p2, p2, pq2[(c >> 1) & 3]);
+                f2_unpack(p2, x[c], x[c + 1]);
             }
-            const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-            const float psq = ((pq8[0] + pq8[1]) + (pq8[2] + pq8[3])) + ((pq8[4] + pq8[5]) + (pq8[6] + pq8[7]));
+            float psum, psq;
+            {
+                float a0, a1, b0, b1;
+                f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), a0, a1);
+                f2_unpack(f2_add(f2_add(pq2[0], pq2[1]), f2_add(pq2[2], pq2[3])), b0, b1);
+                psum = a0 + a1;
+                psq = b0 + b1;
+            }
             l = l * alpha + psum;
             // this warp's vote: does any of its rows need the remainder of P?
+            // (half sums: if neither half's weights are concentrated, the row's
+            // are not either)
             const bool need = j < p.lo_tiles || psq > kLoConcentration * l * l;
             const bool wneed = __any_sync(0xffffffffu, need);
             // P V of tile j-1 must be done before O is rescaled; the barrier of
@@ -395,38 +516,33 @@ __global__ void __launch_bounds__(256, 1)
                 ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + sb], ((j - 2) >> 1) & 1, status));
                 if (!ok) break;
             }
-            if (__any_sync(0xffffffffu, grow)) {              // rare: O rescale, one chunk at a time
+            if (__any_sync(0xffffffffu, grow)) {              // rare: this half of O rescaled
                 if (j >= 1) {
                     ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + (sb ^ 1)], ((j - 1) >> 1) & 1, status));
                     if (!ok) break;
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < HD / 32; ++c) {
+                for (int c = 0; c < kHalfDims / 32; ++c) {
                     uint32_t v[32];
-                    tmem_ld32(trow + Cfg::kColO + c * 32, v);
+                    tmem_ld32(trow + Cfg::kColO + half * kHalfDims + c * 32, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(trow + Cfg::kColO + c * 32, v);
+                    tmem_st32(trow + Cfg::kColO + half * kHalfDims + c * 32, v);
                 }
             }
-            // P (bf16 pairs) into this tile's S buffer; the remainder too when
-            // this warp asks for it, zeros otherwise (another warp may)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            // P (bf16 pairs) of this half's keys into the tile's S buffer; the
+            // remainder too when this warp asks for it, zeros otherwise
+            {
                 uint32_t w[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1]);
-                tmem_st32(sbuf + c * 32, w);
-            }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t w[32];
+                for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                tmem_st32(sbuf + half * 32, w);
                 if (wneed) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float a0 = x[c * 64 + 2 * e], a1 = x[c * 64 + 2 * e + 1];
+                        const float a0 = x[2 * e], a1 = x[2 * e + 1];
                         const float2 hb = __bfloat1622float2(__floats2bfloat162_rn(a0, a1));
                         w[e] = pack_bf16x2(a0 - hb.x, a1 - hb.y);
                     }
@@ -434,10 +550,10 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) w[e] = 0u;
                 }
-                tmem_st32(sbuf + Cfg::kPLo + c * 32, w);
+                tmem_st32(sbuf + Cfg::kPLo + half * 32, w);
             }
             tmem_st_wait();
-            if (lane == 0) votes[(j & 1) * 4 + (warp - 4)] = wneed ? 1u : 0u;
+            if (lane == 0) votes[(j & 1) * 8 + (warp - 4)] = wneed ? 1u : 0u;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kPFull0 + (j & 1)]);
@@ -449,12 +565,18 @@ __global__ void __launch_bounds__(256, 1)
             if (ok) ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + ((n_kv - 1) & 1)], ((n_kv - 1) >> 1) & 1,
                                                          status));
         }
+        // the row's sum: this half's plus the other's
+        if (ok) {
+            xsum[half * kPrefillRows + row] = l;
+            ok = exchange(n_kv);
+            l += xsum[(half ^ 1) * kPrefillRows + row];
+        }
         if (ok) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint32_t v[HD / 32][32];
+            uint32_t v[kHalfDims / 32][32];
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) tmem_ld32(trow + Cfg::kColO + c * 32, v[c]);
+            for (int c = 0; c < kHalfDims / 32; ++c) tmem_ld32(trow + Cfg::kColO + half * kHalfDims + c * 32, v[c]);
             tmem_ld_wait();
             if constexpr (CASCADE) {
                 if (valid) {
@@ -462,21 +584,23 @@ __global__ void __launch_bounds__(256, 1)
                     const int4 ri = reinterpret_cast<const int4 *>(p.ws + hdr->off_req)[crow.y];
                     const int64_t prow =
                         ri.y + (static_cast<int64_t>(crow.z) * p.num_q_heads + g * G + hh) * ri.x + part;
-                    float *po = reinterpret_cast<float *>(p.ws + hdr->off_part_o) + prow * HD;
+                    float *po = reinterpret_cast<float *>(p.ws + hdr->off_part_o) + prow * HD + half * kHalfDims;
 #pragma unroll
-                    for (int c = 0; c < HD / 32; ++c)
+                    for (int c = 0; c < kHalfDims / 32; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
                             *reinterpret_cast<float4 *>(po + c * 32 + e) =
                                 make_float4(__uint_as_float(v[c][e]) * inv, __uint_as_float(v[c][e + 1]) * inv,
                                             __uint_as_float(v[c][e + 2]) * inv, __uint_as_float(v[c][e + 3]) * inv);
-                    reinterpret_cast<float *>(p.ws + hdr->off_part_lse)[prow] =
-                        l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+                    if (half == 0)
+                        reinterpret_cast<float *>(p.ws + hdr->off_part_lse)[prow] =
+                            l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
                 }
             } else if (valid) {
-                __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(tok) * p.num_q_heads + g * G + hh) * HD;
+                __nv_bfloat16 *dst =
+                    p.out + (static_cast<int64_t>(tok) * p.num_q_heads + g * G + hh) * HD + half * kHalfDims;
 #pragma unroll
-                for (int c = 0; c < HD / 32; ++c)
+                for (int c = 0; c < kHalfDims / 32; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 w;
@@ -535,7 +659,7 @@ static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, con
             done_mask |= bit;
         }
     }
-    if (launch_pdl(prefill_kernel<HD, CASCADE>, dim3(static_cast<unsigned>(grid)), dim3(256), Cfg::kSmem, stream,
+    if (launch_pdl(prefill_kernel<HD, CASCADE>, dim3(static_cast<unsigned>(grid)), dim3(384), Cfg::kSmem, stream,
                    kvm, static_cast<const __nv_bfloat16 *>(query), q_stride, p) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
