@@ -99,36 +99,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// 2^y for a pair, on the FMA pipe (the special-function unit runs one
-// exponential per lane every few cycles; part of a tile's exponentials go
-// here instead).  y is held at >= -125 (weights below 2^-125 of the row's
-// reference are negligible); y = n + f with n the nearest integer (found by
-// adding 1.5 * 2^23, whose low bits then hold n) and f in [-1/2, 1/2]; 2^f is
-// a degree-5 polynomial fitted here by least squares on Chebyshev nodes with
-// relative weights (relative error 2.3e-7 in fp32); 2^n enters as n added to
-// the exponent field.
-__device__ __forceinline__ uint64_t f2_exp2_poly(uint64_t y2) {
-    constexpr float kMagic = 12582912.0f;            // 1.5 * 2^23
-    float y0, y1;
-    f2_unpack(y2, y0, y1);
-    y0 = fmaxf(y0, -125.f);
-    y1 = fmaxf(y1, -125.f);
-    const uint64_t y = f2_pack(y0, y1);
-    const uint64_t ym = f2_add(y, f2_pack(kMagic, kMagic));            // n in the low mantissa bits
-    const uint64_t n = f2_add(ym, f2_pack(-kMagic, -kMagic));
-    const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), y);
-    uint64_t q = f2_fma(f, f2_pack(1.326744794e-3f, 1.326744794e-3f), f2_pack(9.675463662e-3f, 9.675463662e-3f));
-    q = f2_fma(q, f, f2_pack(5.550741032e-2f, 5.550741032e-2f));
-    q = f2_fma(q, f, f2_pack(2.402212173e-1f, 2.402212173e-1f));
-    q = f2_fma(q, f, f2_pack(6.931469440e-1f, 6.931469440e-1f));
-    q = f2_fma(q, f, f2_pack(1.000000119f, 1.000000119f));
-    float q0, q1, m0, m1;
-    f2_unpack(q, q0, q1);
-    f2_unpack(ym, m0, m1);
-    return f2_pack(__int_as_float(__float_as_int(q0) + (__float_as_int(m0) << 23)),
-                   __int_as_float(__float_as_int(q1) + (__float_as_int(m1) << 23)));
-}
-
 // Bounded wait shared by every role; on timeout records the error and
 // reports it so the role can stop.
 __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
@@ -290,37 +260,27 @@ __global__ void __launch_bounds__(384, 1)
             constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillRows, HD, 0, 1);
             bool ok = pf_wait(&bars[kQFull], 0, status);
             // S(j) = Q K^T into S buffer j & 1; A = Q in tensor memory
-            // descriptors are built once per stage; a K step advances the
-            // start-address field (16-byte units, never carrying past its 14
-            // bits: shared-memory addresses are below 2^18)
-            uint64_t dk[S], dv[S];
-#pragma unroll
-            for (int st = 0; st < S; ++st) {
-                dk[st] = smem_desc_sw128(sK + st * Cfg::kKVBytes, 16, 1024);
-                dv[st] = smem_desc_sw128(sV + st * Cfg::kKVBytes, kPrefillKeys * 128, 1024);
-            }
             auto issue_s = [&](int j) {
                 const int st = j % S;
                 const uint32_t d = tmem + ((j & 1) ? Cfg::kColS1 : Cfg::kColS0);
-                const uint64_t b0 = dk[st];
-                umma_bf16_ts_c<false>(d, tmem + Cfg::kColQ, b0, kIdescS);
 #pragma unroll
-                for (int kk = 1; kk < HD / 16; ++kk)
-                    umma_bf16_ts_c<true>(d, tmem + Cfg::kColQ + kk * 8, b0 + (((kk >> 2) * (kPrefillKeys * 128) +
-                                                                              (kk & 3) * 32) >> 4),
-                                         kIdescS);
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint64_t b = smem_desc_sw128(sK + st * Cfg::kKVBytes + (kk >> 2) * (kPrefillKeys * 128) +
+                                                           (kk & 3) * 32,
+                                                       16, 1024);
+                    umma_bf16_ts(d, tmem + Cfg::kColQ + kk * 8, b, kIdescS, kk > 0);
+                }
                 umma_commit(&bars[kSFull0 + (j & 1)]);
                 umma_commit(&bars[kKEmpty0 + st]);
             };
             // O (+)= P V; A = P (or its remainder) in S buffer j & 1
-            auto issue_pv = [&](int j, uint32_t pcol, bool accumulate) {
+            auto issue_pv = [&](int j, uint32_t pcol, uint32_t accumulate) {
                 const int st = j % S;
-                const uint64_t b0 = dv[st];
-                if (accumulate) umma_bf16_ts_c<true>(tmem + Cfg::kColO, pcol, b0, kIdescO);
-                else umma_bf16_ts_c<false>(tmem + Cfg::kColO, pcol, b0, kIdescO);
 #pragma unroll
-                for (int kk = 1; kk < kPrefillKeys / 16; ++kk)
-                    umma_bf16_ts_c<true>(tmem + Cfg::kColO, pcol + kk * 8, b0 + ((kk * 2048) >> 4), kIdescO);
+                for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
+                    const uint64_t b = smem_desc_sw128(sV + st * Cfg::kKVBytes + kk * 2048, kPrefillKeys * 128, 1024);
+                    umma_bf16_ts(tmem + Cfg::kColO, pcol + kk * 8, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+                }
             };
             for (int j0 = 0; j0 < 2 && j0 < n_kv && ok; ++j0) {
                 ok = pf_wait(&bars[kKFull0 + j0], 0, status);
@@ -341,7 +301,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int w = 0; w < 8; ++w) vote |= votes[(j & 1) * 8 + w];
                 const bool lo = vote != 0u;
                 issue_pv(j, pbuf, j > 0);
-                if (lo) issue_pv(j, pbuf + Cfg::kPLo, true);
+                if (lo) issue_pv(j, pbuf + Cfg::kPLo, 1);
                 umma_commit(&bars[kODone0 + (j & 1)]);
                 umma_commit(&bars[kVEmpty0 + st]);
                 // S of tile j+2 overwrites S buffer j & 1, where P V of tile j reads
@@ -447,8 +407,7 @@ __global__ void __launch_bounds__(384, 1)
             // keys a row may not see become -inf; only tiles reaching some
             // row's limit need the test (warp-uniform branch)
             const int key0 = (t0 + j) * kPrefillKeys + half * kHalfKeys;
-            const bool masked = __any_sync(0xffffffffu, key0 + kHalfKeys > lim);
-            if (masked) {
+            if (__any_sync(0xffffffffu, key0 + kHalfKeys > lim)) {
 #pragma unroll
                 for (int c = 0; c < kHalfKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
             }
@@ -476,21 +435,16 @@ __global__ void __launch_bounds__(384, 1)
             const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
             if (first || grow) m_ref = m_new;
             const float ref = (m_ref == NEG_INF) ? 0.f : m_ref;
-            // weights p = 2^(x scale - ref) on pairs; in tiles with no masked key
-            // one pair in four takes the FMA-pipe exponential
+            // weights p = 2^(x scale - ref) on pairs (the special-function unit
+            // has room for every exponential of the tile)
             const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
             uint64_t ps2[4] = {0, 0, 0, 0}, pq2[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int c = 0; c < kHalfKeys; c += 2) {
                 const uint64_t y2 = f2_fma(f2_pack(x[c], x[c + 1]), sc2, nref2);
-                uint64_t p2;
-                if ((c & 7) == 6 && !masked) {
-                    p2 = f2_exp2_poly(y2);
-                } else {
-                    float y0, y1;
-                    f2_unpack(y2, y0, y1);
-                    p2 = f2_pack(fast_exp2(y0), fast_exp2(y1));
-                }
+                float y0, y1;
+                f2_unpack(y2, y0, y1);
+                const uint64_t p2 = f2_pack(fast_exp2(y0), fast_exp2(y1));
                 ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], p2);
                 pq2[(c >> 1) & 3] = f2_fma(p2, p2, pq2[(c >> 1) & 3]);
                 f2_unpack(p2, x[c], x[c + 1]);

@@ -121,42 +121,6 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
-// The same two MMAs with the accumulate flag fixed at compile time (no
-// predicate computed per instruction), for lean issue loops.
-template <bool ACC>
-__device__ __forceinline__ void umma_bf16_ss_c(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
-    if constexpr (ACC) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, 1, 1;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc)
-            : "memory");
-    }
-}
-
-template <bool ACC>
-__device__ __forceinline__ void umma_bf16_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc) {
-    if constexpr (ACC) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "r"(a_tmem), "l"(bdesc), "r"(idesc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, 1, 1;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-            "r"(a_tmem), "l"(bdesc), "r"(idesc)
-            : "memory");
-    }
-}
-
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
