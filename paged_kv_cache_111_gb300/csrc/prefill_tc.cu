@@ -55,7 +55,6 @@ struct PrefillCfg {
     // bf16 remainder), O, and Q as the A operand of S = Q K^T
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColQ = 384;
-    static constexpr uint32_t kPLo = 64;                     // remainder's columns within an S buffer
 };
 
 enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kKFull2, kVFull0, kVFull1, kVFull2, kKEmpty0, kKEmpty1, kKEmpty2,
@@ -273,13 +272,16 @@ __global__ void __launch_bounds__(384, 1)
                 umma_commit(&bars[kSFull0 + (j & 1)]);
                 umma_commit(&bars[kKEmpty0 + st]);
             };
-            // O (+)= P V; A = P (or its remainder) in S buffer j & 1
+            // O (+)= P V; A = P (or its remainder) in S buffer j & 1: keys
+            // 64 h .. 64 h + 63 sit at columns 64 h + [0, 32) (P) and
+            // 64 h + [32, 64) (remainder), each half within its own S columns
             auto issue_pv = [&](int j, uint32_t pcol, uint32_t accumulate) {
                 const int st = j % S;
 #pragma unroll
                 for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
                     const uint64_t b = smem_desc_sw128(sV + st * Cfg::kKVBytes + kk * 2048, kPrefillKeys * 128, 1024);
-                    umma_bf16_ts(tmem + Cfg::kColO, pcol + kk * 8, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tmem + Cfg::kColO, pcol + kk * 8 + (kk >> 2) * 32, b, kIdescO,
+                                 (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
             for (int j0 = 0; j0 < 2 && j0 < n_kv && ok; ++j0) {
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int w = 0; w < 8; ++w) vote |= votes[(j & 1) * 8 + w];
                 const bool lo = vote != 0u;
                 issue_pv(j, pbuf, j > 0);
-                if (lo) issue_pv(j, pbuf + Cfg::kPLo, 1);
+                if (lo) issue_pv(j, pbuf + 32, 1);
                 umma_commit(&bars[kODone0 + (j & 1)]);
                 umma_commit(&bars[kVEmpty0 + st]);
                 // S of tile j+2 overwrites S buffer j & 1, where P V of tile j reads
@@ -352,13 +354,14 @@ __global__ void __launch_bounds__(384, 1)
         // the two warps of this quadrant meet on an mbarrier, one phase per
         // tile plus one for the final sums (bounded waits, like every other)
         uint64_t *xbar = &bars[kXchg0 + quad];
-        auto exchange = [&](int phase) -> bool {
-            tc_fence_before();
+        auto post = [&]() {
             __syncwarp();
             if (lane == 0) mbar_arrive(xbar);
-            const bool done = __all_sync(0xffffffffu, pf_wait(xbar, phase & 1, status));
-            tc_fence_after();
-            return done;
+        };
+        auto meet = [&](int phase) -> bool { return __all_sync(0xffffffffu, pf_wait(xbar, phase & 1, status)); };
+        auto exchange = [&](int phase) -> bool {
+            post();
+            return meet(phase);
         };
         bool ok = true;
 
@@ -393,8 +396,11 @@ __global__ void __launch_bounds__(384, 1)
             ok = __all_sync(0xffffffffu, pf_wait(&bars[kSFull0 + sb], (j >> 1) & 1, status));
             if (!ok) break;
             tc_fence_after();
+            // this half's scores (keys key0 .. key0 + 63); keys a row may not see
+            // become -inf, tested only in tiles reaching some row's limit
+            const int key0 = (t0 + j) * kPrefillKeys + half * kHalfKeys;
             float x[kHalfKeys];
-            {
+            auto load_scores = [&]() {
                 uint32_t v[2][32];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) tmem_ld32(sbuf + half * kHalfKeys + c * 32, v[c]);
@@ -403,15 +409,36 @@ __global__ void __launch_bounds__(384, 1)
                 for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
-            }
-            // keys a row may not see become -inf; only tiles reaching some
-            // row's limit need the test (warp-uniform branch)
-            const int key0 = (t0 + j) * kPrefillKeys + half * kHalfKeys;
-            if (__any_sync(0xffffffffu, key0 + kHalfKeys > lim)) {
+                if (__any_sync(0xffffffffu, key0 + kHalfKeys > lim)) {
 #pragma unroll
-                for (int c = 0; c < kHalfKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
-            }
-            // this half's max (four chains of three-input maxima), then the row's
+                    for (int c = 0; c < kHalfKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
+                }
+            };
+            // weights p = 2^(x scale - ref) on pairs in place, with their sum
+            // and sum of squares (the special-function unit has room for every
+            // exponential of the tile)
+            float psum = 0.f, psq = 0.f;
+            auto weights = [&](float ref) {
+                const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
+                uint64_t ps2[4] = {0, 0, 0, 0}, pq2[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int c = 0; c < kHalfKeys; c += 2) {
+                    const uint64_t y2 = f2_fma(f2_pack(x[c], x[c + 1]), sc2, nref2);
+                    float y0, y1;
+                    f2_unpack(y2, y0, y1);
+                    const uint64_t p2 = f2_pack(fast_exp2(y0), fast_exp2(y1));
+                    ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], p2);
+                    pq2[(c >> 1) & 3] = f2_fma(p2, p2, pq2[(c >> 1) & 3]);
+                    f2_unpack(p2, x[c], x[c + 1]);
+                }
+                float a0, a1, b0, b1;
+                f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), a0, a1);
+                f2_unpack(f2_add(f2_add(pq2[0], pq2[1]), f2_add(pq2[2], pq2[3])), b0, b1);
+                psum = a0 + a1;
+                psq = b0 + b1;
+            };
+            load_scores();
+            // this half's max (four chains of three-input maxima)
             float mx4[4] = {fmaxf(x[0], x[1]), fmaxf(x[2], x[3]), fmaxf(x[4], x[5]), fmaxf(x[6], x[7])};
 #pragma unroll
             for (int c = 8; c < kHalfKeys; c += 8) {
@@ -421,41 +448,33 @@ __global__ void __launch_bounds__(384, 1)
                 mx4[3] = fmax3(mx4[3], x[c + 6], x[c + 7]);
             }
             float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            // the other half's max; both halves have read all of S (the barrier
-            // follows both tensor-memory loads), so P may overwrite S afterwards
+            // post this half's max; while the other half's arrives, the weights
+            // are computed against the current reference when it holds for
+            // every row of this warp (the usual case after the first tile).
+            // Rows past the request never see a key and keep a -inf reference;
+            // a half that sees no key of a row has zero weights whatever the
+            // reference becomes.  Every lane takes part in the vote.
             xmax[(sb * 2 + half) * kPrefillRows + row] = mx;
-            ok = exchange(j);
+            post();
+            const bool first = m_ref == NEG_INF;           // O holds nothing yet for this row
+            const bool ready = first ? mx == NEG_INF : mx * p.scale_log2 <= m_ref + 8.f;
+            const bool early = __all_sync(0xffffffffu, ready);
+            if (early) weights(first ? 0.f : m_ref);
+            ok = meet(j);
             if (!ok) break;
             mx = fmaxf(mx, xmax[(sb * 2 + (half ^ 1)) * kPrefillRows + row]);
             // log2-domain max (scale > 0 keeps the order of scores); both halves
             // take the same decisions from the same values
             const float m_new = fmaxf(m_ref, mx * p.scale_log2);
-            const bool first = m_ref == NEG_INF;           // O holds nothing yet for this row
             const bool grow = !first && m_new > m_ref + 8.f;
             const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
             if (first || grow) m_ref = m_new;
-            const float ref = (m_ref == NEG_INF) ? 0.f : m_ref;
-            // weights p = 2^(x scale - ref) on pairs (the special-function unit
-            // has room for every exponential of the tile)
-            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
-            uint64_t ps2[4] = {0, 0, 0, 0}, pq2[4] = {0, 0, 0, 0};
-#pragma unroll
-            for (int c = 0; c < kHalfKeys; c += 2) {
-                const uint64_t y2 = f2_fma(f2_pack(x[c], x[c + 1]), sc2, nref2);
-                float y0, y1;
-                f2_unpack(y2, y0, y1);
-                const uint64_t p2 = f2_pack(fast_exp2(y0), fast_exp2(y1));
-                ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], p2);
-                pq2[(c >> 1) & 3] = f2_fma(p2, p2, pq2[(c >> 1) & 3]);
-                f2_unpack(p2, x[c], x[c + 1]);
-            }
-            float psum, psq;
-            {
-                float a0, a1, b0, b1;
-                f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), a0, a1);
-                f2_unpack(f2_add(f2_add(pq2[0], pq2[1]), f2_add(pq2[2], pq2[3])), b0, b1);
-                psum = a0 + a1;
-                psq = b0 + b1;
+            if (!early || __any_sync(0xffffffffu, grow)) {
+                // the reference moved for some row of this warp: weights again
+                // from this half's own S columns (no other warp writes them)
+                tc_fence_after();
+                load_scores();
+                weights((m_ref == NEG_INF) ? 0.f : m_ref);
             }
             l = l * alpha + psum;
             // this warp's vote: does any of its rows need the remainder of P?
@@ -492,7 +511,7 @@ __global__ void __launch_bounds__(384, 1)
                 uint32_t w[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-                tmem_st32(sbuf + half * 32, w);
+                tmem_st32(sbuf + half * 64, w);
                 if (wneed) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
@@ -504,7 +523,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) w[e] = 0u;
                 }
-                tmem_st32(sbuf + Cfg::kPLo + half * 32, w);
+                tmem_st32(sbuf + half * 64 + 32, w);
             }
             tmem_st_wait();
             if (lane == 0) votes[(j & 1) * 8 + (warp - 4)] = wneed ? 1u : 0u;
