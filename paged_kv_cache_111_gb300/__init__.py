@@ -36,7 +36,7 @@ __all__ = [
     "BLOCK_SIZE", "PagedKVError", "load", "kv_write", "paged_attn", "paged_attn_combine",
     "paged_attn_workspace_size", "workspace_status", "STATUS_NAMES", "library_path", "copy_blocks",
     "paged_attn_noalloc", "paged_attn_shared_prefix", "paged_attn_shared_prefix_workspace_size",
-    "kv_write_fp8", "paged_attn_fp8",
+    "kv_write_fp8", "paged_attn_fp8", "workspace_schedule",
 ]
 
 BLOCK_SIZE = 16
@@ -269,6 +269,24 @@ def paged_attn_combine(out: torch.Tensor, workspace: torch.Tensor, stream=None) 
 def workspace_status(workspace: torch.Tensor) -> int:
     """The device status word (first int32 of the workspace); synchronises on its read."""
     return int(workspace[:4].view(torch.int32)[0].item())
+
+
+# per-CTA record of the persistent prefill kernels' dynamic schedule: int32
+# [2][1024] right after the workspace's 256-byte header
+_SCHEDULE_OFFSET, _SCHEDULE_CTAS = 256, 1024
+
+
+def workspace_schedule(workspace: torch.Tensor):
+    """Work items each CTA of the tensor-core prefill kernel (first list) and of
+    the shared-prefix pass (second list) took in the last attention call on
+    this workspace, trailing idle CTAs dropped; synchronises on its read."""
+    a = workspace[_SCHEDULE_OFFSET:_SCHEDULE_OFFSET + 8 * _SCHEDULE_CTAS].view(torch.int32).cpu().tolist()
+
+    def trim(v):
+        while v and v[-1] == 0:
+            v.pop()
+        return v
+    return trim(a[:_SCHEDULE_CTAS]), trim(a[_SCHEDULE_CTAS:])
 
 
 def paged_attn_noalloc(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Tensor, block_tables: torch.Tensor,

@@ -25,7 +25,8 @@ struct WsHeader {
     int32_t n_crows;         // rows of the shared-prefix (cascade) pass, per kv head
     int32_t prefix_blocks;   // shared prefix in blocks (0: no cascade)
     int32_t prefix_parts;    // the prefix keys are cut into this many splits (KV-tile ranges)
-    int32_t pad_[2];
+    int32_t next_ptile_item;    // prefill kernel: next work item to claim, less its grid size
+    int32_t next_prefix_item;   // shared-prefix pass: the same
     int64_t off_req;         // int4 [num_seqs]: {splits (0: refused), partial row base, first chunk, chunks}
     int64_t off_tok;         // int2 [num_tokens]: {request, index in request} (-1 if none)
     int64_t off_chunks;      // int4 [max_chunks]: {request, split or tile, page begin, page end}
@@ -40,6 +41,12 @@ struct WsHeader {
     int64_t prow_used;
 };
 static_assert(sizeof(WsHeader) <= 256, "header must fit its 256-byte slot");
+
+// After the header: int32 [2][kStatsCtas], the work items each CTA of the
+// persistent prefill kernel (row 0) and of the shared-prefix pass (row 1)
+// took, zeroed by the plan (a record of the dynamic schedule).
+constexpr int64_t kStatsOffset = 256;
+constexpr int kStatsCtas = 1024;
 
 struct WsLayout {
     int64_t off_req, off_tok, off_chunks, off_ptiles, off_crows, off_part_lse, off_part_o, total;

@@ -77,7 +77,7 @@ static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_quer
     w.max_chunks = num_seqs * splits + (num_tokens * G + 15) / 16 + num_seqs;
     // prefill tiles: ceil(q_r G / 128) <= q_r G / 128 + 1
     w.max_ptiles = (num_tokens * G + kPrefillRows - 1) / kPrefillRows + num_seqs;
-    int64_t off = 256;
+    int64_t off = kStatsOffset + 2 * kStatsCtas * 4;
     w.off_req = off;
     off = align256(off + 16 * num_seqs);
     w.off_tok = off;
@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __shared__ int2 ctotals;
     pdl_wait();       // the previous kernel on the stream may still read this workspace
     pdl_trigger();
+    for (int i = tid; i < 2 * kStatsCtas; i += nthr) reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[i] = 0;
 
     for (int i = tid; i < kSizeBins; i += nthr) {
         bin_count[i] = 0;
@@ -510,6 +511,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         hdr->n_crows = fits ? ctotals.x : 0;
         hdr->prefix_blocks = p.prefix_blocks;
         hdr->prefix_parts = p.lay.prefix_parts;
+        hdr->next_ptile_item = 0;
+        hdr->next_prefix_item = 0;
         hdr->max_chunks = p.lay.max_chunks;
         hdr->max_ptiles = p.lay.max_ptiles;
         hdr->max_crows = p.lay.max_crows;
@@ -1247,14 +1250,16 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     fp.lo_tiles = 0;
     fp.ws = ap.ws;
     if (prefix_blocks > 0) {
+        // persistent kernels: one CTA per SM at most
         rc = launch_prefix(fp, query, query_token_stride, kv_cache, num_blocks, head_size,
-                           (lay.max_crows + kPrefillRows - 1) / kPrefillRows * num_kv_heads * lay.prefix_parts,
+                           std::min<int64_t>(std::min(sms, kStatsCtas), (lay.max_crows + kPrefillRows - 1) / kPrefillRows * num_kv_heads *
+                                                      lay.prefix_parts),
                            dev, st);
         if (rc) return rc;
     }
     if (!may_prefill) return PKV_OK;
     return launch_prefill(fp, query, query_token_stride, num_tokens, kv_cache, num_blocks, head_size,
-                          lay.max_ptiles * num_kv_heads, dev, st);
+                          std::min<int64_t>(std::min(sms, kStatsCtas), lay.max_ptiles * num_kv_heads), dev, st);
 }
 
 }  // namespace pkv

@@ -8,7 +8,8 @@
 // managing the KV cache like an OS manages memory", section 3.2) attends
 // causally, query i of the chunk seeing keys 0 .. context + i.
 //
-// One CTA computes one 128-row tile for one kv head.  Rows are
+// Work item: one 128-row tile for one kv head; a persistent CTA per SM
+// takes items largest first from a shared counter.  Rows are
 // (query token, q head of the GQA group) pairs, so one K/V tile in shared
 // memory serves every q head of the group.  Per 128-key KV tile:
 //   S = Q K^T      tcgen05.mma, A = Q from tensor memory, B = K from shared
@@ -50,7 +51,8 @@ struct PrefillCfg {
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffBar = kOffV + kStages * kKVBytes;
     static constexpr int kOffXchg = kOffBar + 512;            // softmax halves' maxima and sums (3 KiB)
-    static constexpr int kSmem = kOffXchg + 3072 + 1024;    // + alignment slack
+    static constexpr int kOffItems = kOffXchg + 3072;         // ring of work items (256 bytes)
+    static constexpr int kSmem = kOffItems + 256 + 1024;      // + alignment slack
     // tensor memory: two S buffers (each later holding that tile's P and its
     // bf16 remainder), O, and Q as the A operand of S = Q K^T
     static constexpr uint32_t kTmemCols = 512;
@@ -58,8 +60,12 @@ struct PrefillCfg {
 };
 
 enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kKFull2, kVFull0, kVFull1, kVFull2, kKEmpty0, kKEmpty1, kKEmpty2,
-                  kVEmpty0, kVEmpty1, kVEmpty2, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kVFix,
+                  kVEmpty0, kVEmpty1, kVEmpty2, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1,
+                  kVFix0, kVFix1, kVFix2,              // V rows past the sequence end zeroed, per stage
                   kXchg0, kXchg1, kXchg2, kXchg3,      // the two softmax warps of a lane quadrant
+                  kItemFull0, kItemFull1, kItemFull2, kItemFull3,      // work-item ring
+                  kItemEmpty0, kItemEmpty1, kItemEmpty2, kItemEmpty3,
+                  kOFree,                              // O read out by the epilogue
                   kNumBars };
 static_assert(kNumBars * 8 + 16 + 64 <= 512, "barriers, the TMEM address slot and the votes fit their 512 bytes");
 // P of tile j is announced on kPFull0 + (j & 1): with one barrier per parity a
@@ -106,13 +112,35 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t 
     return false;
 }
 
-// CASCADE = false: one 128-row tile of one long request (a prefill chunk),
-// causal, written to `out`.  CASCADE = true: 128 rows taken from every
-// request that shares the first prefix_blocks blocks of its table with
-// request 0, against one range of those blocks' KV tiles (every key of the
-// prefix is visible to every such row); the result for range i is split i of
-// each row (normalised partial output and its log-sum-exp), merged with the
-// row's other splits by the combine.
+// One work item: one 128-row tile for one kv head.  CASCADE = false: rows of
+// one long request (a prefill chunk), causal, written to `out`.
+// CASCADE = true: 128 rows taken from every request that shares the first
+// prefix_blocks blocks of its table with request 0, against one range of
+// those blocks' KV tiles (every key of the prefix is visible to every such
+// row); the result for range i is split i of each row (normalised partial
+// output and its log-sum-exp), merged with the row's other splits by the
+// combine.
+struct PfItem {
+    int32_t valid;        // 0: no further item for this CTA
+    int32_t r;            // request whose block table is read
+    int32_t n_kv;         // KV tiles of the item
+    int32_t L;            // keys of the request (cascade: of the prefix)
+    int32_t qs, ctx;      // first query token, keys before the chunk
+    int32_t rows_total;   // rows of the request (cascade: of the pass)
+    int32_t row0;         // first row of the tile
+    int32_t n_pages;      // pages of the key range's sequence
+    int32_t part, t0;     // cascade split and its first KV tile (0 otherwise)
+    int32_t g;            // kv head
+};
+constexpr int kItemSlots = 4;
+static_assert(kItemSlots * sizeof(PfItem) <= 256, "item ring fits its 256 bytes");
+
+// Persistent: one CTA per SM.  The CTA's first item is its index; each later
+// one is claimed from a counter the plan zeroes, in the plan's order
+// (largest first).  The producer warp claims and decodes items and publishes
+// them through a ring in shared memory; tiles and their barriers are counted
+// across items, so the loads, the first products and the Q of the next item
+// overlap the epilogue of the current one.
 template <int HD, bool CASCADE>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16 *__restrict__ query,
@@ -124,6 +152,7 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
     volatile uint32_t *votes = tmem_slot + 4;          // [2 tiles in flight][8 softmax warps]
+    volatile PfItem *items = reinterpret_cast<volatile PfItem *>(smem + Cfg::kOffItems);
     const uint32_t sK = smem_u32(smem + Cfg::kOffK);
     const uint32_t sV = smem_u32(smem + Cfg::kOffV);
 
@@ -134,41 +163,18 @@ __global__ void __launch_bounds__(384, 1)
     const int n_parts = CASCADE ? hdr->prefix_parts : 1;
     const int n_tiles = CASCADE ? (hdr->n_crows + kPrefillRows - 1) / kPrefillRows : hdr->n_ptiles;
     const int n_items = n_tiles * p.num_kv_heads * n_parts;
-    const int item = blockIdx.x;
-    if (item >= n_items) return;                       // uniform over the CTA
-    const int g = item % p.num_kv_heads;
+    if (static_cast<int>(blockIdx.x) >= n_items) return;   // uniform over the CTA
     const int G = p.G;
-    // t0: first KV tile of this CTA's key range (cascade part; 0 otherwise)
-    int r, n_kv, L, qs, ctx, rows_total, row0, n_pages, part = 0, t0 = 0;
-    if constexpr (CASCADE) {
-        r = 0;                                         // the prefix blocks are read through request 0's table
-        L = hdr->prefix_blocks * kBlock;               // every row sees keys 0 .. L-1
-        const int kv_all = (L + kPrefillKeys - 1) / kPrefillKeys;
-        const int per = (kv_all + n_parts - 1) / n_parts;   // the plan makes every range non-empty
-        part = (item / p.num_kv_heads) % n_parts;
-        t0 = part * per;
-        n_kv = min(kv_all, t0 + per) - t0;
-        n_pages = hdr->prefix_blocks;
-        qs = ctx = 0;
-        rows_total = hdr->n_crows;
-        row0 = (item / (p.num_kv_heads * n_parts)) * kPrefillRows;
-    } else {
-        const int4 tile = reinterpret_cast<const int4 *>(p.ws + hdr->off_ptiles)[item / p.num_kv_heads];
-        r = tile.x;
-        n_kv = tile.z;
-        L = p.seq_lens[r];
-        qs = p.qsl[r];
-        const int qlen = p.qsl[r + 1] - qs;
-        ctx = L - qlen;
-        rows_total = qlen * G;
-        row0 = tile.y * kPrefillRows;                  // first request row of the tile
-        n_pages = (L + kBlock - 1) / kBlock;
-    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < kNumBars; ++b)
-            mbar_init(&bars[b], (b == kPFull0 || b == kPFull1 || b == kQFull) ? 8 : (b >= kXchg0 ? 2 : 1));
+        for (int b = 0; b < kNumBars; ++b) {
+            int count = 1;
+            if (b == kPFull0 || b == kPFull1 || b == kQFull || b == kOFree) count = 8;
+            else if (b >= kXchg0 && b <= kXchg3) count = 2;
+            else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = 9;
+            mbar_init(&bars[b], count);
+        }
         tma_prefetch_desc(&kv_map);
     }
     if (warp == 2) {
@@ -181,87 +187,147 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // the KV tile holding the sequence's last key, when that page is partial
-    const int end_tile = (!CASCADE && (L % kBlock)) ? (L - 1) / kPrefillKeys : -1;
+    // the item's KV tile holding the sequence's last key, when that page is partial
+    auto end_tile_of = [](int L) { return (!CASCADE && (L % kBlock)) ? (L - 1) / kPrefillKeys : -1; };
 
     if (warp == 0) {
-        // ---------------- producer: K and V pages through the block table ----------------
+        // ---------------- producer: items, then K and V pages through the block table ----------------
         bool ok = true;
-        const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks_per_seq;
-        // block ids in windows of 32 pages (4 KV tiles), one lane per page; the
-        // next window is loaded a window ahead.  Pages past the sequence are -1
-        // and load as zeros (outside the tensor map).
-        constexpr int kPagesPerTile = kPrefillKeys / kBlock;
-        auto load_window = [&](int w) -> int {
-            const int page = t0 * kPagesPerTile + w * 32 + lane;
-            const int b = page < n_pages ? __ldg(bt + page) : -1;
-            if (page < n_pages && (b < 0 || b >= p.num_blocks))
-                set_status(status, PKV_ERR_DEVICE_INDEX);   // loaded as zeros by the bounded TMA, reported
-            return b;
-        };
-        int win_cur = load_window(0);
-        int win_next = load_window(1);
-        for (int j = 0; j < n_kv && ok; ++j) {
-            const int st = j % S;
-            if (j > 0 && (j * kPagesPerTile) % 32 == 0) {
-                win_cur = win_next;
-                win_next = load_window(j * kPagesPerTile / 32 + 1);
-            }
-            const int wofs = (j * kPagesPerTile) % 32;
-            int pb[kPagesPerTile];
-#pragma unroll
-            for (int pg = 0; pg < kPagesPerTile; ++pg) pb[pg] = __shfl_sync(0xffffffffu, win_cur, wofs + pg);
-            // K of tile j once S of tile j-S has read its stage
-            if (j >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKEmpty0 + st], ((j - S) / S) & 1, status));
+        int item = blockIdx.x;
+        int gj = 0;                                    // KV tiles of this CTA so far (ring position)
+        int taken = 0;                                 // items of this CTA
+        int *next_item = reinterpret_cast<int *>(p.ws + (CASCADE ? offsetof(WsHeader, next_prefix_item)
+                                                                  : offsetof(WsHeader, next_ptile_item)));
+        for (int k = 0; ok; ++k) {
+            const int slot = k % kItemSlots;
+            // the slot's previous item has been read by the MMA thread and every softmax warp
+            if (k >= kItemSlots)
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kItemEmpty0 + slot], (k / kItemSlots - 1) & 1, status));
             if (!ok) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars[kKFull0 + st], Cfg::kKVBytes);
-#pragma unroll
-                for (int pg = 0; pg < kPagesPerTile; ++pg)
-                    for (int h = 0; h < Cfg::kHalves; ++h)
-                        tma_load_5d(smem + Cfg::kOffK + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
-                                    &kv_map, &bars[kKFull0 + st], h * 64, 0, 0, g, pb[pg]);
-            }
-            // V of tile j once P V of tile j-S has read its stage
-            if (j >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kVEmpty0 + st], ((j - S) / S) & 1, status));
-            if (!ok) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars[kVFull0 + st], Cfg::kKVBytes);
-#pragma unroll
-                for (int pg = 0; pg < kPagesPerTile; ++pg)
-                    for (int h = 0; h < Cfg::kHalves; ++h)
-                        tma_load_5d(smem + Cfg::kOffV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
-                                    &kv_map, &bars[kVFull0 + st], h * 64, 0, 1, g, pb[pg]);
-            }
-            if (j == end_tile) {
-                // zero V rows past the sequence end in its last (partial) page
-                ok = __all_sync(0xffffffffu, pf_wait(&bars[kVFull0 + st], (j / S) & 1, status));
-                if (!ok) break;
-                const int lp = (L - 1) / kBlock - j * kPagesPerTile;   // page within the tile
-                const int first = L % kBlock;
-                const int nrows = kBlock - first;
-                for (int e = lane; e < Cfg::kHalves * nrows * 8; e += 32) {
-                    const int h = e / (nrows * 8);
-                    const int rem = e % (nrows * 8);
-                    const int row = lp * kBlock + first + rem / 8;
-                    const uint32_t a = sV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + row * 128 + (rem % 8) * 16;
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+            PfItem it{};
+            if (item < n_items) {
+                it.valid = 1;
+                it.g = item % p.num_kv_heads;
+                if constexpr (CASCADE) {
+                    it.r = 0;                          // the prefix blocks are read through request 0's table
+                    it.L = hdr->prefix_blocks * kBlock;
+                    const int kv_all = (it.L + kPrefillKeys - 1) / kPrefillKeys;
+                    const int per = (kv_all + n_parts - 1) / n_parts;   // the plan makes every range non-empty
+                    it.part = (item / p.num_kv_heads) % n_parts;
+                    it.t0 = it.part * per;
+                    it.n_kv = min(kv_all, it.t0 + per) - it.t0;
+                    it.n_pages = hdr->prefix_blocks;
+                    it.rows_total = hdr->n_crows;
+                    it.row0 = (item / (p.num_kv_heads * n_parts)) * kPrefillRows;
+                } else {
+                    const int4 tile = reinterpret_cast<const int4 *>(p.ws + hdr->off_ptiles)[item / p.num_kv_heads];
+                    it.r = tile.x;
+                    it.n_kv = tile.z;
+                    it.L = p.seq_lens[it.r];
+                    it.qs = p.qsl[it.r];
+                    const int qlen = p.qsl[it.r + 1] - it.qs;
+                    it.ctx = it.L - qlen;
+                    it.rows_total = qlen * G;
+                    it.row0 = tile.y * kPrefillRows;
+                    it.n_pages = (it.L + kBlock - 1) / kBlock;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kVFix]);
             }
+            if (lane == 0) {
+                volatile int32_t *dst = reinterpret_cast<volatile int32_t *>(items + slot);
+                const int32_t *src = reinterpret_cast<const int32_t *>(&it);
+#pragma unroll
+                for (int e = 0; e < static_cast<int>(sizeof(PfItem) / 4); ++e) dst[e] = src[e];
+                mbar_arrive(&bars[kItemFull0 + slot]);
+            }
+            if (!it.valid) break;
+            ++taken;
+
+            const int end_tile = end_tile_of(it.L);
+            const int32_t *bt = p.block_tables + static_cast<int64_t>(it.r) * p.max_blocks_per_seq;
+            // block ids in windows of 32 pages (4 KV tiles), one lane per page; the
+            // next window is loaded a window ahead.  Pages past the sequence are -1
+            // and load as zeros (outside the tensor map).
+            constexpr int kPagesPerTile = kPrefillKeys / kBlock;
+            auto load_window = [&](int w) -> int {
+                const int page = it.t0 * kPagesPerTile + w * 32 + lane;
+                const int b = page < it.n_pages ? __ldg(bt + page) : -1;
+                if (page < it.n_pages && (b < 0 || b >= p.num_blocks))
+                    set_status(status, PKV_ERR_DEVICE_INDEX);   // loaded as zeros by the bounded TMA, reported
+                return b;
+            };
+            int win_cur = load_window(0);
+            int win_next = load_window(1);
+            for (int j = 0; j < it.n_kv && ok; ++j) {
+                const int gt = gj + j;
+                const int st = gt % S;
+                if (j > 0 && (j * kPagesPerTile) % 32 == 0) {
+                    win_cur = win_next;
+                    win_next = load_window(j * kPagesPerTile / 32 + 1);
+                }
+                const int wofs = (j * kPagesPerTile) % 32;
+                int pb[kPagesPerTile];
+#pragma unroll
+                for (int pg = 0; pg < kPagesPerTile; ++pg) pb[pg] = __shfl_sync(0xffffffffu, win_cur, wofs + pg);
+                // K of tile gt once S of tile gt-S has read its stage
+                if (gt >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKEmpty0 + st], ((gt - S) / S) & 1, status));
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[kKFull0 + st], Cfg::kKVBytes);
+#pragma unroll
+                    for (int pg = 0; pg < kPagesPerTile; ++pg)
+                        for (int h = 0; h < Cfg::kHalves; ++h)
+                            tma_load_5d(smem + Cfg::kOffK + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
+                                        &kv_map, &bars[kKFull0 + st], h * 64, 0, 0, it.g, pb[pg]);
+                }
+                // V of tile gt once P V of tile gt-S has read its stage
+                if (gt >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kVEmpty0 + st], ((gt - S) / S) & 1, status));
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[kVFull0 + st], Cfg::kKVBytes);
+#pragma unroll
+                    for (int pg = 0; pg < kPagesPerTile; ++pg)
+                        for (int h = 0; h < Cfg::kHalves; ++h)
+                            tma_load_5d(smem + Cfg::kOffV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
+                                        &kv_map, &bars[kVFull0 + st], h * 64, 0, 1, it.g, pb[pg]);
+                }
+                if (j == end_tile) {
+                    // zero V rows past the sequence end in its last (partial) page;
+                    // one fix barrier per stage, so none runs two phases ahead
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kVFull0 + st], (gt / S) & 1, status));
+                    if (!ok) break;
+                    const int lp = (it.L - 1) / kBlock - j * kPagesPerTile;   // page within the tile
+                    const int first = it.L % kBlock;
+                    const int nrows = kBlock - first;
+                    for (int e = lane; e < Cfg::kHalves * nrows * 8; e += 32) {
+                        const int h = e / (nrows * 8);
+                        const int rem = e % (nrows * 8);
+                        const int row = lp * kBlock + first + rem / 8;
+                        const uint32_t a =
+                            sV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + row * 128 + (rem % 8) * 16;
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[kVFix0 + st]);
+                }
+            }
+            gj += it.n_kv;
+            int nxt = 0;
+            if (lane == 0) nxt = static_cast<int>(gridDim.x) + atomicAdd(next_item, 1);
+            item = __shfl_sync(0xffffffffu, nxt, 0);
         }
+        // this CTA's share of the schedule
+        if (lane == 0)
+            reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[(CASCADE ? kStatsCtas : 0) + blockIdx.x] = taken;
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillRows, kPrefillKeys, 0, 0);
             constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillRows, HD, 0, 1);
-            bool ok = pf_wait(&bars[kQFull], 0, status);
-            // S(j) = Q K^T into S buffer j & 1; A = Q in tensor memory
-            auto issue_s = [&](int j) {
-                const int st = j % S;
-                const uint32_t d = tmem + ((j & 1) ? Cfg::kColS1 : Cfg::kColS0);
+            // S(gt) = Q K^T into S buffer gt & 1; A = Q in tensor memory
+            auto issue_s = [&](int gt) {
+                const int st = gt % S;
+                const uint32_t d = tmem + ((gt & 1) ? Cfg::kColS1 : Cfg::kColS0);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint64_t b = smem_desc_sw128(sK + st * Cfg::kKVBytes + (kk >> 2) * (kPrefillKeys * 128) +
@@ -269,14 +335,14 @@ __global__ void __launch_bounds__(384, 1)
                                                        16, 1024);
                     umma_bf16_ts(d, tmem + Cfg::kColQ + kk * 8, b, kIdescS, kk > 0);
                 }
-                umma_commit(&bars[kSFull0 + (j & 1)]);
+                umma_commit(&bars[kSFull0 + (gt & 1)]);
                 umma_commit(&bars[kKEmpty0 + st]);
             };
-            // O (+)= P V; A = P (or its remainder) in S buffer j & 1: keys
+            // O (+)= P V; A = P (or its remainder) in S buffer gt & 1: keys
             // 64 h .. 64 h + 63 sit at columns 64 h + [0, 32) (P) and
             // 64 h + [32, 64) (remainder), each half within its own S columns
-            auto issue_pv = [&](int j, uint32_t pcol, uint32_t accumulate) {
-                const int st = j % S;
+            auto issue_pv = [&](int gt, uint32_t pcol, uint32_t accumulate) {
+                const int st = gt % S;
 #pragma unroll
                 for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
                     const uint64_t b = smem_desc_sw128(sV + st * Cfg::kKVBytes + kk * 2048, kPrefillKeys * 128, 1024);
@@ -284,38 +350,63 @@ __global__ void __launch_bounds__(384, 1)
                                  (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
-            for (int j0 = 0; j0 < 2 && j0 < n_kv && ok; ++j0) {
-                ok = pf_wait(&bars[kKFull0 + j0], 0, status);
+            bool ok = true;
+            int gj = 0;
+            uint32_t vfix_par = 0;                     // phase parity of each stage's fix barrier
+            for (int k = 0; ok; ++k) {
+                const int slot = k % kItemSlots;
+                ok = pf_wait(&bars[kItemFull0 + slot], (k / kItemSlots) & 1, status);
                 if (!ok) break;
-                tc_fence_after();
-                issue_s(j0);
-            }
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j % S;
-                ok = pf_wait(&bars[kPFull0 + (j & 1)], (j >> 1) & 1, status);
-                if (ok) ok = pf_wait(&bars[kVFull0 + st], (j / S) & 1, status);
-                if (ok && j == end_tile) ok = pf_wait(&bars[kVFix], 0, status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t pbuf = tmem + ((j & 1) ? Cfg::kColS1 : Cfg::kColS0);
-                uint32_t vote = 0;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) vote |= votes[(j & 1) * 8 + w];
-                const bool lo = vote != 0u;
-                issue_pv(j, pbuf, j > 0);
-                if (lo) issue_pv(j, pbuf + 32, 1);
-                umma_commit(&bars[kODone0 + (j & 1)]);
-                umma_commit(&bars[kVEmpty0 + st]);
-                // S of tile j+2 overwrites S buffer j & 1, where P V of tile j reads
-                // P: it is issued only once that product has completed (no
-                // overlap of a tensor-memory operand read with a later write)
-                if (j + 2 < n_kv) {
-                    ok = pf_wait(&bars[kODone0 + (j & 1)], (j >> 1) & 1, status);
-                    if (ok) ok = pf_wait(&bars[kKFull0 + (j + 2) % S], ((j + 2) / S) & 1, status);
+                const bool valid = items[slot].valid != 0;
+                const int n_kv = items[slot].n_kv;
+                const int end_tile = end_tile_of(items[slot].L);
+                mbar_arrive(&bars[kItemEmpty0 + slot]);
+                if (!valid) break;
+                // Q of this item in tensor memory (written by the softmax warps)
+                ok = pf_wait(&bars[kQFull], k & 1, status);
+                for (int j0 = 0; j0 < 2 && j0 < n_kv && ok; ++j0) {
+                    const int gt = gj + j0;
+                    // S buffer gt & 1 is free once P V of tile gt-2 has read its P
+                    if (gt >= 2) ok = pf_wait(&bars[kODone0 + (gt & 1)], ((gt - 2) >> 1) & 1, status);
+                    if (ok) ok = pf_wait(&bars[kKFull0 + gt % S], (gt / S) & 1, status);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(j + 2);
+                    issue_s(gt);
                 }
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    const int gt = gj + j;
+                    const int st = gt % S;
+                    ok = pf_wait(&bars[kPFull0 + (gt & 1)], (gt >> 1) & 1, status);
+                    if (ok) ok = pf_wait(&bars[kVFull0 + st], (gt / S) & 1, status);
+                    if (ok && j == end_tile) {
+                        ok = pf_wait(&bars[kVFix0 + st], (vfix_par >> st) & 1u, status);
+                        vfix_par ^= 1u << st;
+                    }
+                    // the previous item's O has been read out by its epilogue
+                    if (ok && j == 0 && k > 0) ok = pf_wait(&bars[kOFree], (k - 1) & 1, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t pbuf = tmem + ((gt & 1) ? Cfg::kColS1 : Cfg::kColS0);
+                    uint32_t vote = 0;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) vote |= votes[(gt & 1) * 8 + w];
+                    const bool lo = vote != 0u;
+                    issue_pv(gt, pbuf, j > 0);
+                    if (lo) issue_pv(gt, pbuf + 32, 1);
+                    umma_commit(&bars[kODone0 + (gt & 1)]);
+                    umma_commit(&bars[kVEmpty0 + st]);
+                    // S of tile gt+2 overwrites S buffer gt & 1, where P V of tile gt
+                    // reads P: it is issued only once that product has completed (no
+                    // overlap of a tensor-memory operand read with a later write)
+                    if (j + 2 < n_kv) {
+                        ok = pf_wait(&bars[kODone0 + (gt & 1)], (gt >> 1) & 1, status);
+                        if (ok) ok = pf_wait(&bars[kKFull0 + (gt + 2) % S], ((gt + 2) / S) & 1, status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(gt + 2);
+                    }
+                }
+                gj += n_kv;
             }
         }
         __syncwarp();
@@ -327,23 +418,6 @@ __global__ void __launch_bounds__(384, 1)
         const int quad = warp & 3;
         const int half = (warp - 4) >> 2;
         const int row = quad * 32 + lane;
-        const int rrow = row0 + row;                       // request row (cascade: row of the prefix pass)
-        const bool valid = rrow < rows_total;
-        // the row's query token and q head within the group; keys [0, lim) visible
-        int tok = 0, hh = 0, lim = 0;
-        int4 crow = make_int4(0, 0, 0, 0);
-        if (valid) {
-            if constexpr (CASCADE) {
-                crow = reinterpret_cast<const int4 *>(p.ws + hdr->off_crows)[rrow];   // {token, request, index, head}
-                tok = crow.x;
-                hh = crow.w;
-                lim = L;
-            } else {
-                tok = qs + rrow / G;
-                hh = rrow % G;
-                lim = ctx + rrow / G + 1;
-            }
-        }
         const float NEG_INF = -__int_as_float(0x7f800000);
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         constexpr int kHalfKeys = kPrefillKeys / 2;        // keys of a tile per thread
@@ -352,27 +426,66 @@ __global__ void __launch_bounds__(384, 1)
         float *xmax = reinterpret_cast<float *>(smem + Cfg::kOffXchg);          // [2][2][128]
         float *xsum = xmax + 2 * 2 * kPrefillRows;                               // [2][128]
         // the two warps of this quadrant meet on an mbarrier, one phase per
-        // tile plus one for the final sums (bounded waits, like every other)
+        // tile plus one per item for the final sums (bounded waits, like every other)
         uint64_t *xbar = &bars[kXchg0 + quad];
+        int xph = 0;
         auto post = [&]() {
             __syncwarp();
             if (lane == 0) mbar_arrive(xbar);
         };
-        auto meet = [&](int phase) -> bool { return __all_sync(0xffffffffu, pf_wait(xbar, phase & 1, status)); };
-        auto exchange = [&](int phase) -> bool {
-            post();
-            return meet(phase);
+        auto meet = [&]() -> bool {
+            const bool done = __all_sync(0xffffffffu, pf_wait(xbar, xph & 1, status));
+            ++xph;
+            return done;
         };
         bool ok = true;
 
-        // this half of the Q row -> tensor memory (A operand of S = Q K^T), zeros past the request
-        {
+        // this thread's row of an item (read from the item's ring slot): query
+        // token, q head within the group, keys [0, lim) visible; cascade rows
+        // {token, request, index, head}
+        struct RowInfo {
+            int tok, hh, lim;
+            bool valid;
+            int4 crow;
+        };
+        auto row_info = [&](const volatile PfItem *it) -> RowInfo {
+            RowInfo ri{0, 0, 0, false, make_int4(0, 0, 0, 0)};
+            const int rrow = it->row0 + row;
+            ri.valid = rrow < it->rows_total;
+            if (ri.valid) {
+                if constexpr (CASCADE) {
+                    ri.crow = reinterpret_cast<const int4 *>(p.ws + hdr->off_crows)[rrow];
+                    ri.tok = ri.crow.x;
+                    ri.hh = ri.crow.w;
+                    ri.lim = it->L;
+                } else {
+                    ri.tok = it->qs + rrow / G;
+                    ri.hh = rrow % G;
+                    ri.lim = it->ctx + rrow / G + 1;
+                }
+            }
+            return ri;
+        };
+        // item k of this CTA: its ring slot once published; the slot is
+        // released after the item's epilogue (every lane reads it meanwhile)
+        auto wait_item = [&](int k) -> bool {
+            return __all_sync(0xffffffffu,
+                              pf_wait(&bars[kItemFull0 + k % kItemSlots], (k / kItemSlots) & 1, status));
+        };
+        auto release_item = [&](int k) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + k % kItemSlots]);
+        };
+        // this half of the item's Q row -> tensor memory (A operand of S = Q K^T),
+        // zeros past the request
+        auto load_q = [&](const volatile PfItem *it) {
+            const RowInfo ri = row_info(it);
             uint32_t qv[kHalfDims / 2];
-            const __nv_bfloat16 *qp = query + static_cast<int64_t>(tok) * q_stride +
-                                      static_cast<int64_t>(g * G + hh) * HD + half * kHalfDims;
+            const __nv_bfloat16 *qp = query + static_cast<int64_t>(ri.tok) * q_stride +
+                                      static_cast<int64_t>(it->g * G + ri.hh) * HD + half * kHalfDims;
 #pragma unroll
             for (int c = 0; c < kHalfDims / 8; ++c) {
-                const uint4 w = valid ? __ldg(reinterpret_cast<const uint4 *>(qp) + c) : make_uint4(0, 0, 0, 0);
+                const uint4 w = ri.valid ? __ldg(reinterpret_cast<const uint4 *>(qp) + c) : make_uint4(0, 0, 0, 0);
                 qv[4 * c + 0] = w.x;
                 qv[4 * c + 1] = w.y;
                 qv[4 * c + 2] = w.z;
@@ -387,204 +500,240 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kQFull]);
-        }
+        };
 
-        float m_ref = NEG_INF, l = 0.f;                    // l: this half's sum
-        for (int j = 0; j < n_kv && ok; ++j) {
-            const int sb = j & 1;
-            const uint32_t sbuf = trow + (sb ? Cfg::kColS1 : Cfg::kColS0);
-            ok = __all_sync(0xffffffffu, pf_wait(&bars[kSFull0 + sb], (j >> 1) & 1, status));
-            if (!ok) break;
-            tc_fence_after();
-            // this half's scores (keys key0 .. key0 + 63); keys a row may not see
-            // become -inf, tested only in tiles reaching some row's limit
-            const int key0 = (t0 + j) * kPrefillKeys + half * kHalfKeys;
-            float x[kHalfKeys];
-            auto load_scores = [&]() {
-                uint32_t v[2][32];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) tmem_ld32(sbuf + half * kHalfKeys + c * 32, v[c]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
-                if (__any_sync(0xffffffffu, key0 + kHalfKeys > lim)) {
-#pragma unroll
-                    for (int c = 0; c < kHalfKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
+        ok = wait_item(0);
+        if (ok && items[0].valid) load_q(items);
+        int gj = 0;                                        // KV tiles of this CTA so far
+        int k = 0;
+        for (; ok && items[k % kItemSlots].valid; ++k) {
+            const volatile PfItem *cur = items + k % kItemSlots;
+            const int n_kv = cur->n_kv;
+            const int kbase = cur->t0 * kPrefillKeys + half * kHalfKeys;
+            // where this row's result goes (-1: nowhere): element offset in out,
+            // or the partial row of split `part` (cascade)
+            int64_t dst = -1;
+            int lim = 0;
+            {
+                const RowInfo ri = row_info(cur);
+                lim = ri.lim;
+                if (ri.valid) {
+                    if constexpr (CASCADE) {
+                        const int4 rq = reinterpret_cast<const int4 *>(p.ws + hdr->off_req)[ri.crow.y];
+                        dst = rq.y + (static_cast<int64_t>(ri.crow.z) * p.num_q_heads + cur->g * G + ri.hh) * rq.x +
+                              cur->part;
+                    } else {
+                        dst = (static_cast<int64_t>(ri.tok) * p.num_q_heads + cur->g * G + ri.hh) * HD +
+                              half * kHalfDims;
+                    }
                 }
-            };
-            // weights p = 2^(x scale - ref) on pairs in place, with their sum
-            // and sum of squares (the special-function unit has room for every
-            // exponential of the tile)
-            float psum = 0.f, psq = 0.f;
-            auto weights = [&](float ref) {
-                const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
-                uint64_t ps2[4] = {0, 0, 0, 0}, pq2[4] = {0, 0, 0, 0};
-#pragma unroll
-                for (int c = 0; c < kHalfKeys; c += 2) {
-                    const uint64_t y2 = f2_fma(f2_pack(x[c], x[c + 1]), sc2, nref2);
-                    float y0, y1;
-                    f2_unpack(y2, y0, y1);
-                    const uint64_t p2 = f2_pack(fast_exp2(y0), fast_exp2(y1));
-                    ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], p2);
-                    pq2[(c >> 1) & 3] = f2_fma(p2, p2, pq2[(c >> 1) & 3]);
-                    f2_unpack(p2, x[c], x[c + 1]);
-                }
-                float a0, a1, b0, b1;
-                f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), a0, a1);
-                f2_unpack(f2_add(f2_add(pq2[0], pq2[1]), f2_add(pq2[2], pq2[3])), b0, b1);
-                psum = a0 + a1;
-                psq = b0 + b1;
-            };
-            load_scores();
-            // this half's max (four chains of three-input maxima)
-            float mx4[4] = {fmaxf(x[0], x[1]), fmaxf(x[2], x[3]), fmaxf(x[4], x[5]), fmaxf(x[6], x[7])};
-#pragma unroll
-            for (int c = 8; c < kHalfKeys; c += 8) {
-                mx4[0] = fmax3(mx4[0], x[c], x[c + 1]);
-                mx4[1] = fmax3(mx4[1], x[c + 2], x[c + 3]);
-                mx4[2] = fmax3(mx4[2], x[c + 4], x[c + 5]);
-                mx4[3] = fmax3(mx4[3], x[c + 6], x[c + 7]);
             }
-            float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            // post this half's max; while the other half's arrives, the weights
-            // are computed against the current reference when it holds for
-            // every row of this warp (the usual case after the first tile).
-            // Rows past the request never see a key and keep a -inf reference;
-            // a half that sees no key of a row has zero weights whatever the
-            // reference becomes.  Every lane takes part in the vote.
-            xmax[(sb * 2 + half) * kPrefillRows + row] = mx;
-            post();
-            const bool first = m_ref == NEG_INF;           // O holds nothing yet for this row
-            const bool ready = first ? mx == NEG_INF : mx * p.scale_log2 <= m_ref + 8.f;
-            const bool early = __all_sync(0xffffffffu, ready);
-            if (early) weights(first ? 0.f : m_ref);
-            ok = meet(j);
-            if (!ok) break;
-            mx = fmaxf(mx, xmax[(sb * 2 + (half ^ 1)) * kPrefillRows + row]);
-            // log2-domain max (scale > 0 keeps the order of scores); both halves
-            // take the same decisions from the same values
-            const float m_new = fmaxf(m_ref, mx * p.scale_log2);
-            const bool grow = !first && m_new > m_ref + 8.f;
-            const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
-            if (first || grow) m_ref = m_new;
-            if (!early || __any_sync(0xffffffffu, grow)) {
-                // the reference moved for some row of this warp: weights again
-                // from this half's own S columns (no other warp writes them)
-                tc_fence_after();
-                load_scores();
-                weights((m_ref == NEG_INF) ? 0.f : m_ref);
-            }
-            l = l * alpha + psum;
-            // this warp's vote: does any of its rows need the remainder of P?
-            // (half sums: if neither half's weights are concentrated, the row's
-            // are not either)
-            const bool need = j < p.lo_tiles || psq > kLoConcentration * l * l;
-            const bool wneed = __any_sync(0xffffffffu, need);
-            // P V of tile j-1 must be done before O is rescaled; the barrier of
-            // tile j-2 (same parity) is waited every tile, which keeps each
-            // barrier at most one phase ahead of this thread
-            if (j >= 2) {
-                ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + sb], ((j - 2) >> 1) & 1, status));
+            float m_ref = NEG_INF, l = 0.f;                // l: this half's sum
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int gt = gj + j;
+                const int sb = gt & 1;
+                const uint32_t sbuf = trow + (sb ? Cfg::kColS1 : Cfg::kColS0);
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kSFull0 + sb], (gt >> 1) & 1, status));
                 if (!ok) break;
-            }
-            if (__any_sync(0xffffffffu, grow)) {              // rare: this half of O rescaled
-                if (j >= 1) {
-                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + (sb ^ 1)], ((j - 1) >> 1) & 1, status));
-                    if (!ok) break;
-                }
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < kHalfDims / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(trow + Cfg::kColO + half * kHalfDims + c * 32, v);
+                // this half's scores (keys key0 .. key0 + 63); keys a row may not see
+                // become -inf, tested only in tiles reaching some row's limit
+                const int key0 = kbase + j * kPrefillKeys;
+                float x[kHalfKeys];
+                auto load_scores = [&]() {
+                    uint32_t v[2][32];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) tmem_ld32(sbuf + half * kHalfKeys + c * 32, v[c]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(trow + Cfg::kColO + half * kHalfDims + c * 32, v);
-                }
-            }
-            // P (bf16 pairs) of this half's keys into the tile's S buffer; the
-            // remainder too when this warp asks for it, zeros otherwise
-            {
-                uint32_t w[32];
+                    for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-                tmem_st32(sbuf + half * 64, w);
-                if (wneed) {
+                        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[c][e]);
+                    if (__any_sync(0xffffffffu, key0 + kHalfKeys > lim)) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float a0 = x[2 * e], a1 = x[2 * e + 1];
-                        const float2 hb = __bfloat1622float2(__floats2bfloat162_rn(a0, a1));
-                        w[e] = pack_bf16x2(a0 - hb.x, a1 - hb.y);
+                        for (int c = 0; c < kHalfKeys; ++c) x[c] = (key0 + c < lim) ? x[c] : NEG_INF;
                     }
-                } else {
+                };
+                // weights p = 2^(x scale - ref) on pairs in place, with their sum
+                // and sum of squares (the special-function unit has room for every
+                // exponential of the tile)
+                float psum = 0.f, psq = 0.f;
+                auto weights = [&](float ref) {
+                    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
+                    uint64_t ps2[4] = {0, 0, 0, 0}, pq2[4] = {0, 0, 0, 0};
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) w[e] = 0u;
-                }
-                tmem_st32(sbuf + half * 64 + 32, w);
-            }
-            tmem_st_wait();
-            if (lane == 0) votes[(j & 1) * 8 + (warp - 4)] = wneed ? 1u : 0u;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kPFull0 + (j & 1)]);
-        }
-        if (ok) {
-            // epilogue: the last two P V, then O / l to bf16
-            if (n_kv >= 2) ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + (n_kv & 1)], ((n_kv - 2) >> 1) & 1,
-                                                                status));
-            if (ok) ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + ((n_kv - 1) & 1)], ((n_kv - 1) >> 1) & 1,
-                                                         status));
-        }
-        // the row's sum: this half's plus the other's
-        if (ok) {
-            xsum[half * kPrefillRows + row] = l;
-            ok = exchange(n_kv);
-            l += xsum[(half ^ 1) * kPrefillRows + row];
-        }
-        if (ok) {
-            tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint32_t v[kHalfDims / 32][32];
-#pragma unroll
-            for (int c = 0; c < kHalfDims / 32; ++c) tmem_ld32(trow + Cfg::kColO + half * kHalfDims + c * 32, v[c]);
-            tmem_ld_wait();
-            if constexpr (CASCADE) {
-                if (valid) {
-                    // split `part` of the row: normalised partial output and natural log-sum-exp
-                    const int4 ri = reinterpret_cast<const int4 *>(p.ws + hdr->off_req)[crow.y];
-                    const int64_t prow =
-                        ri.y + (static_cast<int64_t>(crow.z) * p.num_q_heads + g * G + hh) * ri.x + part;
-                    float *po = reinterpret_cast<float *>(p.ws + hdr->off_part_o) + prow * HD + half * kHalfDims;
-#pragma unroll
-                    for (int c = 0; c < kHalfDims / 32; ++c)
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4 *>(po + c * 32 + e) =
-                                make_float4(__uint_as_float(v[c][e]) * inv, __uint_as_float(v[c][e + 1]) * inv,
-                                            __uint_as_float(v[c][e + 2]) * inv, __uint_as_float(v[c][e + 3]) * inv);
-                    if (half == 0)
-                        reinterpret_cast<float *>(p.ws + hdr->off_part_lse)[prow] =
-                            l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
-                }
-            } else if (valid) {
-                __nv_bfloat16 *dst =
-                    p.out + (static_cast<int64_t>(tok) * p.num_q_heads + g * G + hh) * HD + half * kHalfDims;
-#pragma unroll
-                for (int c = 0; c < kHalfDims / 32; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[c][e + 0]) * inv, __uint_as_float(v[c][e + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(v[c][e + 2]) * inv, __uint_as_float(v[c][e + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(v[c][e + 4]) * inv, __uint_as_float(v[c][e + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(v[c][e + 6]) * inv, __uint_as_float(v[c][e + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
+                    for (int c = 0; c < kHalfKeys; c += 2) {
+                        const uint64_t y2 = f2_fma(f2_pack(x[c], x[c + 1]), sc2, nref2);
+                        float y0, y1;
+                        f2_unpack(y2, y0, y1);
+                        const uint64_t p2 = f2_pack(fast_exp2(y0), fast_exp2(y1));
+                        ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], p2);
+                        pq2[(c >> 1) & 3] = f2_fma(p2, p2, pq2[(c >> 1) & 3]);
+                        f2_unpack(p2, x[c], x[c + 1]);
                     }
+                    float a0, a1, b0, b1;
+                    f2_unpack(f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3])), a0, a1);
+                    f2_unpack(f2_add(f2_add(pq2[0], pq2[1]), f2_add(pq2[2], pq2[3])), b0, b1);
+                    psum = a0 + a1;
+                    psq = b0 + b1;
+                };
+                load_scores();
+                // this half's max (four chains of three-input maxima)
+                float mx4[4] = {fmaxf(x[0], x[1]), fmaxf(x[2], x[3]), fmaxf(x[4], x[5]), fmaxf(x[6], x[7])};
+#pragma unroll
+                for (int c = 8; c < kHalfKeys; c += 8) {
+                    mx4[0] = fmax3(mx4[0], x[c], x[c + 1]);
+                    mx4[1] = fmax3(mx4[1], x[c + 2], x[c + 3]);
+                    mx4[2] = fmax3(mx4[2], x[c + 4], x[c + 5]);
+                    mx4[3] = fmax3(mx4[3], x[c + 6], x[c + 7]);
+                }
+                float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                // post this half's max; while the other half's arrives, the weights
+                // are computed against the current reference when it holds for
+                // every row of this warp (the usual case after the first tile).
+                // Rows past the request never see a key and keep a -inf reference;
+                // a half that sees no key of a row has zero weights whatever the
+                // reference becomes.  Every lane takes part in the vote.
+                xmax[(sb * 2 + half) * kPrefillRows + row] = mx;
+                post();
+                const bool first = m_ref == NEG_INF;       // O holds nothing yet for this row
+                const bool ready = first ? mx == NEG_INF : mx * p.scale_log2 <= m_ref + 8.f;
+                const bool early = __all_sync(0xffffffffu, ready);
+                if (early) weights(first ? 0.f : m_ref);
+                ok = meet();
+                if (!ok) break;
+                mx = fmaxf(mx, xmax[(sb * 2 + (half ^ 1)) * kPrefillRows + row]);
+                // log2-domain max (scale > 0 keeps the order of scores); both halves
+                // take the same decisions from the same values
+                const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+                const bool grow = !first && m_new > m_ref + 8.f;
+                const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
+                if (first || grow) m_ref = m_new;
+                if (!early || __any_sync(0xffffffffu, grow)) {
+                    // the reference moved for some row of this warp: weights again
+                    // from this half's own S columns (no other warp writes them)
+                    tc_fence_after();
+                    load_scores();
+                    weights((m_ref == NEG_INF) ? 0.f : m_ref);
+                }
+                l = l * alpha + psum;
+                // this warp's vote: does any of its rows need the remainder of P?
+                // (half sums: if neither half's weights are concentrated, the row's
+                // are not either)
+                const bool need = j < p.lo_tiles || psq > kLoConcentration * l * l;
+                const bool wneed = __any_sync(0xffffffffu, need);
+                // P V of tile gt-1 must be done before O is rescaled; the barrier of
+                // tile gt-2 (same parity) is waited every tile, which keeps each
+                // barrier at most one phase ahead of this thread
+                if (gt >= 2) {
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + sb], ((gt - 2) >> 1) & 1, status));
+                    if (!ok) break;
+                }
+                if (__any_sync(0xffffffffu, grow)) {          // rare: this half of O rescaled
+                    // grow needs an earlier tile of this item, so j >= 1
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + (sb ^ 1)], ((gt - 1) >> 1) & 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < kHalfDims / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(trow + Cfg::kColO + half * kHalfDims + c * 32, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st32(trow + Cfg::kColO + half * kHalfDims + c * 32, v);
+                    }
+                }
+                // P (bf16 pairs) of this half's keys into the tile's S buffer; the
+                // remainder too when this warp asks for it, zeros otherwise
+                // (16 columns at a time: fewer registers live)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]);
+                    tmem_st16(sbuf + half * 64 + 16 * c, w);
+                    if (wneed) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float a0 = x[32 * c + 2 * e], a1 = x[32 * c + 2 * e + 1];
+                            const float2 hb = __bfloat1622float2(__floats2bfloat162_rn(a0, a1));
+                            w[e] = pack_bf16x2(a0 - hb.x, a1 - hb.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) w[e] = 0u;
+                    }
+                    tmem_st16(sbuf + half * 64 + 32 + 16 * c, w);
+                }
+                tmem_st_wait();
+                if (lane == 0) votes[sb * 8 + (warp - 4)] = wneed ? 1u : 0u;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kPFull0 + sb]);
             }
+            gj += n_kv;
+            // the next item's Q right away: every S of this item has completed
+            if (ok) ok = wait_item(k + 1);
+            if (ok && items[(k + 1) % kItemSlots].valid) load_q(items + (k + 1) % kItemSlots);
+            if (ok) {
+                // epilogue: the last two P V, then O / l
+                if (n_kv >= 2)
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + (gj & 1)], ((gj - 2) >> 1) & 1, status));
+                if (ok)
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kODone0 + ((gj - 1) & 1)], ((gj - 1) >> 1) & 1, status));
+            }
+            // the row's sum: this half's plus the other's
+            if (ok) {
+                xsum[half * kPrefillRows + row] = l;
+                post();
+                ok = meet();
+                l += xsum[(half ^ 1) * kPrefillRows + row];
+            }
+            if (ok) {
+                tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint32_t v[kHalfDims / 32][32];
+#pragma unroll
+                for (int c = 0; c < kHalfDims / 32; ++c) tmem_ld32(trow + Cfg::kColO + half * kHalfDims + c * 32, v[c]);
+                tmem_ld_wait();
+                // O is in registers: the next item's first P V may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kOFree]);
+                if (dst >= 0) {
+                    if constexpr (CASCADE) {
+                        // split `part` of the row: normalised partial output and natural log-sum-exp
+                        float *po = reinterpret_cast<float *>(p.ws + hdr->off_part_o) + dst * HD + half * kHalfDims;
+#pragma unroll
+                        for (int c = 0; c < kHalfDims / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                *reinterpret_cast<float4 *>(po + c * 32 + e) =
+                                    make_float4(__uint_as_float(v[c][e]) * inv, __uint_as_float(v[c][e + 1]) * inv,
+                                                __uint_as_float(v[c][e + 2]) * inv, __uint_as_float(v[c][e + 3]) * inv);
+                        if (half == 0)
+                            reinterpret_cast<float *>(p.ws + hdr->off_part_lse)[dst] =
+                                l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+                    } else {
+                        __nv_bfloat16 *o = p.out + dst;
+#pragma unroll
+                        for (int c = 0; c < kHalfDims / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; e += 8) {
+                                uint4 w;
+                                w.x = pack_bf16x2(__uint_as_float(v[c][e + 0]) * inv, __uint_as_float(v[c][e + 1]) * inv);
+                                w.y = pack_bf16x2(__uint_as_float(v[c][e + 2]) * inv, __uint_as_float(v[c][e + 3]) * inv);
+                                w.z = pack_bf16x2(__uint_as_float(v[c][e + 4]) * inv, __uint_as_float(v[c][e + 5]) * inv);
+                                w.w = pack_bf16x2(__uint_as_float(v[c][e + 6]) * inv, __uint_as_float(v[c][e + 7]) * inv);
+                                *reinterpret_cast<uint4 *>(o + c * 32 + e) = w;
+                            }
+                    }
+                }
+            }
+            release_item(k);
         }
+        if (ok) release_item(k);                           // the closing (empty) item
     }
 
     // teardown: every role is done with tensor memory
