@@ -27,8 +27,10 @@ struct WsHeader {
     int32_t prefix_parts;    // the prefix keys are cut into this many splits (KV-tile ranges)
     int32_t next_ptile_item;    // prefill kernel: next work item to claim, less its grid size
     int32_t next_prefix_item;   // shared-prefix pass: the same
+    int32_t n_split_tokens;     // tokens whose rows the combine merges
+    int32_t pad_;
     int64_t off_req;         // int4 [num_seqs]: {splits (0: refused), partial row base, first chunk, chunks}
-    int64_t off_tok;         // int2 [num_tokens]: {request, index in request} (-1 if none)
+    int64_t off_stoks;       // int4 [num_tokens]: split tokens {token, partial row of q head 0, splits, 0}
     int64_t off_chunks;      // int4 [max_chunks]: {request, split or tile, page begin, page end}
     int64_t off_ptiles;      // int4 [max_ptiles]: {request, q tile, kv tiles, 0}
     int64_t off_crows;       // int4 [max_crows]: {token, request, query index, q head in group}
@@ -49,7 +51,7 @@ constexpr int64_t kStatsOffset = 256;
 constexpr int kStatsCtas = 1024;
 
 struct WsLayout {
-    int64_t off_req, off_tok, off_chunks, off_ptiles, off_crows, off_part_lse, off_part_o, total;
+    int64_t off_req, off_stoks, off_chunks, off_ptiles, off_crows, off_part_lse, off_part_o, total;
     int64_t max_chunks, max_ptiles, max_crows, max_prow;
     int32_t prefix_parts;     // splits of the shared prefix (0: no cascade)
 };

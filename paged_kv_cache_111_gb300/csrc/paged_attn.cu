@@ -80,8 +80,8 @@ static WsLayout ws_layout(int64_t num_seqs, int64_t num_tokens, int64_t max_quer
     int64_t off = kStatsOffset + 2 * kStatsCtas * 4;
     w.off_req = off;
     off = align256(off + 16 * num_seqs);
-    w.off_tok = off;
-    off = align256(off + 8 * num_tokens);
+    w.off_stoks = off;
+    off = align256(off + 16 * num_tokens);
     w.off_chunks = off;
     off = align256(off + 16 * w.max_chunks);
     w.off_ptiles = off;
@@ -148,21 +148,22 @@ struct ReqPlan {
 // Mode 0 request r may take the cascade path: its table starts with request
 // 0's first prefix_blocks blocks (`differs`: it does not), and every one of
 // its rows sees all of them.
-__device__ bool cascade_eligible(const PlanParams &p, int r, bool differs) {
+__device__ bool cascade_eligible(const PlanParams &p, const int *qsl, const int *lens, int r, bool differs) {
     const int K = p.prefix_blocks;
     if (K <= 0 || differs) return false;
-    const int q = p.qsl[r + 1] - p.qsl[r];
+    const int q = qsl[r + 1] - qsl[r];
     const int G = p.num_q_heads / p.num_kv_heads;
-    if (q <= 0 || q * G > 16 || p.seq_lens[0] - (p.qsl[1] - p.qsl[0]) < K * kBlock) return false;
-    return p.seq_lens[r] - q >= K * kBlock && K <= p.max_blocks_per_seq;
+    if (q <= 0 || q * G > 16 || lens[0] - (qsl[1] - qsl[0]) < K * kBlock) return false;
+    return lens[r] - q >= K * kBlock && K <= p.max_blocks_per_seq;
 }
 
-__device__ ReqPlan plan_request(const PlanParams &p, int r, int pages_per_split, bool cascade = false) {
+__device__ ReqPlan plan_request(const PlanParams &p, const int *qsl, const int *lens, int r, int pages_per_split,
+                                bool cascade) {
     ReqPlan rp{0, 0, 0, 0, 0, 0, 0, 0, 0};
     const int G = p.num_q_heads / p.num_kv_heads;
-    const int q0 = p.qsl[r], q1 = p.qsl[r + 1];
+    const int q0 = qsl[r], q1 = qsl[r + 1];
     const int q = q1 - q0;
-    const int L = p.seq_lens[r];
+    const int L = lens[r];
     if (q0 < 0 || q < 0 || q1 > p.num_tokens || L < q || L > p.max_seq_len || q > p.max_query_len ||
         div_up(L, kBlock) > p.max_blocks_per_seq)
         return rp;
@@ -254,86 +255,106 @@ __device__ __forceinline__ int agg_inc(int *counter, int bin) {
     return base + __popc(peers & ((1u << lane) - 1u));
 }
 
-// Block-wide exclusive scan of a pair of non-negative counts (one pair per
+// Block-wide exclusive scan of four non-negative counts (one set per
 // thread); returns this thread's prefix and writes the totals to *total.
-__device__ int2 block_scan2(int a, int b, int2 *warp_tot, int2 *total) {
+__device__ int4 block_scan4(int a, int b, int c, int d, int4 *warp_tot, int4 *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int ia = a, ib = b;
+    int4 in = make_int4(a, b, c, d);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int va = __shfl_up_sync(0xffffffffu, ia, o);
-        const int vb = __shfl_up_sync(0xffffffffu, ib, o);
+        const int va = __shfl_up_sync(0xffffffffu, in.x, o);
+        const int vb = __shfl_up_sync(0xffffffffu, in.y, o);
+        const int vc = __shfl_up_sync(0xffffffffu, in.z, o);
+        const int vd = __shfl_up_sync(0xffffffffu, in.w, o);
         if (lane >= o) {
-            ia += va;
-            ib += vb;
+            in.x += va;
+            in.y += vb;
+            in.z += vc;
+            in.w += vd;
         }
     }
-    if (lane == 31) warp_tot[warp] = make_int2(ia, ib);
+    if (lane == 31) warp_tot[warp] = in;
     __syncthreads();
     if (warp == 0) {
         const int nw = blockDim.x >> 5;
-        int2 w = lane < nw ? warp_tot[lane] : make_int2(0, 0);
-        int wa = w.x, wb = w.y;
+        const int4 w = lane < nw ? warp_tot[lane] : make_int4(0, 0, 0, 0);
+        int4 x = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int va = __shfl_up_sync(0xffffffffu, wa, o);
-            const int vb = __shfl_up_sync(0xffffffffu, wb, o);
+            const int va = __shfl_up_sync(0xffffffffu, x.x, o);
+            const int vb = __shfl_up_sync(0xffffffffu, x.y, o);
+            const int vc = __shfl_up_sync(0xffffffffu, x.z, o);
+            const int vd = __shfl_up_sync(0xffffffffu, x.w, o);
             if (lane >= o) {
-                wa += va;
-                wb += vb;
+                x.x += va;
+                x.y += vb;
+                x.z += vc;
+                x.w += vd;
             }
         }
-        if (lane < nw) warp_tot[lane] = make_int2(wa - w.x, wb - w.y);   // exclusive warp prefix
-        if (lane == nw - 1) *total = make_int2(wa, wb);
+        if (lane < nw) warp_tot[lane] = make_int4(x.x - w.x, x.y - w.y, x.z - w.z, x.w - w.w);   // exclusive
+        if (lane == nw - 1) *total = x;
     }
     __syncthreads();
-    const int2 wp = warp_tot[warp];
-    return make_int2(wp.x + ia - a, wp.y + ib - b);
+    const int4 wp = warp_tot[warp];
+    return make_int4(wp.x + in.x - a, wp.y + in.y - b, wp.z + in.z - c, wp.w + in.w - d);
 }
 
 // One CTA plans the call: checks every request, splits decode rows along
 // keys, cuts long requests into tiles, and lists the work largest first
 // (counting sort by size) so the persistent decode kernel's fixed item order
 // balances its warps.  Per-request and per-chunk passes run in parallel over
-// requests and over chunks.
+// requests and over chunks.  The requests' query starts, lengths and plans
+// sit in shared memory when there are at most kPlanStagedSeqs of them (every
+// pass then reads shared memory only); larger batches use the workspace.
+constexpr int kPlanStagedSeqs = 1024;
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __shared__ int bin_count[kSizeBins];
     __shared__ int bin_cursor[kSizeBins];
     __shared__ int pbin_count[kSizeBins];
     __shared__ int pbin_cursor[kSizeBins];
-    __shared__ int2 warp_tot[kPlanThreads / 32];
-    __shared__ int2 totals;
+    __shared__ int4 warp_tot[kPlanThreads / 32];
+    __shared__ int4 totals;
     __shared__ unsigned long long total_pages;
     __shared__ int bad;
     __shared__ int pages_per_split;
+    __shared__ int s_qsl[kPlanStagedSeqs + 1];
+    __shared__ int s_len[kPlanStagedSeqs];
+    __shared__ int4 s_req[kPlanStagedSeqs];
 
     WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
-    int4 *req = reinterpret_cast<int4 *>(p.ws + p.lay.off_req);
-    int2 *tok = reinterpret_cast<int2 *>(p.ws + p.lay.off_tok);
+    int4 *req_ws = reinterpret_cast<int4 *>(p.ws + p.lay.off_req);
+    int4 *stoks = reinterpret_cast<int4 *>(p.ws + p.lay.off_stoks);
     int4 *chunks = reinterpret_cast<int4 *>(p.ws + p.lay.off_chunks);
     int4 *ptiles = reinterpret_cast<int4 *>(p.ws + p.lay.off_ptiles);
     int4 *crows = reinterpret_cast<int4 *>(p.ws + p.lay.off_crows);
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int G = p.num_q_heads / p.num_kv_heads;
-    __shared__ int2 ctotals;
     pdl_wait();       // the previous kernel on the stream may still read this workspace
     pdl_trigger();
-    for (int i = tid; i < 2 * kStatsCtas; i += nthr) reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[i] = 0;
 
+    const bool staged = p.num_seqs <= kPlanStagedSeqs;
+    const int *qsl = staged ? s_qsl : p.qsl;
+    const int *lens = staged ? s_len : p.seq_lens;
+    // {splits (0: refused), partial row base, first chunk, chunks} per request;
+    // .x is first the flag "table differs from request 0's in the prefix"
+    int4 *req = staged ? s_req : req_ws;
+    if (staged) {
+        for (int r = tid; r <= p.num_seqs; r += nthr) s_qsl[r] = __ldg(p.qsl + r);
+        for (int r = tid; r < p.num_seqs; r += nthr) s_len[r] = __ldg(p.seq_lens + r);
+    }
+    for (int i = tid; i < 2 * kStatsCtas; i += nthr) reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[i] = 0;
     for (int i = tid; i < kSizeBins; i += nthr) {
         bin_count[i] = 0;
         pbin_count[i] = 0;
     }
-    if (tid == 0) {
-        total_pages = 0;
-        bad = p.qsl[0] != 0;
-    }
-    for (int t = tid; t < p.num_tokens; t += nthr) tok[t] = make_int2(-1, -1);
-    // req[r].x is first the flag "table differs from request 0's in the prefix"
+    if (tid == 0) total_pages = 0;
     if (p.prefix_blocks > 0)
         for (int r = tid; r < p.num_seqs; r += nthr) req[r] = make_int4(0, 0, 0, 0);
     __syncthreads();
+    if (tid == 0) bad = qsl[0] != 0;
     if (p.prefix_blocks > 0 && p.prefix_blocks <= p.max_blocks_per_seq) {
         // every (request, prefix block) pair at once, four loads in flight per thread
         const int K = p.prefix_blocks;
@@ -359,11 +380,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     // pass 1: total key pages of split requests (sets the automatic split size)
     unsigned long long mine = 0;
     for (int r = tid; r < p.num_seqs; r += nthr) {
-        const int q = p.qsl[r + 1] - p.qsl[r];
-        const int L = p.seq_lens[r];
+        const int q = qsl[r + 1] - qsl[r];
+        const int L = lens[r];
         if (q > 0 && q * G <= 16 && L >= q) {
             // a cascade request's prefix pages are not decode-kernel work
-            const bool casc = cascade_eligible(p, r, p.prefix_blocks > 0 && req[r].x != 0);
+            const bool casc = cascade_eligible(p, qsl, lens, r, p.prefix_blocks > 0 && req[r].x != 0);
             mine += (unsigned long long)(div_up(L, kBlock) - (casc ? p.prefix_blocks : 0));
         }
     }
@@ -385,45 +406,53 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const int per_thr = div_up(max(p.num_seqs, 1), nthr);
     const int r_begin = min(p.num_seqs, tid * per_thr), r_end = min(p.num_seqs, r_begin + per_thr);
     // (a cascade request's splits are its suffix chunks plus the shared prefix)
-    int my_chunks = 0, my_prows = 0, my_crows = 0;
+    int my_chunks = 0, my_prows = 0, my_crows = 0, my_stoks = 0;
     unsigned my_casc = 0;                            // bit k: request r_begin + k takes the cascade path
     for (int r = r_begin; r < r_end; ++r) {
-        const bool casc = cascade_eligible(p, r, p.prefix_blocks > 0 && req[r].x != 0);
+        const bool casc = cascade_eligible(p, qsl, lens, r, p.prefix_blocks > 0 && req[r].x != 0);
         if (casc && r - r_begin < 32) my_casc |= 1u << (r - r_begin);
-        const ReqPlan rp = plan_request(p, r, pps, casc && r - r_begin < 32);
+        const ReqPlan rp = plan_request(p, qsl, lens, r, pps, casc && r - r_begin < 32);
         if (!rp.valid) {
             bad = 1;
             continue;
         }
         my_chunks += rp.n_chunks;
         const int nsplit = rp.n_chunks + (rp.first > 0 ? p.lay.prefix_parts : 0);
-        if (rp.mode == 0 && nsplit > 1) my_prows += rp.q * p.num_q_heads * nsplit;
+        if (rp.mode == 0 && nsplit > 1) {
+            my_prows += rp.q * p.num_q_heads * nsplit;
+            my_stoks += rp.q;
+        }
         if (rp.first > 0) my_crows += rp.rows;
     }
-    const int2 pre = block_scan2(my_chunks, my_prows, warp_tot, &totals);
-    const int2 cpre = block_scan2(my_crows, 0, warp_tot, &ctotals);
+    const int4 pre = block_scan4(my_chunks, my_prows, my_crows, my_stoks, warp_tot, &totals);
     const int n_total = totals.x;
     const bool fits = n_total <= p.lay.max_chunks + p.lay.max_ptiles && totals.y <= p.lay.max_prow &&
-                      ctotals.x <= p.lay.max_crows;
+                      totals.z <= p.lay.max_crows;
     {
-        int cb = pre.x, pbase = pre.y, crow = cpre.x;
+        int cb = pre.x, pbase = pre.y, crow = pre.z, sbase = pre.w;
         for (int r = r_begin; r < r_end; ++r) {
             const bool casc = (my_casc >> (r - r_begin)) & 1u;
-            const ReqPlan rp = plan_request(p, r, pps, casc);
+            const ReqPlan rp = plan_request(p, qsl, lens, r, pps, casc);
             const int n = (rp.valid && fits) ? rp.n_chunks : 0;
             const int nsplit = rp.n_chunks + (rp.first > 0 ? p.lay.prefix_parts : 0);
             const bool split = rp.valid && fits && rp.mode == 0 && nsplit > 1;
-            // {splits (0: request refused), partial row base, first chunk, chunks};
             // a cascade request has splits = chunks + prefix_parts (>= 1), which
             // no other request has
             req[r] = make_int4(rp.valid && fits ? (split ? nsplit : 1) : 0, split ? pbase : 0, cb, n);
             if (rp.valid && fits && rp.first > 0) {
-                const int q0 = p.qsl[r];
+                const int q0 = qsl[r];
                 for (int row = 0; row < rp.rows; ++row) crows[crow + row] = make_int4(q0 + row / G, r, row / G, row % G);
                 crow += rp.rows;
             }
             cb += n;
-            if (split) pbase += rp.q * p.num_q_heads * nsplit;
+            if (split) {
+                // the request's tokens, whose rows the combine merges
+                const int q0 = qsl[r];
+                for (int i = 0; i < rp.q; ++i)
+                    stoks[sbase + i] = make_int4(q0 + i, pbase + i * p.num_q_heads * nsplit, nsplit, 0);
+                pbase += rp.q * p.num_q_heads * nsplit;
+                sbase += rp.q;
+            }
         }
     }
     __syncthreads();
@@ -445,7 +474,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     for (int c = tid; c < n_emit; c += nthr) {
         const int r = owner(c);
         const int4 ri = req[r];
-        const ReqPlan rp = plan_request(p, r, pps, is_cascade(ri));
+        const ReqPlan rp = plan_request(p, qsl, lens, r, pps, is_cascade(ri));
         const int2 pg = chunk_pages(rp, G, c - ri.z);
         if (rp.mode == 2) agg_inc(pbin_count, min(pg.y, kSizeBins - 1));
         else agg_inc(bin_count, min(pg.y - pg.x, kSizeBins - 1));
@@ -468,7 +497,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         const int r = owner(c);
         const int4 ri = req[r];
         const bool casc = is_cascade(ri);
-        const ReqPlan rp = plan_request(p, r, pps, casc);
+        const ReqPlan rp = plan_request(p, qsl, lens, r, pps, casc);
         const int k = c - ri.z;
         const int2 pg = chunk_pages(rp, G, k);
         if (rp.mode == 2) {
@@ -480,18 +509,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             if (pos < p.lay.max_chunks) chunks[pos] = make_int4(r, k + (casc ? p.lay.prefix_parts : 0), pg.x, pg.y);
         }
     }
-    // token owners, one thread per token: the last request starting at or
-    // before t (requests with no tokens share their start with the next one)
-    for (int t = tid; t < p.num_tokens; t += nthr) {
-        int lo = 0, hi = p.num_seqs - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.qsl[mid] <= t) lo = mid;
-            else hi = mid - 1;
-        }
-        if (p.num_seqs > 0 && p.qsl[lo] <= t && t < p.qsl[lo + 1] && req[lo].x > 0)
-            tok[t] = make_int2(lo, t - p.qsl[lo]);
-    }
+    if (staged)
+        for (int r = tid; r < p.num_seqs; r += nthr) req_ws[r] = s_req[r];
     __syncthreads();
     if (tid == 0) {
         hdr->status = bad ? PKV_ERR_DEVICE_METADATA : PKV_OK;
@@ -502,13 +521,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         hdr->num_seqs = p.num_seqs;
         hdr->pages_per_split = pps;
         hdr->off_req = p.lay.off_req;
-        hdr->off_tok = p.lay.off_tok;
+        hdr->off_stoks = p.lay.off_stoks;
+        hdr->n_split_tokens = fits ? totals.w : 0;
         hdr->off_chunks = p.lay.off_chunks;
         hdr->off_ptiles = p.lay.off_ptiles;
         hdr->off_part_lse = p.lay.off_part_lse;
         hdr->off_part_o = p.lay.off_part_o;
         hdr->off_crows = p.lay.off_crows;
-        hdr->n_crows = fits ? ctotals.x : 0;
+        hdr->n_crows = fits ? totals.z : 0;
         hdr->prefix_blocks = p.prefix_blocks;
         hdr->prefix_parts = p.lay.prefix_parts;
         hdr->next_ptile_item = 0;
@@ -980,60 +1000,62 @@ __global__ void __launch_bounds__(256) combine_kernel(__nv_bfloat16 *out, const 
                                                       int32_t num_q_heads) {
     pdl_wait();       // every partial of the attention kernels is written
     const WsHeader *hdr = reinterpret_cast<const WsHeader *>(ws);
-    if (hdr->magic != kMagic || hdr->num_tokens != num_tokens || hdr->num_q_heads != num_q_heads ||
-        hdr->head_size != HD) {
+    // every header field this kernel uses, loaded at once (one round trip)
+    const int magic = hdr->magic, h_tokens = hdr->num_tokens, h_heads = hdr->num_q_heads, h_hd = hdr->head_size;
+    const int n_split = hdr->n_split_tokens;
+    const int64_t off_stoks = hdr->off_stoks, off_lse = hdr->off_part_lse, off_o = hdr->off_part_o;
+    if ((magic != kMagic) | (h_tokens != num_tokens) | (h_heads != num_q_heads) | (h_hd != HD)) {
         if (blockIdx.x == 0 && threadIdx.x == 0)
             set_status(reinterpret_cast<int32_t *>(const_cast<uint8_t *>(ws)), PKV_ERR_PROTOCOL);
         return;
     }
-    const int4 *req = reinterpret_cast<const int4 *>(ws + hdr->off_req);
-    const int2 *tok = reinterpret_cast<const int2 *>(ws + hdr->off_tok);
-    const float *part_lse = reinterpret_cast<const float *>(ws + hdr->off_part_lse);
-    const float *part_o = reinterpret_cast<const float *>(ws + hdr->off_part_o);
+    const int4 *stoks = reinterpret_cast<const int4 *>(ws + off_stoks);
+    const float *part_lse = reinterpret_cast<const float *>(ws + off_lse);
+    const float *part_o = reinterpret_cast<const float *>(ws + off_o);
     const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (row >= static_cast<int64_t>(num_tokens) * num_q_heads) return;
-    const int t = static_cast<int>(row / num_q_heads);
-    const int h = static_cast<int>(row % num_q_heads);
-    const int2 ti = tok[t];
-    if (ti.x < 0) return;
-    const int4 info = req[ti.x];
-    const int n = info.x;
-    if (n <= 1) return;
-    const int64_t base = info.y + (static_cast<int64_t>(ti.y) * num_q_heads + h) * n;
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const float lse = lane < n ? part_lse[base + lane] : NEG_INF;
-    float mx = lse;
+    // one warp per row (split token, q head), grid-strided over the rows
+    const int64_t n_rows = static_cast<int64_t>(n_split) * num_q_heads;
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); row < n_rows;
+         row += static_cast<int64_t>(gridDim.x) * 8) {
+        const int4 st = stoks[row / num_q_heads];      // {token, partial row of q head 0, splits, 0}
+        const int h = static_cast<int>(row % num_q_heads);
+        const int n = st.z;
+        const int64_t base = st.y + static_cast<int64_t>(h) * n;
+        const float lse = lane < n ? part_lse[base + lane] : NEG_INF;
+        float mx = lse;
 #pragma unroll
-    for (int s = 16; s; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-    const float w = (lse == NEG_INF) ? 0.f : __expf(lse - mx);
-    float wsum = w;
+        for (int s = 16; s; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+        const float w = (lse == NEG_INF) ? 0.f : __expf(lse - mx);
+        float wsum = w;
 #pragma unroll
-    for (int s = 16; s; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
-    constexpr int PER = HD / 32;          // dims per lane (2 or 4)
-    float acc[PER];
+        for (int s = 16; s; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
+        constexpr int PER = HD / 32;          // dims per lane (2 or 4)
+        float acc[PER];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    for (int s = 0; s < n; ++s) {
-        const float wt = __shfl_sync(0xffffffffu, w, s);
-        const float *src = part_o + (base + s) * HD + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] += wt * v.x;
-            acc[1] += wt * v.y;
-            acc[2] += wt * v.z;
-            acc[3] += wt * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(src);
-            acc[0] += wt * v.x;
-            acc[1] += wt * v.y;
+        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll 4
+        for (int s = 0; s < n; ++s) {
+            const float wt = __shfl_sync(0xffffffffu, w, s);
+            const float *src = part_o + (base + s) * HD + lane * PER;
+            if constexpr (PER == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                acc[0] += wt * v.x;
+                acc[1] += wt * v.y;
+                acc[2] += wt * v.z;
+                acc[3] += wt * v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                acc[0] += wt * v.x;
+                acc[1] += wt * v.y;
+            }
         }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    __nv_bfloat16 *dst = out + row * HD + lane * PER;
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        __nv_bfloat16 *dst = out + (static_cast<int64_t>(st.x) * num_q_heads + h) * HD + lane * PER;
 #pragma unroll
-    for (int e = 0; e < PER; e += 2)
-        *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+        for (int e = 0; e < PER; e += 2)
+            *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    }
 }
 
 // ---- host side ----------------------------------------------------------------------------
@@ -1302,8 +1324,14 @@ extern "C" int pkv_paged_attn_combine(void *out, const void *workspace, size_t w
     if (workspace_bytes < 256) return PKV_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(out) & 15u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PKV_ERR_ALIGNMENT;
+    // the rows to merge are known on the device only: a grid of at most 8
+    // CTAs per SM strides over them
     const int64_t rows = static_cast<int64_t>(num_tokens) * num_q_heads;
-    const int64_t grid = (rows + 7) / 8;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    const int64_t grid = std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 8);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
     const uint8_t *w = static_cast<const uint8_t *>(workspace);
