@@ -40,18 +40,18 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per algorithmic byte of the attention launch, from
 # the ncu capture summarised in profiles/decode_kernel_llama13b-decode-64req.md
-# (64-request case of the 13B batch: 1.0509 GB of traffic for 1.0339 GB of
+# (64-request case of the 13B batch: 1.0476 GB of traffic for 1.0339 GB of
 # algorithmic bytes).  Traffic grows with the KV bytes read, so the full
 # launch's traffic is this ratio times its algorithmic bytes.  It holds only
-# for the kernel sources it was measured on (hash below); otherwise null.
-DECODE_TRAFFIC = {"sources_sha256_16": "24c226af4f7424a5", "ratio": (1.042311 + 0.005737) / 1.033885,
+# for the decode kernel sources it was measured on (hash below); otherwise null.
+DECODE_TRAFFIC = {"sources_sha256_16": "74d513b3a61752f9", "ratio": (1.042246 + 0.005344) / 1.033885,
                   "profile": "profiles/decode_kernel_llama13b-decode-64req.md"}
 
 
 def decode_sources_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("paged_attn.cu", "pkv_common.cuh"):
+    for f in ("decode.cu", "pkv_common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_111_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -73,6 +73,34 @@ struct PrefillParams {
     uint8_t *ws;
 };
 
+// Parameters of the decode kernel (decode.cu).
+struct AttnParams {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *query;
+    int64_t q_stride;         // elements per token
+    const int32_t *block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t *seq_lens;
+    const int32_t *qsl;
+    int32_t num_q_heads, num_kv_heads, G;
+    int64_t num_blocks;
+    float scale_log2;         // scale * log2(e)
+    float k_scale, v_scale;   // E4M3 cache: stored code * scale is the value (1 for bf16)
+    uint8_t *ws;
+};
+
+// Decode grid: persistent CTAs of kDecodeWarps warps, kDecodeCtasPerSm per SM.
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeCtasPerSm = 2;
+
+// Tensor map of the cache for the decode kernel (bf16 or E4M3 pages).
+int make_decode_map(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                    int32_t head_size, bool kv8);
+// Launch the decode kernel for this head size and cache type (programmatic
+// dependent launch after the plan).
+int launch_decode_path(const CUtensorMap &map, const AttnParams &ap, int32_t head_size, bool kv8, int grid, int dev,
+                       cudaStream_t st);
+
 // The shared-prefix (cascade) pass on the same kernel: rows of every request
 // that shares the first `prefix_blocks` blocks of its table with request 0
 // attend once to those blocks' keys, cut into `prefix_parts` ranges of KV

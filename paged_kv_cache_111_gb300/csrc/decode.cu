@@ -1,0 +1,591 @@
+// Decode kernel of the paged-attention path: split-K and 16-row tiles over
+// a block-table-indexed KV cache (see paged_attn.cu for the plan that lists
+// its chunks and the combine that merges split rows).
+//
+// What is computed ("continuous batching and PagedAttention" tutorial,
+// section 3.6 "PagedAttention kernel"; "vLLM source reading", sections 2.3
+// and 5.1): every query row loops over its request's logical blocks, looks
+// up the physical block in the block table, loads that block's K and V and
+// folds softmax(scale * q.K^T) V into a running (max, sum, accumulator) state.
+//
+// Persistent CTAs of NW warps.  Each warp takes chunks (x kv heads) in a
+// fixed order and streams the chunk's 16-token pages through its own ring of
+// DEPTH shared-memory stages.  A page of one kv head (K then V,
+// 2*16*head_size bf16, contiguous in the cache) arrives by TMA tensor loads
+// with 128-byte swizzle, so ldmatrix reads are free of bank conflicts.
+// S = Q K^T and O += P V run on bf16 mma.sync tiles: rows are the tile's
+// (query token, q head of the group) pairs, so every q head of a GQA group is
+// served by one read of each KV page.
+#include <mutex>
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "attn_internal.cuh"
+
+namespace pkv {
+
+// Shared-memory address of (row, 16-byte chunk) inside one TMA box of
+// 32 rows x 128 bytes written with the 128-byte swizzle: chunk c of row R is
+// stored at chunk position c ^ (R & 7).
+__device__ __forceinline__ uint32_t swz(uint32_t box_base, int row, int chunk) {
+    return box_base + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// KV8 = false: bf16 cache; ring stages hold pages in the 16-bit layout the
+// MMA loads read (128-byte swizzled 64-column boxes).  KV8 = true: E4M3
+// cache; ring stages hold the raw 8-bit page, which the warp widens to f16
+// into a private staging page of the 16-bit layout before the MMAs.
+template <int HD, int NW, int DEPTH, bool KV8>
+struct DecodeCfg {
+    static constexpr int kBoxes = HD / 64;                 // 64-element boxes per row
+    static constexpr int kBoxBytes = 2 * kBlock * 128;     // K and V rows of one box: 4 KiB
+    static constexpr int kPageBytes = kBoxes * kBoxBytes;  // one 16-bit page of one kv head
+    static constexpr int kStageBytes = KV8 ? 2 * kBlock * HD : kPageBytes;
+    static constexpr int kWarpBytes = DEPTH * kStageBytes + (KV8 ? kPageBytes : 0);
+    static constexpr int kSmem = NW * kWarpBytes + NW * DEPTH * 8 + 1024;
+};
+
+// MMA element type of the decode kernel: bf16 for a bf16 cache; f16 for an
+// E4M3 cache (E4M3 widens to f16 exactly in one instruction per pair).
+template <bool F16> struct DecodeMath;
+template <> struct DecodeMath<false> {
+    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+        mma_bf16_16816(d, a, b0, b1);
+    }
+    static __device__ __forceinline__ void split(float x, float y, uint32_t &big, uint32_t &rest) {
+        split_bf16x2(x, y, big, rest);
+    }
+};
+template <> struct DecodeMath<true> {
+    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // (x, y) -> f16x2 pair plus its f16x2 remainder (about 22 bits together)
+    static __device__ __forceinline__ void split(float x, float y, uint32_t &big, uint32_t &rest) {
+        const __half2 b = __floats2half2_rn(x, y);
+        const float2 bf = __half22float2(b);
+        const __half2 r = __floats2half2_rn(x - bf.x, y - bf.y);
+        big = *reinterpret_cast<const uint32_t *>(&b);
+        rest = *reinterpret_cast<const uint32_t *>(&r);
+    }
+};
+
+// Four E4M3 values (one 32-bit word, element 0 in the low byte) -> two f16x2
+// words (elements 0,1 and 2,3; the lower element in the low half).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &h01, uint32_t &h23) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w));
+}
+
+// Widen one raw E4M3 page (linear [2][16][HD] bytes) into the 16-bit staging
+// page: f16 values, 128-byte swizzled 64-column boxes of 32 rows (K rows
+// 0..15, V rows 16..31).  Every lane converts 16-byte pieces.  At HD = 128 a
+// quarter-warp takes two rows, half a row each, in alternating halves, so
+// that both its 8-bit reads and its 16-bit stores hit eight distinct bank
+// groups.
+template <int HD>
+__device__ __forceinline__ void widen_e4m3_page(uint32_t src, uint32_t dst, int lane) {
+    constexpr int kChunks = 2 * kBlock * HD / 16;
+    constexpr int kBoxBytes = 2 * kBlock * 128;
+#pragma unroll
+    for (int q = lane; q < kChunks; q += 32) {
+        int row, col;
+        if constexpr (HD == 128) {
+            const int ph = q >> 3, k = q & 7, sub = k >> 2;
+            row = 2 * (ph >> 1) + sub;
+            col = 16 * (4 * (sub ^ (ph & 1)) + (k & 3));
+        } else {
+            row = (q * 16) / HD;
+            col = (q * 16) % HD;
+        }
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(src + row * HD + col));
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x4(w[i], h[2 * i], h[2 * i + 1]);
+        const uint32_t box = dst + (col / 64) * kBoxBytes;
+        const int ch = (col % 64) / 8;
+        const uint32_t a0 = box + row * 128 + ((ch ^ (row & 7)) << 4);
+        const uint32_t a1 = box + row * 128 + (((ch + 1) ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                     "r"(h[3])
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(h[4]), "r"(h[5]), "r"(h[6]),
+                     "r"(h[7])
+                     : "memory");
+    }
+}
+
+template <int HD, int NW, int DEPTH, bool KV8>
+__global__ void __launch_bounds__(NW * 32, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
+    using Cfg = DecodeCfg<HD, NW, DEPTH, KV8>;
+    using Math = DecodeMath<KV8>;
+    constexpr int KSTEPS = HD / 16;       // k-steps of S = Q K^T
+    constexpr int NTILES = HD / 8;        // n-tiles of O
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t *ring = smem + warp * Cfg::kWarpBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * Cfg::kWarpBytes) + warp * DEPTH;
+    const uint32_t ring_u32 = smem_u32(ring);
+    const uint32_t staging_u32 = ring_u32 + DEPTH * Cfg::kStageBytes;   // KV8 only
+
+    if (lane == 0) {
+        for (int s = 0; s < DEPTH; ++s) mbar_init(&bars[s], 1);
+        if (warp == 0) tma_prefetch_desc(&kv_map);
+    }
+    fence_barrier_init();
+    __syncwarp();
+    pdl_wait();       // the plan (and the cache write before it) are complete
+    pdl_trigger();
+    const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
+    int32_t *status = reinterpret_cast<int32_t *>(p.ws);
+    const int4 *req = reinterpret_cast<const int4 *>(p.ws + hdr->off_req);
+    const int4 *chunks = reinterpret_cast<const int4 *>(p.ws + hdr->off_chunks);
+    float *part_lse = reinterpret_cast<float *>(p.ws + hdr->off_part_lse);
+    float *part_o = reinterpret_cast<float *>(p.ws + hdr->off_part_o);
+    const int n_items = hdr->n_chunks * p.num_kv_heads;
+
+    const int W = gridDim.x * NW;
+    const int wid = blockIdx.x * NW + warp;
+    uint32_t seq = 0;              // pages consumed so far by this warp (ring position)
+    const int g4 = lane >> 2;      // fragment row within 8
+    const int t4 = lane & 3;       // fragment column pair
+    const float NEG_INF = -__int_as_float(0x7f800000);
+
+    for (int round = 0; round * W < n_items; ++round) {
+        const int item = (round & 1) ? round * W + (W - 1 - wid) : round * W + wid;   // snake order
+        if (item >= n_items) continue;
+        const int4 ch = chunks[item / p.num_kv_heads];
+        const int g = item % p.num_kv_heads;
+        const int r = ch.x;
+        const int pb = ch.z;
+        const int npages = ch.w - ch.z;
+        const int L = p.seq_lens[r];
+        const int qs = p.qsl[r];
+        const int qlen = p.qsl[r + 1] - qs;
+        const int ctx = L - qlen;
+        const int rows_total = qlen * p.G;
+        const bool split_mode = rows_total <= 16;
+        const int tile = split_mode ? 0 : ch.y;
+        const int split = split_mode ? ch.y : 0;
+        const int4 info = req[r];
+        const int n_split = split_mode ? info.x : 1;
+        const int rows = min(16, rows_total - 16 * tile);
+
+        // this thread's two fragment rows
+        const int R0 = g4, R1 = g4 + 8;
+        const int i0 = (16 * tile + R0) / p.G, hh0 = (16 * tile + R0) % p.G;
+        const int i1 = (16 * tile + R1) / p.G, hh1 = (16 * tile + R1) % p.G;
+        const int lim0 = R0 < rows ? ctx + i0 + 1 : 0;      // keys [0, lim) visible
+        const int lim1 = R1 < rows ? ctx + i1 + 1 : 0;
+
+        // block-table window: lane l holds the block of page (wbase + l)
+        const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks_per_seq + pb;
+        int wbase = 0;
+        int win = lane < npages ? __ldg(bt + lane) : -1;
+
+        auto issue = [&](int k) {            // page k of this chunk -> its ring stage
+            const int blk = __shfl_sync(0xffffffffu, win, k - wbase);
+            if (lane == 0) {
+                if (blk < 0 || blk >= p.num_blocks) set_status(status, PKV_ERR_DEVICE_INDEX);
+                const uint32_t st = (seq + k) % DEPTH;
+                uint8_t *dst = ring + st * Cfg::kStageBytes;
+                mbar_arrive_expect_tx(&bars[st], Cfg::kStageBytes);
+                if constexpr (KV8) {
+                    tma_load_5d(dst, &kv_map, &bars[st], 0, 0, 0, g, blk);       // the whole 8-bit page
+                } else {
+#pragma unroll
+                    for (int bx = 0; bx < Cfg::kBoxes; ++bx)
+                        tma_load_5d(dst + bx * Cfg::kBoxBytes, &kv_map, &bars[st], bx * 64, 0, 0, g, blk);
+                }
+            }
+        };
+        int issued = min(DEPTH, npages);
+        for (int k = 0; k < issued; ++k) issue(k);
+
+        // Q fragments (A operand, rows = (query token, q head) pairs)
+        uint32_t qf[KSTEPS][4];
+        {
+            const __nv_bfloat16 *q0p = p.query + static_cast<int64_t>(qs + i0) * p.q_stride +
+                                       static_cast<int64_t>(g * p.G + hh0) * HD;
+            const __nv_bfloat16 *q1p = p.query + static_cast<int64_t>(qs + i1) * p.q_stride +
+                                       static_cast<int64_t>(g * p.G + hh1) * HD;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int c = kk * 16 + 2 * t4;
+                qf[kk][0] = R0 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q0p + c)) : 0u;
+                qf[kk][1] = R1 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q1p + c)) : 0u;
+                qf[kk][2] = R0 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q0p + c + 8)) : 0u;
+                qf[kk][3] = R1 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q1p + c + 8)) : 0u;
+            }
+        }
+        // score factors of the two rows (log2 domain); for an E4M3 cache each
+        // Q row is scaled by a power of two 2^e into [2^14, 2^15) before it is
+        // rounded to f16 (exact but for parts below 2^-24 of the row's
+        // largest), and 2^-e and k_scale go into the factor
+        float sf0 = p.scale_log2, sf1 = p.scale_log2;
+        if constexpr (KV8) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                a0 = fmaxf(a0, fmaxf(fmaxf(fabsf(__uint_as_float(qf[kk][0] << 16)),
+                                           fabsf(__uint_as_float(qf[kk][0] & 0xFFFF0000u))),
+                                     fmaxf(fabsf(__uint_as_float(qf[kk][2] << 16)),
+                                           fabsf(__uint_as_float(qf[kk][2] & 0xFFFF0000u)))));
+                a1 = fmaxf(a1, fmaxf(fmaxf(fabsf(__uint_as_float(qf[kk][1] << 16)),
+                                           fabsf(__uint_as_float(qf[kk][1] & 0xFFFF0000u))),
+                                     fmaxf(fabsf(__uint_as_float(qf[kk][3] << 16)),
+                                           fabsf(__uint_as_float(qf[kk][3] & 0xFFFF0000u)))));
+            }
+            a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 1));
+            a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, 2));
+            a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+            a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 2));
+            // e = 14 - floor(log2 a), held in [-114, 126] so 2^e and 2^-e are normal
+            const int e0 = a0 > 0.f ? min(126, max(-114, 14 - ilogbf(a0))) : 0;
+            const int e1 = a1 > 0.f ? min(126, max(-114, 14 - ilogbf(a1))) : 0;
+            const float u0 = __int_as_float((e0 + 127) << 23), u1 = __int_as_float((e1 + 127) << 23);
+            auto to_f16 = [](uint32_t bf2, float u) {
+                const __half2 h = __floats2half2_rn(__uint_as_float(bf2 << 16) * u,
+                                                    __uint_as_float(bf2 & 0xFFFF0000u) * u);
+                return *reinterpret_cast<const uint32_t *>(&h);
+            };
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                qf[kk][0] = to_f16(qf[kk][0], u0);
+                qf[kk][1] = to_f16(qf[kk][1], u1);
+                qf[kk][2] = to_f16(qf[kk][2], u0);
+                qf[kk][3] = to_f16(qf[kk][3], u1);
+            }
+            sf0 = p.scale_log2 * p.k_scale * __int_as_float((127 - e0) << 23);
+            sf1 = p.scale_log2 * p.k_scale * __int_as_float((127 - e1) << 23);
+        }
+
+        float o[NTILES][4];
+#pragma unroll
+        for (int n = 0; n < NTILES; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+        int failed_at = -1;
+
+        for (int k = 0; k < npages; ++k) {
+            const uint32_t st = (seq + k) % DEPTH;
+            const uint32_t par = ((seq + k) / DEPTH) & 1u;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[st], par));
+            if (!ok) {
+                failed_at = k;
+                break;
+            }
+            uint32_t page = ring_u32 + st * Cfg::kStageBytes;
+            const int j0 = (pb + k) * kBlock;       // first key of this page
+            if constexpr (KV8) {
+                // widen the 8-bit page, then hand its stage back to the copy engine
+                widen_e4m3_page<HD>(page, staging_u32, lane);
+                page = staging_u32;
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int nk = k + DEPTH;
+                if (nk < npages) {
+                    if (nk - wbase >= 32) {
+                        wbase += 32;
+                        win = wbase + lane < npages ? __ldg(bt + wbase + lane) : -1;
+                    }
+                    issue(nk);
+                    ++issued;
+                }
+            }
+
+            // zero V rows past the end of the sequence (last page only)
+            if (j0 + kBlock > L) {
+                const int vfirst = L - j0;
+                const int nrows = kBlock - vfirst;
+                for (int e = lane; e < Cfg::kBoxes * nrows * 8; e += 32) {
+                    const int bx = e / (nrows * 8);
+                    const int rem = e % (nrows * 8);
+                    const int row = kBlock + vfirst + rem / 8;
+                    const int chunk = rem % 8;
+                    const uint32_t a = swz(page + bx * Cfg::kBoxBytes, row, chunk);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                }
+                __syncwarp();
+            }
+
+            // S = Q K^T for the page's 16 tokens (two n-tiles)
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int bx = kk / 4;
+                const int tok = ((lane >> 4) << 3) + (lane & 7);
+                const int chunk = (kk % 4) * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(swz(page + bx * Cfg::kBoxBytes, tok, chunk), b0, b1, b2, b3);
+                Math::mma(s0, qf[kk], b0, b1);
+                Math::mma(s1, qf[kk], b2, b3);
+            }
+
+            // online softmax in the log2 domain; keys a row may not see get -inf
+            const int c0 = j0 + 2 * t4, c1 = c0 + 1, c8 = c0 + 8, c9 = c0 + 9;
+            float x[8];
+            x[0] = c0 < lim0 ? s0[0] * sf0 : NEG_INF;
+            x[1] = c1 < lim0 ? s0[1] * sf0 : NEG_INF;
+            x[2] = c0 < lim1 ? s0[2] * sf1 : NEG_INF;
+            x[3] = c1 < lim1 ? s0[3] * sf1 : NEG_INF;
+            x[4] = c8 < lim0 ? s1[0] * sf0 : NEG_INF;
+            x[5] = c9 < lim0 ? s1[1] * sf0 : NEG_INF;
+            x[6] = c8 < lim1 ? s1[2] * sf1 : NEG_INF;
+            x[7] = c9 < lim1 ? s1[3] * sf1 : NEG_INF;
+            float mx0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[4], x[5]));
+            float mx1 = fmaxf(fmaxf(x[2], x[3]), fmaxf(x[6], x[7]));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            // a row's reference maximum moves only on its first visible key or
+            // when the page's maximum exceeds it by more than 2^8, so weights
+            // stay below 2^8 and O is rescaled (warp-uniformly) only then
+            const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;
+            if (__any_sync(0xffffffffu, up0 || up1)) {
+                const float a0 = up0 ? fast_exp2(m0 - mx0) : 1.f;   // 0 when m = -inf
+                const float a1 = up1 ? fast_exp2(m1 - mx1) : 1.f;
+                m0 = up0 ? mx0 : m0;
+                m1 = up1 ? mx1 : m1;
+                l0 *= a0;
+                l1 *= a1;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a0;
+                    o[n][2] *= a1;
+                    o[n][3] *= a1;
+                }
+            }
+            const float ref0 = m0 == NEG_INF ? 0.f : m0;
+            const float ref1 = m1 == NEG_INF ? 0.f : m1;
+            float pr[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pr[e] = fast_exp2(x[e] - (((e >> 1) & 1) ? ref1 : ref0));
+            l0 += (pr[0] + pr[1] + pr[4] + pr[5]);
+            l1 += (pr[2] + pr[3] + pr[6] + pr[7]);
+            // P as a 16-bit pair (hi + remainder): the PV product keeps about
+            // 16 bits (bf16) or 22 bits (f16) of each weight
+            uint32_t pa[4], pl[4];
+            Math::split(pr[0], pr[1], pa[0], pl[0]);
+            Math::split(pr[2], pr[3], pa[1], pl[1]);
+            Math::split(pr[4], pr[5], pa[2], pl[2]);
+            Math::split(pr[6], pr[7], pa[3], pl[3]);
+
+            // O += P V (V rows are the page's tokens, read transposed)
+#pragma unroll
+            for (int n = 0; n < NTILES; n += 2) {
+                const int bx = n / 8;
+                const int tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int chunk = (n % 8) + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(swz(page + bx * Cfg::kBoxBytes, kBlock + tok, chunk), b0, b1, b2, b3);
+                Math::mma(o[n], pa, b0, b1);
+                Math::mma(o[n + 1], pa, b2, b3);
+                Math::mma(o[n], pl, b0, b1);
+                Math::mma(o[n + 1], pl, b2, b3);
+            }
+
+            if constexpr (!KV8) {
+                // refill this stage with page k + DEPTH of the chunk
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int nk = k + DEPTH;
+                if (nk < npages) {
+                    if (nk - wbase >= 32) {
+                        wbase += 32;
+                        win = wbase + lane < npages ? __ldg(bt + wbase + lane) : -1;
+                    }
+                    issue(nk);
+                    ++issued;
+                }
+            } else {
+                __syncwarp();                    // the staging page is rewritten by the next page
+            }
+        }
+
+        if (failed_at >= 0) {
+            set_status(status, PKV_ERR_DEVICE_TIMEOUT);
+            // let copies already in flight land before the CTA's memory is released
+            for (int k = failed_at; k < issued; ++k) {
+                const uint32_t st = (seq + k) % DEPTH;
+                mbar_wait_bounded(&bars[st], ((seq + k) / DEPTH) & 1u);
+            }
+            return;
+        }
+        seq += npages;
+
+        // finish the rows: quad sums of l, then normalise
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        // (an E4M3 cache's V values are code * v_scale: the scale is applied once here)
+        const float inv0 = l0 > 0.f ? (KV8 ? p.v_scale / l0 : 1.f / l0) : 0.f;
+        const float inv1 = l1 > 0.f ? (KV8 ? p.v_scale / l1 : 1.f / l1) : 0.f;
+        const int h0 = g * p.G + hh0, h1 = g * p.G + hh1;
+        if (n_split <= 1) {
+            if (R0 < rows) {
+                __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(qs + i0) * p.num_q_heads + h0) * HD;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n)
+                    *reinterpret_cast<uint32_t *>(dst + n * 8 + 2 * t4) = pack_bf16x2(o[n][0] * inv0, o[n][1] * inv0);
+            }
+            if (R1 < rows) {
+                __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(qs + i1) * p.num_q_heads + h1) * HD;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n)
+                    *reinterpret_cast<uint32_t *>(dst + n * 8 + 2 * t4) = pack_bf16x2(o[n][2] * inv1, o[n][3] * inv1);
+            }
+        } else {
+            const float LN2 = 0.69314718055994531f;
+            if (R0 < rows) {
+                const int64_t prow = info.y + (static_cast<int64_t>(i0) * p.num_q_heads + h0) * n_split + split;
+                float *dst = part_o + prow * HD;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n)
+                    *reinterpret_cast<float2 *>(dst + n * 8 + 2 * t4) = make_float2(o[n][0] * inv0, o[n][1] * inv0);
+                if (t4 == 0) part_lse[prow] = l0 > 0.f ? (m0 + __log2f(l0)) * LN2 : NEG_INF;
+            }
+            if (R1 < rows) {
+                const int64_t prow = info.y + (static_cast<int64_t>(i1) * p.num_q_heads + h1) * n_split + split;
+                float *dst = part_o + prow * HD;
+#pragma unroll
+                for (int n = 0; n < NTILES; ++n)
+                    *reinterpret_cast<float2 *>(dst + n * 8 + 2 * t4) = make_float2(o[n][2] * inv1, o[n][3] * inv1);
+                if (t4 == 0) part_lse[prow] = l1 > 0.f ? (m1 + __log2f(l1)) * LN2 : NEG_INF;
+            }
+        }
+    }
+}
+
+// ---- host side --------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Tensor map of the cache as a 5-D bf16 tensor {head_size, 16, 2, Hkv, num_blocks}
+// (innermost first), loaded in boxes of {64, 16, 2, 1, 1} with 128-byte swizzle.
+static int make_kv_map(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t head_size) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return PKV_ERR_CUDA;
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2,
+                                static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t row = static_cast<cuuint64_t>(head_size) * 2;
+    const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * num_kv_heads};
+    const cuuint32_t box[5] = {64, kBlock, 2, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult rc = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Tensor map of an E4M3 cache as a 5-D byte tensor {head_size, 16, 2, Hkv,
+// num_blocks}; one box is a whole page of one kv head (K and V rows, 2*16*d
+// bytes), unswizzled: the kernel widens it to f16 itself.
+static int make_kv_map_e4m3(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                            int32_t head_size) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return PKV_ERR_CUDA;
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2,
+                                static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t row = static_cast<cuuint64_t>(head_size);
+    const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * num_kv_heads};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(head_size), kBlock, 2, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult rc = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(kv_cache), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+template <int HD, int NW, int DEPTH, bool KV8>
+static int launch_decode(const CUtensorMap &map, const AttnParams &p, int grid, int dev, cudaStream_t stream) {
+    using Cfg = DecodeCfg<HD, NW, DEPTH, KV8>;
+    static std::mutex mu;
+    static uint64_t done_mask = 0;       // devices whose shared-memory limit is already raised
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+        if (!bit || !(done_mask & bit)) {
+            if (cudaFuncSetAttribute(decode_kernel<HD, NW, DEPTH, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::kSmem) != cudaSuccess)
+                return PKV_ERR_CUDA;
+            done_mask |= bit;
+        }
+    }
+    if (launch_pdl(decode_kernel<HD, NW, DEPTH, KV8>, dim3(grid), dim3(NW * 32), Cfg::kSmem, stream, map, p) !=
+        cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+// decode tiling per head size: warps per CTA, ring stages per warp, CTAs per SM
+template <int HD, bool KV8 = false> struct DecodeTiling;
+template <> struct DecodeTiling<64> { static constexpr int NW = 4, DEPTH = 6, CTAS_PER_SM = 2; };
+template <> struct DecodeTiling<128> { static constexpr int NW = 4, DEPTH = 3, CTAS_PER_SM = 2; };
+// E4M3 pages are half the bytes: more stages in flight, plus one staging page per warp
+template <> struct DecodeTiling<64, true> { static constexpr int NW = 4, DEPTH = 8, CTAS_PER_SM = 2; };
+template <> struct DecodeTiling<128, true> { static constexpr int NW = 4, DEPTH = 4, CTAS_PER_SM = 2; };
+
+
+static_assert(DecodeTiling<64>::NW == kDecodeWarps && DecodeTiling<128>::NW == kDecodeWarps &&
+                  DecodeTiling<64, true>::NW == kDecodeWarps && DecodeTiling<128, true>::NW == kDecodeWarps,
+              "every decode tiling has kDecodeWarps warps per CTA");
+static_assert(DecodeTiling<64>::CTAS_PER_SM == kDecodeCtasPerSm && DecodeTiling<128>::CTAS_PER_SM == kDecodeCtasPerSm,
+              "bf16 decode tilings fit kDecodeCtasPerSm CTAs per SM");
+
+int make_decode_map(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                    int32_t head_size, bool kv8) {
+    return kv8 ? make_kv_map_e4m3(map, kv_cache, num_blocks, num_kv_heads, head_size)
+               : make_kv_map(map, kv_cache, num_blocks, num_kv_heads, head_size);
+}
+
+int launch_decode_path(const CUtensorMap &map, const AttnParams &ap, int32_t head_size, bool kv8, int grid, int dev,
+                       cudaStream_t st) {
+    if (kv8) {
+        using T64 = DecodeTiling<64, true>;
+        using T128 = DecodeTiling<128, true>;
+        return head_size == 64 ? launch_decode<64, T64::NW, T64::DEPTH, true>(map, ap, grid, dev, st)
+                               : launch_decode<128, T128::NW, T128::DEPTH, true>(map, ap, grid, dev, st);
+    }
+    using T64 = DecodeTiling<64>;
+    using T128 = DecodeTiling<128>;
+    return head_size == 64 ? launch_decode<64, T64::NW, T64::DEPTH, false>(map, ap, grid, dev, st)
+                           : launch_decode<128, T128::NW, T128::DEPTH, false>(map, ap, grid, dev, st);
+}
+
+}  // namespace pkv
