@@ -19,6 +19,9 @@ from tolerance import check_close
 pytestmark = pytest.mark.gpu
 
 
+_last_workspace = [None]
+
+
 def run_cascade(step, prefix_blocks, num_splits=0):
     dev = to_dev(step)
     pool = new_pool(step)
@@ -36,6 +39,7 @@ def run_cascade(step, prefix_blocks, num_splits=0):
     pkv.paged_attn_combine(out, ws)
     torch.cuda.synchronize()
     assert pkv.workspace_status(ws) == 0
+    _last_workspace[0] = ws
     return out
 
 
@@ -96,3 +100,20 @@ def test_cascade_with_forced_suffix_splits(splits):
     out = run_cascade(step, 64, num_splits=splits)
     _, ref, _ = oracle.run_step(step)
     check_close(out, ref, f"cascade splits={splits}")
+
+
+def test_cascade_pass_with_more_items_than_ctas():
+    # 1024 sharers with 1 or 2 query tokens x G = 8: 12288 rows per kv head,
+    # 96 row tiles x 4 kv heads = 384 cascade items (one prefix range), more
+    # than one per persistent CTA
+    rng = torch.Generator().manual_seed(65)
+    ctx = (256 + torch.randint(0, 48, (1024,), generator=rng)).tolist()
+    q = (1 + (torch.arange(1024) % 2)).tolist()
+    specs = [wl.RequestSpec(int(c), int(n)) for c, n in zip(ctx, q)]
+    step = wl.build_step("many", specs, 32, 4, 128, 8192, 65, shared_prefix_len=256)
+    out = run_cascade(step, 16)
+    _, px = pkv.workspace_schedule(_last_workspace[0])
+    assert sum(px) == 384 and len(px) == min(384, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert min(px) >= 1
+    _, ref, _ = oracle.run_step(step)
+    check_close(out, ref, "cascade, 384 items")
