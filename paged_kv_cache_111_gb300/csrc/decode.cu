@@ -86,19 +86,21 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &h01, uint3
         : "r"(w));
 }
 
-// Widen one raw E4M3 page (linear [2][16][HD] bytes) into the 16-bit staging
-// page: f16 values, 128-byte swizzled 64-column boxes of 32 rows (K rows
-// 0..15, V rows 16..31).  Every lane converts 16-byte pieces.  At HD = 128 a
-// quarter-warp takes two rows, half a row each, in alternating halves, so
-// that both its 8-bit reads and its 16-bit stores hit eight distinct bank
-// groups.
+// Widen the V rows of one raw E4M3 page (linear [2][16][HD] bytes) into the
+// 16-bit staging page: f16 values, 128-byte swizzled 64-column boxes of 32
+// rows (V rows 16..31; K is read from the raw page directly).  Every lane
+// converts 16-byte pieces, loading all of its pieces before converting any.
+// At HD = 128 a quarter-warp takes two rows, half a row each, in alternating
+// halves, so that both its 8-bit reads and its 16-bit stores hit eight
+// distinct bank groups.
 template <int HD>
-__device__ __forceinline__ void widen_e4m3_page(uint32_t src, uint32_t dst, int lane) {
-    constexpr int kChunks = 2 * kBlock * HD / 16;
+__device__ __forceinline__ void widen_e4m3_values(uint32_t src, uint32_t dst, int lane) {
+    constexpr int kChunks = 2 * kBlock * HD / 16;          // pieces of the page (K and V)
+    constexpr int kFirst = kChunks / 2;                    // the V rows' pieces
+    constexpr int kPerLane = (kChunks - kFirst) / 32;      // 2 or 4
     constexpr int kBoxBytes = 2 * kBlock * 128;
-#pragma unroll
-    for (int q = lane; q < kChunks; q += 32) {
-        int row, col;
+    static_assert(kChunks % 64 == 0, "whole V pieces per lane");
+    auto piece = [&](int q, int &row, int &col) {
         if constexpr (HD == 128) {
             const int ph = q >> 3, k = q & 7, sub = k >> 2;
             row = 2 * (ph >> 1) + sub;
@@ -107,13 +109,23 @@ __device__ __forceinline__ void widen_e4m3_page(uint32_t src, uint32_t dst, int 
             row = (q * 16) / HD;
             col = (q * 16) % HD;
         }
-        uint32_t w[4];
+    };
+    uint32_t w[kPerLane][4];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        int row, col;
+        piece(kFirst + lane + 32 * i, row, col);
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "=r"(w[i][0]), "=r"(w[i][1]), "=r"(w[i][2]), "=r"(w[i][3])
                      : "r"(src + row * HD + col));
+    }
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        int row, col;
+        piece(kFirst + lane + 32 * i, row, col);
         uint32_t h[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) e4m3x4_to_f16x4(w[i], h[2 * i], h[2 * i + 1]);
+        for (int e = 0; e < 4; ++e) e4m3x4_to_f16x4(w[i][e], h[2 * e], h[2 * e + 1]);
         const uint32_t box = dst + (col / 64) * kBoxBytes;
         const int ch = (col % 64) / 8;
         const uint32_t a0 = box + row * 128 + ((ch ^ (row & 7)) << 4);
@@ -225,13 +237,19 @@ __global__ void __launch_bounds__(NW * 32, 1)
                                        static_cast<int64_t>(g * p.G + hh0) * HD;
             const __nv_bfloat16 *q1p = p.query + static_cast<int64_t>(qs + i1) * p.q_stride +
                                        static_cast<int64_t>(g * p.G + hh1) * HD;
+            // E4M3 cache: the head dimension is permuted, the same way for Q and
+            // K (a dot product does not depend on the order of its terms): in
+            // k-step kk, lane column t4 takes dims t4 * HD/4 + 4 kk + 0..3 into
+            // its k slots (2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9), so that its K
+            // values for one key are HD/4 contiguous bytes of the raw page
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int c = kk * 16 + 2 * t4;
+                const int c = KV8 ? t4 * (HD / 4) + 4 * kk : kk * 16 + 2 * t4;
+                const int c2 = KV8 ? c + 2 : c + 8;
                 qf[kk][0] = R0 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q0p + c)) : 0u;
                 qf[kk][1] = R1 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q1p + c)) : 0u;
-                qf[kk][2] = R0 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q0p + c + 8)) : 0u;
-                qf[kk][3] = R1 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q1p + c + 8)) : 0u;
+                qf[kk][2] = R0 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q0p + c2)) : 0u;
+                qf[kk][3] = R1 < rows ? __ldg(reinterpret_cast<const uint32_t *>(q1p + c2)) : 0u;
             }
         }
         // score factors of the two rows (log2 domain); for an E4M3 cache each
@@ -292,9 +310,20 @@ __global__ void __launch_bounds__(NW * 32, 1)
             }
             uint32_t page = ring_u32 + st * Cfg::kStageBytes;
             const int j0 = (pb + k) * kBlock;       // first key of this page
+            // E4M3: this lane's K bytes of keys g4 and 8 + g4 (HD/4 each, see the Q
+            // fragments), straight from the raw page
+            uint32_t kraw[2][KV8 ? KSTEPS : 1];
             if constexpr (KV8) {
-                // widen the 8-bit page, then hand its stage back to the copy engine
-                widen_e4m3_page<HD>(page, staging_u32, lane);
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int v = 0; v < KSTEPS / 4; ++v)
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(kraw[n][4 * v]), "=r"(kraw[n][4 * v + 1]), "=r"(kraw[n][4 * v + 2]),
+                                       "=r"(kraw[n][4 * v + 3])
+                                     : "r"(page + (8 * n + g4) * HD + t4 * (HD / 4) + 16 * v));
+                // widen the V rows, then hand the stage back to the copy engine
+                widen_e4m3_values<HD>(page, staging_u32, lane);
                 page = staging_u32;
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -328,11 +357,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int bx = kk / 4;
-                const int tok = ((lane >> 4) << 3) + (lane & 7);
-                const int chunk = (kk % 4) * 2 + ((lane >> 3) & 1);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4(swz(page + bx * Cfg::kBoxBytes, tok, chunk), b0, b1, b2, b3);
+                if constexpr (KV8) {
+                    e4m3x4_to_f16x4(kraw[0][kk], b0, b1);
+                    e4m3x4_to_f16x4(kraw[1][kk], b2, b3);
+                } else {
+                    const int bx = kk / 4;
+                    const int tok = ((lane >> 4) << 3) + (lane & 7);
+                    const int chunk = (kk % 4) * 2 + ((lane >> 3) & 1);
+                    ldsm_x4(swz(page + bx * Cfg::kBoxBytes, tok, chunk), b0, b1, b2, b3);
+                }
                 Math::mma(s0, qf[kk], b0, b1);
                 Math::mma(s1, qf[kk], b2, b3);
             }
