@@ -40,11 +40,11 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per algorithmic byte of the attention launch, from
 # the ncu capture summarised in profiles/decode_kernel_llama13b-decode-64req.md
-# (64-request case of the 13B batch: 1.0476 GB of traffic for 1.0339 GB of
+# (64-request case of the 13B batch: 1.0477 GB of traffic for 1.0339 GB of
 # algorithmic bytes).  Traffic grows with the KV bytes read, so the full
 # launch's traffic is this ratio times its algorithmic bytes.  It holds only
 # for the decode kernel sources it was measured on (hash below); otherwise null.
-DECODE_TRAFFIC = {"sources_sha256_16": "74d513b3a61752f9", "ratio": (1.042246 + 0.005344) / 1.033885,
+DECODE_TRAFFIC = {"sources_sha256_16": "2b46f5464a4c797a", "ratio": (1.042254 + 0.005473) / 1.033885,
                   "profile": "profiles/decode_kernel_llama13b-decode-64req.md"}
 
 
@@ -273,17 +273,19 @@ def run_gpu(args, rank: int, world: int) -> dict:
         else:
             pkv.paged_attn(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, ws)
 
-    def one_step(ev=None):
-        if ev is not None:
+    def one_step(ev=(None, None, None, None)):
+        """kv_write, paged_attn, combine; ev[k] (if not None) is recorded before
+        call k and ev[3] after the last."""
+        if ev[0] is not None:
             ev[0].record(stream)
         write(to["key"], to["value"], to["slot_mapping"])
-        if ev is not None:
+        if ev[1] is not None:
             ev[1].record(stream)
         attention(to["query"], to["block_tables"], to["seq_lens"], to["query_start_loc"])
-        if ev is not None:
+        if ev[2] is not None:
             ev[2].record(stream)
         pkv.paged_attn_combine(out, ws)
-        if ev is not None:
+        if ev[3] is not None:
             ev[3].record(stream)
 
     for _ in range(args.warmup):
@@ -304,32 +306,73 @@ def run_gpu(args, rank: int, world: int) -> dict:
         torch.cuda.synchronize(dev)
         stream = torch.cuda.current_stream(dev)
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clk:
-        start.record(stream)
-        for i in range(args.steps):
-            if graph is not None:
-                graph.replay()
-            else:
-                one_step(events[i])
-        stop.record(stream)
+    # Inputs that fit in L2 would stay cached from one step to the next: for
+    # such workloads every timed step starts from a cold L2 (a buffer of twice
+    # the L2 size is written, then another one read, so that no dirty line of
+    # the flush is written back during the step), and steps are timed one by
+    # one with events around each step only.
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20))
+    ab_step = algorithmic_bytes(step, 1 if fp8 else 2)
+    flush = ab_step["kv_unique"] <= 2 * l2_bytes
+    flush_bufs = None
+    if flush:
+        n = (2 * l2_bytes + 3) // 4
+        flush_bufs = (torch.empty(n, dtype=torch.float32, device=dev), torch.ones(n, dtype=torch.float32, device=dev))
+        flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def cold_l2():
+        flush_bufs[0].fill_(0.0)
+        torch.sum(flush_bufs[1], dim=0, out=flush_sink)
+
+    def run_steps(n_steps, phase_events):
+        """Time n_steps steps on the device; returns (mean ms per step, phase ms or None)."""
+        if world > 1:
+            torch.distributed.barrier()
         torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = start.elapsed_time(stop)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4 if phase_events else 2)]
+              for _ in range(n_steps if (flush or phase_events) else 1)]
+        if flush or phase_events:
+            for i in range(n_steps):
+                if flush:
+                    cold_l2()
+                e = ev[i]
+                if graph is not None:
+                    e[0].record(stream)
+                    graph.replay()
+                    e[-1].record(stream)
+                else:
+                    one_step(e if phase_events else (e[0], None, None, e[1]))
+            torch.cuda.synchronize(dev)
+            per = [e[0].elapsed_time(e[-1]) for e in ev]
+            mean = sum(per) / n_steps
+        else:
+            ev[0][0].record(stream)
+            for _ in range(n_steps):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    one_step()
+            ev[0][1].record(stream)
+            torch.cuda.synchronize(dev)
+            mean = ev[0][0].elapsed_time(ev[0][1]) / n_steps
+        if world > 1:
+            torch.distributed.barrier()
+        phases = None
+        if phase_events and graph is None:
+            phases = tuple(sum(e[k].elapsed_time(e[k + 1]) for e in ev) / n_steps for k in range(3))
+        return mean, phases
+
+    # the headline: steps back to back (no event between the kernels of a step)
+    with ClockSampler(dev.index) as clk:
+        step_ms, _ = run_steps(args.steps, False)
+    total_ms = step_ms * args.steps
+    # the phase breakdown (kv_write, paged_attn, combine), events between the calls
     if graph is None:
-        kvw_ms = sum(e[0].elapsed_time(e[1]) for e in events) / args.steps
-        attn_ms = sum(e[1].elapsed_time(e[2]) for e in events) / args.steps
-        comb_ms = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps
+        _, (kvw_ms, attn_ms, comb_ms) = run_steps(min(args.steps, 300), True)
     else:
         # one graph per step: the phases are not separable; attribute the step
         kvw_ms = comb_ms = float("nan")
-        attn_ms = total_ms / args.steps
+        attn_ms = step_ms
     status = pkv.workspace_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {pkv.STATUS_NAMES.get(status, status)}")
@@ -358,14 +401,25 @@ def run_gpu(args, rank: int, world: int) -> dict:
         torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        if flush:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(e2e_steps)]
+            for e0, e1 in ev:
+                cold_l2()
+                e0.record(stream)
+                e2e_step()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            e2e_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / e2e_steps
+        else:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     # ---- same-run copy probe (device-to-device copy, read + write bytes) ------
     probe_gbs = None
@@ -388,7 +442,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
     return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K, fp8),
             "fp8_scales": scales,
             "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
-            "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "probe_gbs": probe_gbs}
+            "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "probe_gbs": probe_gbs,
+            "l2_flush": flush, "l2_bytes": l2_bytes}
 
 
 # ---------------------------------------------------------------------------
@@ -582,8 +637,11 @@ def main():
             "physical_blocks": "in order" if args.contiguous_blocks else "random permutation",
             "kv_cache": (f"e4m3, k_scale {r['fp8_scales'][0]:.6g}, v_scale {r['fp8_scales'][1]:.6g}"
                          if fp8 else "bf16"),
-            "l2": "inputs larger than L2 (KV read per step above 129 MB), no flush"
-            if ab["kv_unique"] > 129e6 else "inputs fit in L2; no flush (small workload)",
+            "l2": (f"flushed before every timed step (write then read {2 * r['l2_bytes'] >> 20} MiB); "
+                   f"steps timed one by one" if r["l2_flush"] else
+                   f"inputs larger than L2 ({ab['kv_unique'] / 1e6:.0f} MB of KV per step, L2 "
+                   f"{r['l2_bytes'] / 1e6:.0f} MB), no flush; steps back to back"),
+            "phases": "kv_write / paged_attn / combine from a separate pass with events between the calls",
         },
         "pct_of_peak": value / pk["hbm_gbs"],
         "tokens_per_s": world * step.num_tokens / (ms_per_step * 1e-3),

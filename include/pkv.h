@@ -36,6 +36,14 @@
  *    lengths, a bounded wait that ran out) are written to a device status
  *    word (see each call); the host reads it after synchronising.
  *  - Block size is fixed at 16 tokens.  Head size is 64 or 128.
+ *  - The attention calls launch their first kernel with programmatic
+ *    dependent launch: it may start while the kernel just before it on the
+ *    stream (normally pkv_kv_write) is still running, and it reads
+ *    seq_lens, query_start_loc and block_tables at once.  Work of any
+ *    ordinary kind before the call (copies, memsets, kernels launched
+ *    without programmatic dependent launch) is complete by then.  A
+ *    caller's own kernel that releases its dependents early
+ *    (griddepcontrol.launch_dependents) must write that metadata first.
  *
  * KV cache layout (this library's own, not the one printed on the pages):
  *     bf16 kv_cache[num_blocks][num_kv_heads][2][16][head_size]

@@ -316,10 +316,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int G = p.num_q_heads / p.num_kv_heads;
-    pdl_wait();       // the previous kernel on the stream may still read this workspace
     pdl_trigger();
-
+    // The kernel before this one on the stream (normally the cache write,
+    // which touches neither the metadata nor the workspace) may still run.
+    // A batch staged in shared memory is read and planned meanwhile; the
+    // wait comes before the first workspace write.  A larger batch keeps
+    // its per-request plans in the workspace and waits first.
     const bool staged = p.num_seqs <= kPlanStagedSeqs;
+    if (!staged) pdl_wait();
     const int *qsl = staged ? s_qsl : p.qsl;
     const int *lens = staged ? s_len : p.seq_lens;
     // {splits (0: refused), partial row base, first chunk, chunks} per request;
@@ -329,7 +333,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         for (int r = tid; r <= p.num_seqs; r += nthr) s_qsl[r] = __ldg(p.qsl + r);
         for (int r = tid; r < p.num_seqs; r += nthr) s_len[r] = __ldg(p.seq_lens + r);
     }
-    for (int i = tid; i < 2 * kStatsCtas; i += nthr) reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[i] = 0;
     for (int i = tid; i < kSizeBins; i += nthr) {
         bin_count[i] = 0;
         pbin_count[i] = 0;
@@ -409,6 +412,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         if (rp.first > 0) my_crows += rp.rows;
     }
     const int4 pre = block_scan4(my_chunks, my_prows, my_crows, my_stoks, warp_tot, &totals);
+    if (staged) pdl_wait();       // the previous kernel on the stream may still read this workspace
+    for (int i = tid; i < 2 * kStatsCtas; i += nthr) reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[i] = 0;
     const int n_total = totals.x;
     const bool fits = n_total <= p.lay.max_chunks + p.lay.max_ptiles && totals.y <= p.lay.max_prow &&
                       totals.z <= p.lay.max_crows;
@@ -546,47 +551,68 @@ __global__ void __launch_bounds__(256) combine_kernel(__nv_bfloat16 *out, const 
     const float *part_o = reinterpret_cast<const float *>(ws + off_o);
     const int lane = threadIdx.x & 31;
     const float NEG_INF = -__int_as_float(0x7f800000);
+    constexpr int PER = HD / 32;              // dims per lane (2 or 4)
+    // partial rows loaded per batch, all in flight at once: the merge is a
+    // short chain of dependent loads, so it is bound by their latency
+    constexpr int U = HD == 64 ? 16 : 8;
+    auto load = [&](int64_t prow) -> float4 {
+        const float *src = part_o + prow * HD + lane * PER;
+        if constexpr (PER == 4) {
+            return __ldg(reinterpret_cast<const float4 *>(src));
+        } else {
+            const float2 v = __ldg(reinterpret_cast<const float2 *>(src));
+            return make_float4(v.x, v.y, 0.f, 0.f);
+        }
+    };
     // one warp per row (split token, q head), grid-strided over the rows
     const int64_t n_rows = static_cast<int64_t>(n_split) * num_q_heads;
     for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); row < n_rows;
          row += static_cast<int64_t>(gridDim.x) * 8) {
-        const int4 st = stoks[row / num_q_heads];      // {token, partial row of q head 0, splits, 0}
+        const int4 st = __ldg(stoks + row / num_q_heads);   // {token, partial row of q head 0, splits, 0}
         const int h = static_cast<int>(row % num_q_heads);
         const int n = st.z;
         const int64_t base = st.y + static_cast<int64_t>(h) * n;
-        const float lse = lane < n ? part_lse[base + lane] : NEG_INF;
+        // the log-sum-exps and the first batch of partial rows, issued together
+        const float lse = lane < n ? __ldg(part_lse + base + lane) : NEG_INF;
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = u < n ? load(base + u) : make_float4(0.f, 0.f, 0.f, 0.f);
         float mx = lse;
 #pragma unroll
         for (int s = 16; s; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+        // an empty split (lse = -inf) weighs 0; its partial row holds zeros
         const float w = (lse == NEG_INF) ? 0.f : __expf(lse - mx);
         float wsum = w;
 #pragma unroll
         for (int s = 16; s; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
-        constexpr int PER = HD / 32;          // dims per lane (2 or 4)
         float acc[PER];
 #pragma unroll
         for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll 4
-        for (int s = 0; s < n; ++s) {
-            const float wt = __shfl_sync(0xffffffffu, w, s);
-            const float *src = part_o + (base + s) * HD + lane * PER;
-            if constexpr (PER == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                acc[0] += wt * v.x;
-                acc[1] += wt * v.y;
-                acc[2] += wt * v.z;
-                acc[3] += wt * v.w;
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(src);
-                acc[0] += wt * v.x;
-                acc[1] += wt * v.y;
+        for (int s0 = 0;;) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float wt = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);   // 0 past the last split
+                acc[0] += wt * v[u].x;
+                acc[1] += wt * v[u].y;
+                if constexpr (PER == 4) {
+                    acc[2] += wt * v[u].z;
+                    acc[3] += wt * v[u].w;
+                }
             }
+            s0 += U;
+            if (s0 >= n) break;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                v[u] = s0 + u < n ? load(base + s0 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
         __nv_bfloat16 *dst = out + (static_cast<int64_t>(st.x) * num_q_heads + h) * HD + lane * PER;
-#pragma unroll
-        for (int e = 0; e < PER; e += 2)
-            *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+        if constexpr (PER == 4) {
+            *reinterpret_cast<uint2 *>(dst) =
+                make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+        } else {
+            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        }
     }
 }
 
