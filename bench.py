@@ -656,8 +656,9 @@ def main():
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
     }
-    if fp8:
-        # the profiled traffic ratio is the bf16 decode kernel's
+    if fp8 or r["launches_per_step"] != 4:
+        # the profiled traffic ratio is the bf16 decode kernel's alone (no
+        # shared-prefix pass, no prefill kernel in the call)
         line["roofline"]["traffic"] = None
         line["roofline"]["kernel"] = "paged_attn (plan + E4M3 decode kernel; chunks on its 16-row tiles)"
     if args.graph:

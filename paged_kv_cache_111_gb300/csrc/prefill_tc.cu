@@ -133,6 +133,14 @@ struct PfItem {
     int32_t g;            // kv head
 };
 constexpr int kItemSlots = 4;
+
+// A workspace field written by the plan, loaded through L2 (not L1): the
+// prefill kernel reads the plan before its programmatic-launch wait.
+__device__ __forceinline__ int32_t ws_ld(const int32_t *a) { return __ldcg(a); }
+__device__ __forceinline__ int64_t ws_ld(const int64_t *a) {
+    return static_cast<int64_t>(__ldcg(reinterpret_cast<const long long *>(a)));
+}
+__device__ __forceinline__ int4 ws_ld(const int4 *a) { return __ldcg(a); }
 static_assert(kItemSlots * sizeof(PfItem) <= 256, "item ring fits its 256 bytes");
 
 // Persistent: one CTA per SM.  The CTA's first item is its index; each later
@@ -156,14 +164,22 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t sK = smem_u32(smem + Cfg::kOffK);
     const uint32_t sV = smem_u32(smem + Cfg::kOffV);
 
-    pdl_wait();       // the plan, the cache write and the decode kernel are complete
+    // The kernel launched just before this one (the decode kernel, or the
+    // shared-prefix pass) may still be running: it writes other rows and other
+    // splits than this kernel, and it started only after the plan (and the
+    // cache write before the plan) had completed.  So the plan's lists are read
+    // at once, through L2 (ws_ld), and the wait on that kernel comes at the
+    // end, so that this grid completes after it and the combine sees both.
     pdl_trigger();
     const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
-    const int n_parts = CASCADE ? hdr->prefix_parts : 1;
-    const int n_tiles = CASCADE ? (hdr->n_crows + kPrefillRows - 1) / kPrefillRows : hdr->n_ptiles;
+    const int n_parts = CASCADE ? ws_ld(&hdr->prefix_parts) : 1;
+    const int n_tiles = CASCADE ? (ws_ld(&hdr->n_crows) + kPrefillRows - 1) / kPrefillRows : ws_ld(&hdr->n_ptiles);
     const int n_items = n_tiles * p.num_kv_heads * n_parts;
-    if (static_cast<int>(blockIdx.x) >= n_items) return;   // uniform over the CTA
+    if (static_cast<int>(blockIdx.x) >= n_items) {            // uniform over the CTA
+        pdl_wait();
+        return;
+    }
     const int G = p.G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -210,17 +226,18 @@ __global__ void __launch_bounds__(384, 1)
                 it.g = item % p.num_kv_heads;
                 if constexpr (CASCADE) {
                     it.r = 0;                          // the prefix blocks are read through request 0's table
-                    it.L = hdr->prefix_blocks * kBlock;
+                    it.L = ws_ld(&hdr->prefix_blocks) * kBlock;
                     const int kv_all = (it.L + kPrefillKeys - 1) / kPrefillKeys;
                     const int per = (kv_all + n_parts - 1) / n_parts;   // the plan makes every range non-empty
                     it.part = (item / p.num_kv_heads) % n_parts;
                     it.t0 = it.part * per;
                     it.n_kv = min(kv_all, it.t0 + per) - it.t0;
-                    it.n_pages = hdr->prefix_blocks;
-                    it.rows_total = hdr->n_crows;
+                    it.n_pages = ws_ld(&hdr->prefix_blocks);
+                    it.rows_total = ws_ld(&hdr->n_crows);
                     it.row0 = (item / (p.num_kv_heads * n_parts)) * kPrefillRows;
                 } else {
-                    const int4 tile = reinterpret_cast<const int4 *>(p.ws + hdr->off_ptiles)[item / p.num_kv_heads];
+                    const int4 tile =
+                        ws_ld(reinterpret_cast<const int4 *>(p.ws + ws_ld(&hdr->off_ptiles)) + item / p.num_kv_heads);
                     it.r = tile.x;
                     it.n_kv = tile.z;
                     it.L = p.seq_lens[it.r];
@@ -454,7 +471,7 @@ __global__ void __launch_bounds__(384, 1)
             ri.valid = rrow < it->rows_total;
             if (ri.valid) {
                 if constexpr (CASCADE) {
-                    ri.crow = reinterpret_cast<const int4 *>(p.ws + hdr->off_crows)[rrow];
+                    ri.crow = ws_ld(reinterpret_cast<const int4 *>(p.ws + ws_ld(&hdr->off_crows)) + rrow);
                     ri.tok = ri.crow.x;
                     ri.hh = ri.crow.w;
                     ri.lim = it->L;
@@ -519,7 +536,7 @@ __global__ void __launch_bounds__(384, 1)
                 lim = ri.lim;
                 if (ri.valid) {
                     if constexpr (CASCADE) {
-                        const int4 rq = reinterpret_cast<const int4 *>(p.ws + hdr->off_req)[ri.crow.y];
+                        const int4 rq = ws_ld(reinterpret_cast<const int4 *>(p.ws + ws_ld(&hdr->off_req)) + ri.crow.y);
                         dst = rq.y + (static_cast<int64_t>(ri.crow.z) * p.num_q_heads + cur->g * G + ri.hh) * rq.x +
                               cur->part;
                     } else {
@@ -704,7 +721,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (dst >= 0) {
                     if constexpr (CASCADE) {
                         // split `part` of the row: normalised partial output and natural log-sum-exp
-                        float *po = reinterpret_cast<float *>(p.ws + hdr->off_part_o) + dst * HD + half * kHalfDims;
+                        float *po = reinterpret_cast<float *>(p.ws + ws_ld(&hdr->off_part_o)) + dst * HD + half * kHalfDims;
 #pragma unroll
                         for (int c = 0; c < kHalfDims / 32; ++c)
 #pragma unroll
@@ -713,7 +730,7 @@ __global__ void __launch_bounds__(384, 1)
                                     make_float4(__uint_as_float(v[c][e]) * inv, __uint_as_float(v[c][e + 1]) * inv,
                                                 __uint_as_float(v[c][e + 2]) * inv, __uint_as_float(v[c][e + 3]) * inv);
                         if (half == 0)
-                            reinterpret_cast<float *>(p.ws + hdr->off_part_lse)[dst] =
+                            reinterpret_cast<float *>(p.ws + ws_ld(&hdr->off_part_lse))[dst] =
                                 l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
                     } else {
                         __nv_bfloat16 *o = p.out + dst;
@@ -743,6 +760,7 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
     }
+    pdl_wait();       // complete only after the kernel launched before this one
 }
 
 // ---- host side --------------------------------------------------------------------

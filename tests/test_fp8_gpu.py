@@ -131,6 +131,7 @@ EDGE = [
     ("empty requests", [(20, 4), (0, 0), (47, 1), (5, 0)], 8, 4, 64, None),
     ("peaked softmax (scale 1.0)", [(300, 1), (50, 70)], 8, 2, 128, 1.0),
     ("prefix and forks", [(200, 1), (260, 1), (143, 1)], 16, 2, 128, None),
+    ("8-row tiles q=4 G=2", [(50, 4), (3, 4), (400, 2)], 4, 2, 128, None),
 ]
 
 

@@ -63,6 +63,9 @@ EDGE = [
     ("G=16 one tile per token", [(90, 1), (31, 1)], 32, 2, 128),
     ("empty requests", [(20, 4), (0, 0), (47, 1), (5, 0)], 8, 4, 64),
     ("long prefill chunk", [(130, 300), (0, 1)], 8, 2, 128),
+    # decode tiles of exactly 8 rows (q_r * G = 8) holding several query tokens each
+    ("8-row tiles q=4 G=2", [(50, 4), (3, 4), (200, 2), (17, 1)], 4, 2, 64),
+    ("8-row tiles q=2 G=4 split keys", [(900, 2), (30, 2), (0, 1)], 16, 4, 128),
 ]
 
 
