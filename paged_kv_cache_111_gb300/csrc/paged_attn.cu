@@ -182,16 +182,22 @@ __device__ ReqPlan plan_request(const PlanParams &p, const int *qsl, const int *
     return rp;
 }
 
+// What the chunks of a request need from its plan: {mode, first page (mode
+// 0) or context, pages per split (mode 0) or rows, pages}.
+__device__ __forceinline__ int4 chunk_geometry(const ReqPlan &rp) {
+    return rp.mode == 0 ? make_int4(0, rp.first, rp.per_split, rp.pages) : make_int4(rp.mode, rp.ctx, rp.rows, rp.pages);
+}
+
 // Mode 0/1: page range of chunk k.  Mode 2: {0, KV tiles} of tile k.  A tile
 // ending before request row `row_end` sees keys 0 .. ctx + last_row / G.
-__device__ __forceinline__ int2 chunk_pages(const ReqPlan &rp, int G, int k) {
-    if (rp.mode == 0) {
-        const int b = rp.first + k * rp.per_split;
-        return make_int2(b, min(rp.pages, b + rp.per_split));
+__device__ __forceinline__ int2 chunk_pages(const int4 &gm, int G, int k) {
+    if (gm.x == 0) {
+        const int b = gm.y + k * gm.z;
+        return make_int2(b, min(gm.w, b + gm.z));
     }
-    const int row_end = rp.mode == 1 ? 16 * k + 16 : kPrefillRows * (k + 1);
-    const int lim = rp.ctx + (min(rp.rows, row_end) - 1) / G + 1;
-    if (rp.mode == 1) return make_int2(0, div_up(lim, kBlock));
+    const int row_end = gm.x == 1 ? 16 * k + 16 : kPrefillRows * (k + 1);
+    const int lim = gm.y + (min(gm.z, row_end) - 1) / G + 1;
+    if (gm.x == 1) return make_int2(0, div_up(lim, kBlock));
     return make_int2(0, div_up(lim, kPrefillKeys));
 }
 
@@ -306,6 +312,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     __shared__ int s_qsl[kPlanStagedSeqs + 1];
     __shared__ int s_len[kPlanStagedSeqs];
     __shared__ int4 s_req[kPlanStagedSeqs];
+    __shared__ int4 s_geom[kPlanStagedSeqs];   // chunk geometry per request (staged batches)
 
     WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
     int4 *req_ws = reinterpret_cast<int4 *>(p.ws + p.lay.off_req);
@@ -428,6 +435,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
             // a cascade request has splits = chunks + prefix_parts (>= 1), which
             // no other request has
             req[r] = make_int4(rp.valid && fits ? (split ? nsplit : 1) : 0, split ? pbase : 0, cb, n);
+            if (staged) s_geom[r] = chunk_geometry(rp);
             if (rp.valid && fits && rp.first > 0) {
                 const int q0 = qsl[r];
                 for (int row = 0; row < rp.rows; ++row) crows[crow + row] = make_int4(q0 + row / G, r, row / G, row % G);
@@ -460,12 +468,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         return lo;
     };
     const int n_emit = fits ? n_total : 0;
+    // (a staged batch keeps each request's chunk geometry in shared memory;
+    // a larger one plans the request again)
+    auto geometry = [&](int r, const int4 &ri) {
+        return staged ? s_geom[r] : chunk_geometry(plan_request(p, qsl, lens, r, pps, is_cascade(ri)));
+    };
     for (int c = tid; c < n_emit; c += nthr) {
         const int r = owner(c);
         const int4 ri = req[r];
-        const ReqPlan rp = plan_request(p, qsl, lens, r, pps, is_cascade(ri));
-        const int2 pg = chunk_pages(rp, G, c - ri.z);
-        if (rp.mode == 2) agg_inc(pbin_count, min(pg.y, kSizeBins - 1));
+        const int4 gm = geometry(r, ri);
+        const int2 pg = chunk_pages(gm, G, c - ri.z);
+        if (gm.x == 2) agg_inc(pbin_count, min(pg.y, kSizeBins - 1));
         else agg_inc(bin_count, min(pg.y - pg.x, kSizeBins - 1));
     }
     __syncthreads();
@@ -486,10 +499,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         const int r = owner(c);
         const int4 ri = req[r];
         const bool casc = is_cascade(ri);
-        const ReqPlan rp = plan_request(p, qsl, lens, r, pps, casc);
+        const int4 gm = geometry(r, ri);
         const int k = c - ri.z;
-        const int2 pg = chunk_pages(rp, G, k);
-        if (rp.mode == 2) {
+        const int2 pg = chunk_pages(gm, G, k);
+        if (gm.x == 2) {
             const int pos = agg_inc(pbin_cursor, min(pg.y, kSizeBins - 1));
             if (pos < p.lay.max_ptiles) ptiles[pos] = make_int4(r, k, pg.y, 0);
         } else {
