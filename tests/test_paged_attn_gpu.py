@@ -95,6 +95,20 @@ def test_prefill_tensor_core_path(case):
     compare(step, what=name)
 
 
+def test_more_requests_than_the_plan_stages():
+    # 1500 requests (the plan keeps up to 1024 in shared memory; beyond that
+    # its per-request state lives in the workspace): decode rows, short
+    # multi-token rows, one long chunk on the tensor-core kernel, empty requests
+    rng = np.random.default_rng(11)
+    reqs = [(int(rng.integers(0, 160)), 1) for _ in range(1500)]
+    for i in range(0, 1500, 97):
+        reqs[i] = (int(rng.integers(0, 60)), int(rng.integers(2, 5)))
+    reqs[5] = (40, 0)
+    reqs[700] = (0, 0)
+    reqs[1499] = (33, 90)
+    compare(custom(reqs, 8, 2, 64, seed=11), what="1500 requests")
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 32])
 def test_forced_split_counts_merge_to_the_same_result(splits):
     step = custom([(700, 1), (33, 1), (1500, 1), (0, 1), (255, 1)], 16, 2, 128, seed=splits)

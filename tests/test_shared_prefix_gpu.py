@@ -117,3 +117,15 @@ def test_cascade_pass_with_more_items_than_ctas():
     assert min(px) >= 1
     _, ref, _ = oracle.run_step(step)
     check_close(out, ref, "cascade, 384 items")
+
+
+def test_cascade_with_more_requests_than_the_plan_stages():
+    # 1100 sharers of a 64-token prefix: the plan compares every table with
+    # request 0's and keeps the per-request state in the workspace
+    rng = torch.Generator().manual_seed(66)
+    ctx = (64 + torch.randint(0, 40, (1100,), generator=rng)).tolist()
+    specs = [wl.RequestSpec(int(c), 1) for c in ctx]
+    step = wl.build_step("many", specs, 16, 2, 64, 8192, 66, shared_prefix_len=64)
+    out = run_cascade(step, 4)
+    _, ref, _ = oracle.run_step(step)
+    check_close(out, ref, "cascade, 1100 sharers")
