@@ -7,9 +7,9 @@
 // block slot / 16, offset slot % 16); "vLLM source reading", section 5.1
 // (slot_mapping drives the scatter).
 //
-// A pure bit copy, HBM-bound: each thread moves one 16-byte vector of one
-// token's K or V row; consecutive threads cover consecutive 16-byte pieces of
-// a head's row, so reads and writes are coalesced 128-byte+ runs.
+// A pure bit copy, HBM-bound: each thread moves 16-byte vectors of tokens' K
+// or V rows; consecutive threads cover consecutive 16-byte pieces of a head's
+// row, so reads and writes are coalesced 128-byte+ runs.
 #include <cuda_fp8.h>
 
 #include "pkv_common.cuh"
@@ -30,81 +30,129 @@ struct KvWriteParams {
     int32_t *status;
 };
 
-// One token per CTA iteration; the CTA's threads cover that token's K and V
-// rows of every kv head, 16 bytes each.
+// The scatter is a flat loop over (token, 16-byte vector of the token's K
+// then V row) pairs.  Each thread takes kWriteUnroll of them a grid stride
+// apart and issues every load (slot and data) before any store: the write is
+// a short chain of dependent memory operations, so its time is their latency
+// unless many are in flight.
+constexpr int kWriteUnroll = 4;
+
+// Vector i of the flat loop: token t, K (0) or V (1), and the vector's index
+// rr within that token's K or V row of all kv heads.
+struct KvVec {
+    int64_t t;
+    int which, rr;
+};
+__device__ __forceinline__ KvVec kv_vec(int64_t i, bool narrow, int per_tok, int per_kv) {
+    KvVec v;
+    v.t = narrow ? static_cast<int64_t>(static_cast<uint32_t>(i) / static_cast<uint32_t>(per_tok)) : i / per_tok;
+    const int e = static_cast<int>(i - v.t * per_tok);
+    v.which = e >= per_kv;
+    v.rr = e - v.which * per_kv;
+    return v;
+}
+
+// Cache index (in vectors of `per_vec_bytes`) of vector rr of K or V of a
+// token written to `slot`.
+__device__ __forceinline__ int64_t kv_dst(const KvWriteParams &p, int64_t slot, int which, int rr) {
+    const int vpr = 1 << p.vec_shift;
+    const int64_t blk = slot / kBlock;
+    const int64_t off = slot - blk * kBlock;
+    return (((blk * p.num_kv_heads + (rr >> p.vec_shift)) * 2 + which) * kBlock + off) * vpr + (rr & (vpr - 1));
+}
+
 __global__ void __launch_bounds__(256) kv_write_kernel(KvWriteParams p) {
     pdl_trigger();                                         // the attention plan may start (it reads no cache)
-    const int vpr = 1 << p.vec_shift;                      // vectors per head row
-    const int per_kv = p.num_kv_heads * vpr;               // vectors of K (or V) per token
+    const int per_kv = p.num_kv_heads << p.vec_shift;      // vectors of K (or V) per token
     const int per_tok = 2 * per_kv;
-    for (int64_t t = blockIdx.x; t < p.num_tokens; t += gridDim.x) {
-        const int64_t slot = __ldg(p.slots + t);
-        if (slot < 0) continue;                             // padding token
-        if (slot >= p.num_slots) {
-            if (threadIdx.x == 0) set_status(p.status, PKV_ERR_DEVICE_INDEX);
-            continue;
+    const int64_t total = static_cast<int64_t>(p.num_tokens) * per_tok;
+    const bool narrow = total <= INT32_MAX;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+         i0 += kWriteUnroll * stride) {
+        int64_t slot[kWriteUnroll];
+        uint4 val[kWriteUnroll];
+        int which[kWriteUnroll], rr[kWriteUnroll];
+#pragma unroll
+        for (int u = 0; u < kWriteUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            slot[u] = -1;                                  // nothing to store
+            if (i < total) {
+                const KvVec v = kv_vec(i, narrow, per_tok, per_kv);
+                which[u] = v.which;
+                rr[u] = v.rr;
+                slot[u] = __ldg(p.slots + v.t);
+                val[u] = __ldg((v.which ? p.value + v.t * p.value_stride_v : p.key + v.t * p.key_stride_v) + v.rr);
+            }
         }
-        const int64_t blk = slot / kBlock;
-        const int64_t off = slot - blk * kBlock;
-        const uint4 *ksrc = p.key + t * p.key_stride_v;
-        const uint4 *vsrc = p.value + t * p.value_stride_v;
-        for (int v = threadIdx.x; v < per_tok; v += blockDim.x) {
-            const int which = v >= per_kv;                  // 0 = K, 1 = V
-            const int rr = v - which * per_kv;
-            const int h = rr >> p.vec_shift;
-            const int c = rr & (vpr - 1);
-            const uint4 val = __ldg((which ? vsrc : ksrc) + rr);
-            const int64_t dst = (((blk * p.num_kv_heads + h) * 2 + which) * kBlock + off) * vpr + c;
-            p.cache[dst] = val;
+#pragma unroll
+        for (int u = 0; u < kWriteUnroll; ++u) {
+            if (slot[u] < 0) continue;                     // padding token (or past the end)
+            if (slot[u] >= p.num_slots) {
+                set_status(p.status, PKV_ERR_DEVICE_INDEX);
+                continue;
+            }
+            p.cache[kv_dst(p, slot[u], which[u], rr[u])] = val[u];
         }
     }
 }
 
 // The same scatter into an E4M3 cache: element x is stored as the E4M3 code
 // nearest to the fp32 quotient x / scale (ties to even, held at +-448).
-// Each thread turns one 16-byte vector of 8 bf16 into 8 bytes.
+// Each vector of 8 bf16 becomes 8 bytes.
+__device__ __forceinline__ uint2 bf16x8_to_e4m3(const uint4 &val, float s) {
+    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+    uint32_t packed[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        uint32_t out = 0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t pair = w[2 * i + j];
+            float2 f;
+            f.x = __fdiv_rn(__uint_as_float(pair << 16), s);
+            f.y = __fdiv_rn(__uint_as_float(pair & 0xFFFF0000u), s);
+            const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+            out |= static_cast<uint32_t>(q) << (16 * j);
+        }
+        packed[i] = out;
+    }
+    return make_uint2(packed[0], packed[1]);
+}
+
 __global__ void __launch_bounds__(256) kv_write_fp8_kernel(KvWriteParams p, float k_scale, float v_scale) {
     pdl_trigger();
-    const int vpr = 1 << p.vec_shift;                      // 16-byte input vectors per head row
-    const int per_kv = p.num_kv_heads * vpr;
+    const int per_kv = p.num_kv_heads << p.vec_shift;      // 16-byte input vectors of K (or V) per token
     const int per_tok = 2 * per_kv;
+    const int64_t total = static_cast<int64_t>(p.num_tokens) * per_tok;
+    const bool narrow = total <= INT32_MAX;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     uint2 *cache8 = reinterpret_cast<uint2 *>(p.cache);    // 8-byte output vectors
-    for (int64_t t = blockIdx.x; t < p.num_tokens; t += gridDim.x) {
-        const int64_t slot = __ldg(p.slots + t);
-        if (slot < 0) continue;
-        if (slot >= p.num_slots) {
-            if (threadIdx.x == 0) set_status(p.status, PKV_ERR_DEVICE_INDEX);
-            continue;
-        }
-        const int64_t blk = slot / kBlock;
-        const int64_t off = slot - blk * kBlock;
-        const uint4 *ksrc = p.key + t * p.key_stride_v;
-        const uint4 *vsrc = p.value + t * p.value_stride_v;
-        for (int v = threadIdx.x; v < per_tok; v += blockDim.x) {
-            const int which = v >= per_kv;
-            const int rr = v - which * per_kv;
-            const int h = rr >> p.vec_shift;
-            const int c = rr & (vpr - 1);
-            const uint4 val = __ldg((which ? vsrc : ksrc) + rr);
-            const float s = which ? v_scale : k_scale;
-            const uint32_t w[4] = {val.x, val.y, val.z, val.w};
-            uint32_t packed[2];
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+         i0 += kWriteUnroll * stride) {
+        int64_t slot[kWriteUnroll];
+        uint4 val[kWriteUnroll];
+        int which[kWriteUnroll], rr[kWriteUnroll];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                uint32_t out = 0;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t pair = w[2 * i + j];
-                    float2 f;
-                    f.x = __fdiv_rn(__uint_as_float(pair << 16), s);
-                    f.y = __fdiv_rn(__uint_as_float(pair & 0xFFFF0000u), s);
-                    const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
-                    out |= static_cast<uint32_t>(q) << (16 * j);
-                }
-                packed[i] = out;
+        for (int u = 0; u < kWriteUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            slot[u] = -1;
+            if (i < total) {
+                const KvVec v = kv_vec(i, narrow, per_tok, per_kv);
+                which[u] = v.which;
+                rr[u] = v.rr;
+                slot[u] = __ldg(p.slots + v.t);
+                val[u] = __ldg((v.which ? p.value + v.t * p.value_stride_v : p.key + v.t * p.key_stride_v) + v.rr);
             }
-            const int64_t dst = (((blk * p.num_kv_heads + h) * 2 + which) * kBlock + off) * vpr + c;
-            cache8[dst] = make_uint2(packed[0], packed[1]);
+        }
+#pragma unroll
+        for (int u = 0; u < kWriteUnroll; ++u) {
+            if (slot[u] < 0) continue;
+            if (slot[u] >= p.num_slots) {
+                set_status(p.status, PKV_ERR_DEVICE_INDEX);
+                continue;
+            }
+            cache8[kv_dst(p, slot[u], which[u], rr[u])] = bf16x8_to_e4m3(val[u], which[u] ? v_scale : k_scale);
         }
     }
 }
@@ -150,6 +198,17 @@ extern "C" int pkv_copy_blocks(void *kv_cache, int64_t num_blocks, int32_t num_k
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+namespace pkv {
+// CTAs of the flat cache-write loop: one vector per thread where that takes
+// at most 8 resident 256-thread CTAs per SM, else that many (grid-strided).
+static int64_t write_grid(int64_t num_tokens, int32_t num_kv_heads, int32_t head_size, int sms, int threads) {
+    const int64_t vectors = num_tokens * 2 * num_kv_heads * (head_size / 8);
+    int64_t blocks = (vectors + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    return blocks > cap ? cap : (blocks < 1 ? 1 : blocks);
+}
+}  // namespace pkv
+
 extern "C" int pkv_kv_write(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads, int32_t head_size,
                             int32_t block_size, const void *key, int64_t key_token_stride, const void *value,
                             int64_t value_token_stride, const int64_t *slot_mapping, int32_t num_tokens,
@@ -185,9 +244,7 @@ extern "C" int pkv_kv_write(void *kv_cache, int64_t num_blocks, int32_t num_kv_h
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PKV_ERR_CUDA;
     const int threads = 256;
-    int64_t blocks = num_tokens;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;      // 8 resident 256-thread CTAs per SM
-    if (blocks > cap) blocks = cap;
+    const int64_t blocks = write_grid(num_tokens, num_kv_heads, head_size, sms, threads);
     kv_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -227,9 +284,7 @@ extern "C" int pkv_kv_write_fp8(void *kv_cache, int64_t num_blocks, int32_t num_
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PKV_ERR_CUDA;
-    int64_t blocks = num_tokens;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    if (blocks > cap) blocks = cap;
+    const int64_t blocks = write_grid(num_tokens, num_kv_heads, head_size, sms, 256);
     kv_write_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p, k_scale,
                                                                                                          v_scale);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
