@@ -666,7 +666,7 @@ def main():
         line["roofline"]["traffic"] = None
     if ab["kv_logical"] != ab["kv_unique"]:
         line["logical_kv_gbs_incl_l2_reuse"] = ab["kv_logical"] / (r["attn_ms"] * 1e-3) / 1e9
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:      # the oracle's baseline: rank 0 of a 1-GPU run only
         line["cpu_baseline"] = cpu_baseline(step, scales=r["fp8_scales"])
     print(json.dumps(line), flush=True)
     if world > 1:
