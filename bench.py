@@ -660,7 +660,11 @@ def main():
         # the profiled traffic ratio is the bf16 decode kernel's alone (no
         # shared-prefix pass, no prefill kernel in the call)
         line["roofline"]["traffic"] = None
+    if fp8:
         line["roofline"]["kernel"] = "paged_attn (plan + E4M3 decode kernel; chunks on its 16-row tiles)"
+    elif r["shared_prefix_blocks"]:
+        line["roofline"]["kernel"] = line["roofline"]["kernel"].replace(
+            "paged_attn (plan + decode", "paged_attn_shared_prefix (plan + decode + tcgen05 shared-prefix")
     if args.graph:
         line["roofline"]["kernel"] = "whole layer-step (kv_write + paged_attn + combine), CUDA-graph replay"
         line["roofline"]["traffic"] = None
