@@ -114,14 +114,14 @@ def shared_prefix_blocks(step: wl.Step) -> int:
 def launches_per_step(step: wl.Step, prefix_blocks: int, fp8: bool = False) -> int:
     """Kernels of one layer-step: kv_write, plan, decode, combine; the prefill
     kernel when some request has more than 64 rows (q_r * G) and the head
-    layout has a tensor-core tile; the shared-prefix kernel when asked for.
-    An E4M3 cache runs every row on the decode kernel."""
+    layout has a tensor-core tile; the shared-prefix kernel when asked for
+    (bf16 caches only)."""
     G = step.num_q_heads // step.num_kv_heads
-    tile_ok = step.head_size in (64, 128) and 128 % G == 0 and not fp8
+    tile_ok = step.head_size in (64, 128) and 128 % G == 0
     n = 4
     if tile_ok and step.max_query_len * G > 64:
         n += 1
-    if tile_ok and prefix_blocks > 0:
+    if tile_ok and prefix_blocks > 0 and not fp8:
         n += 1
     return n
 
@@ -661,7 +661,8 @@ def main():
         # shared-prefix pass, no prefill kernel in the call)
         line["roofline"]["traffic"] = None
     if fp8:
-        line["roofline"]["kernel"] = "paged_attn (plan + E4M3 decode kernel; chunks on its 16-row tiles)"
+        line["roofline"]["kernel"] = line["roofline"]["kernel"].replace("decode", "E4M3 decode").replace(
+            "tcgen05 prefill", "E4M3-widening tcgen05 prefill")
     elif r["shared_prefix_blocks"]:
         line["roofline"]["kernel"] = line["roofline"]["kernel"].replace(
             "paged_attn (plan + decode", "paged_attn_shared_prefix (plan + decode + tcgen05 shared-prefix")

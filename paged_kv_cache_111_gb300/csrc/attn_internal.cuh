@@ -70,6 +70,7 @@ struct PrefillParams {
     int64_t num_blocks;
     float scale_log2;
     int32_t lo_tiles;         // leading KV tiles whose P always enters P V as a bf16 pair
+    float k_scale, v_scale;   // E4M3 cache: stored code * scale is the value
     uint8_t *ws;
 };
 
@@ -118,6 +119,6 @@ inline bool prefill_supported(int num_q_heads, int num_kv_heads, int head_size) 
 // beyond the plan's tile count return at once.
 int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
                    const void *kv_cache, int64_t num_blocks, int32_t head_size, int64_t grid, int dev,
-                   cudaStream_t stream);
+                   cudaStream_t stream, bool kv8 = false);
 
 }  // namespace pkv

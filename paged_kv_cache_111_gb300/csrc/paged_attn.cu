@@ -651,10 +651,10 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PKV_ERR_SHAPE;
     if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale > 3.0e38f || v_scale > 3.0e38f) return PKV_ERR_SHAPE;
 
-    // the tensor-core tile kernel (long chunks, the shared-prefix pass) reads
-    // bf16 pages only; with an E4M3 cache every row runs on the decode kernel
-    const bool prefill_ok = !kv8 && prefill_supported(num_q_heads, num_kv_heads, head_size);
-    if (!prefill_ok) prefix_blocks = 0;
+    // long chunks go to the tensor-core tile kernel (over an E4M3 cache too);
+    // the shared-prefix pass reads bf16 pages only
+    const bool prefill_ok = prefill_supported(num_q_heads, num_kv_heads, head_size);
+    if (!prefill_ok || kv8) prefix_blocks = 0;
     const WsLayout lay = ws_layout(num_seqs, num_tokens, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
                                    head_size, prefix_blocks);
     if (workspace_needed) *workspace_needed = static_cast<size_t>(lay.total);
@@ -739,6 +739,8 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     fp.num_blocks = num_blocks;
     fp.scale_log2 = ap.scale_log2;
     fp.lo_tiles = 0;
+    fp.k_scale = k_scale;
+    fp.v_scale = v_scale;
     fp.ws = ap.ws;
     if (prefix_blocks > 0) {
         // persistent kernels: one CTA per SM at most
@@ -750,7 +752,7 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     }
     if (!may_prefill) return PKV_OK;
     return launch_prefill(fp, query, query_token_stride, num_tokens, kv_cache, num_blocks, head_size,
-                          std::min<int64_t>(std::min(sms, kStatsCtas), lay.max_ptiles * num_kv_heads), dev, st);
+                          std::min<int64_t>(std::min(sms, kStatsCtas), lay.max_ptiles * num_kv_heads), dev, st, kv8);
 }
 
 }  // namespace pkv

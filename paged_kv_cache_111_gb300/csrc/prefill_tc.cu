@@ -42,16 +42,23 @@
 
 namespace pkv {
 
-template <int HD>
+// KV8: an E4M3 cache.  Its pages land in a ring of raw 8-bit tiles and
+// warps 2 (K) and 3 (V) widen them to f16 into the 16-bit ring the MMAs
+// read; Q and P are f16 too (both operands of a kind::f16 product share
+// their type).
+template <int HD, bool KV8 = false>
 struct PrefillCfg {
     static constexpr int kHalves = HD / 64;
-    static constexpr int kStages = 3;                        // K and V ring depth
+    static constexpr int kStages = (KV8 && HD == 128) ? 2 : 3;   // 16-bit K and V ring depth
     static constexpr int kKVBytes = kHalves * kPrefillKeys * 128;   // one K (or V) tile
+    static constexpr int kRawStages = 2;                     // raw E4M3 ring depth (KV8)
+    static constexpr int kRawBytes = kPrefillKeys * HD;      // one raw K (or V) tile
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
-    static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-    static constexpr int kOffXchg = kOffBar + 512;            // softmax halves' maxima and sums (3 KiB)
-    static constexpr int kOffItems = kOffXchg + 3072;         // ring of work items (256 bytes)
+    static constexpr int kOffRaw = kOffV + kStages * kKVBytes;
+    static constexpr int kOffBar = kOffRaw + (KV8 ? kRawStages * 2 * kRawBytes : 0);
+    static constexpr int kOffXchg = kOffBar + 512;            // softmax halves' maxima, sums, Q maxima (4 KiB)
+    static constexpr int kOffItems = kOffXchg + 4096;         // ring of work items (256 bytes)
     static constexpr int kSmem = kOffItems + 256 + 1024;      // + alignment slack
     // tensor memory: two S buffers (each later holding that tile's P and its
     // bf16 remainder), O, and Q as the A operand of S = Q K^T
@@ -66,6 +73,7 @@ enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kKFull2, kVFull0, kVFull1, kVFul
                   kItemFull0, kItemFull1, kItemFull2, kItemFull3,      // work-item ring
                   kItemEmpty0, kItemEmpty1, kItemEmpty2, kItemEmpty3,
                   kOFree,                              // O read out by the epilogue
+                  kRFull0, kRFull1, kREmpty0, kREmpty1,  // raw E4M3 tiles (KV8)
                   kNumBars };
 static_assert(kNumBars * 8 + 16 + 64 <= 512, "barriers, the TMEM address slot and the votes fit their 512 bytes");
 // P of tile j is announced on kPFull0 + (j & 1): with one barrier per parity a
@@ -102,6 +110,38 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
+}
+
+// Four E4M3 values (one 32-bit word, element 0 in the low byte) -> two f16x2
+// words (elements 0,1 and 2,3), exactly.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &h01, uint32_t &h23) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w));
+}
+
+// P of a pair of keys as the 16-bit type of the products (bf16, or f16 over
+// an E4M3 cache), and the remainder that the rounding left.
+template <bool F16> __device__ __forceinline__ uint32_t pack_p(float a, float b) {
+    if constexpr (F16) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        return pack_bf16x2(a, b);
+    }
+}
+template <bool F16> __device__ __forceinline__ uint32_t pack_p_rest(float a, float b) {
+    if constexpr (F16) {
+        const float2 hb = __half22float2(__floats2half2_rn(a, b));
+        const __half2 r = __floats2half2_rn(a - hb.x, b - hb.y);
+        return *reinterpret_cast<const uint32_t *>(&r);
+    } else {
+        const float2 hb = __bfloat1622float2(__floats2bfloat162_rn(a, b));
+        return pack_bf16x2(a - hb.x, b - hb.y);
+    }
 }
 
 // Bounded wait shared by every role; on timeout records the error and
@@ -149,11 +189,12 @@ static_assert(kItemSlots * sizeof(PfItem) <= 256, "item ring fits its 256 bytes"
 // them through a ring in shared memory; tiles and their barriers are counted
 // across items, so the loads, the first products and the Q of the next item
 // overlap the epilogue of the current one.
-template <int HD, bool CASCADE>
+template <int HD, bool CASCADE, bool KV8>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16 *__restrict__ query,
                    const int64_t q_stride, const PrefillParams p) {
-    using Cfg = PrefillCfg<HD>;
+    static_assert(!(CASCADE && KV8), "the shared-prefix pass reads bf16 pages");
+    using Cfg = PrefillCfg<HD, KV8>;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -188,7 +229,8 @@ __global__ void __launch_bounds__(384, 1)
             int count = 1;
             if (b == kPFull0 || b == kPFull1 || b == kQFull || b == kOFree) count = 8;
             else if (b >= kXchg0 && b <= kXchg3) count = 2;
-            else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = 9;
+            else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = KV8 ? 11 : 9;   // + converters
+            else if (b == kREmpty0 || b == kREmpty1) count = 2;      // both converter warps
             mbar_init(&bars[b], count);
         }
         tma_prefetch_desc(&kv_map);
@@ -285,6 +327,26 @@ __global__ void __launch_bounds__(384, 1)
                 int pb[kPagesPerTile];
 #pragma unroll
                 for (int pg = 0; pg < kPagesPerTile; ++pg) pb[pg] = __shfl_sync(0xffffffffu, win_cur, wofs + pg);
+                if constexpr (KV8) {
+                    // the raw K and V pages of tile gt, once the converters are done
+                    // with tile gt - 2 (zeroing past the sequence end is theirs)
+                    const int rs = gt % Cfg::kRawStages;
+                    if (gt >= Cfg::kRawStages)
+                        ok = __all_sync(0xffffffffu, pf_wait(&bars[kREmpty0 + rs],
+                                                             ((gt - Cfg::kRawStages) / Cfg::kRawStages) & 1, status));
+                    if (!ok) break;
+                    if (lane == 0) {
+                        uint8_t *raw = smem + Cfg::kOffRaw + rs * 2 * Cfg::kRawBytes;
+                        mbar_arrive_expect_tx(&bars[kRFull0 + rs], 2 * Cfg::kRawBytes);
+#pragma unroll
+                        for (int pg = 0; pg < kPagesPerTile; ++pg) {
+                            tma_load_5d(raw + pg * kBlock * HD, &kv_map, &bars[kRFull0 + rs], 0, 0, 0, it.g, pb[pg]);
+                            tma_load_5d(raw + Cfg::kRawBytes + pg * kBlock * HD, &kv_map, &bars[kRFull0 + rs], 0, 0,
+                                        1, it.g, pb[pg]);
+                        }
+                    }
+                    continue;
+                }
                 // K of tile gt once S of tile gt-S has read its stage
                 if (gt >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKEmpty0 + st], ((gt - S) / S) & 1, status));
                 if (!ok) break;
@@ -339,8 +401,9 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillRows, kPrefillKeys, 0, 0);
-            constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillRows, HD, 0, 1);
+            constexpr uint32_t kIdescS = KV8 ? idesc_f16_f32(kPrefillRows, kPrefillKeys, 0, 0)
+                                             : idesc_bf16_f32(kPrefillRows, kPrefillKeys, 0, 0);
+            constexpr uint32_t kIdescO = KV8 ? idesc_f16_f32(kPrefillRows, HD, 0, 1) : idesc_bf16_f32(kPrefillRows, HD, 0, 1);
             // S(gt) = Q K^T into S buffer gt & 1; A = Q in tensor memory
             auto issue_s = [&](int gt) {
                 const int st = gt % S;
@@ -427,6 +490,64 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
         __syncwarp();
+    } else if (KV8 && (warp == 2 || warp == 3)) {
+        // ---------------- converters (E4M3 cache): raw tiles -> f16 tiles ----------------
+        // warp 2 widens K, warp 3 widens V and zeroes V rows past the sequence
+        // end (its scores there are masked, but NaN times a zero weight is NaN)
+        const bool isv = warp == 3;
+        bool ok = true;
+        int gj = 0;
+        for (int k = 0; ok; ++k) {
+            const int slot = k % kItemSlots;
+            ok = __all_sync(0xffffffffu, pf_wait(&bars[kItemFull0 + slot], (k / kItemSlots) & 1, status));
+            if (!ok) break;
+            const bool valid = items[slot].valid != 0;
+            const int n_kv = items[slot].n_kv;
+            const int L = items[slot].L;
+            const int t0 = items[slot].t0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
+            if (!valid) break;
+            const int end_tile = end_tile_of(L);
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int gt = gj + j;
+                const int st = gt % S, rs = gt % Cfg::kRawStages;
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kRFull0 + rs], (gt / Cfg::kRawStages) & 1, status));
+                if (ok && gt >= S)
+                    ok = __all_sync(0xffffffffu,
+                                    pf_wait(&bars[(isv ? kVEmpty0 : kKEmpty0) + st], ((gt - S) / S) & 1, status));
+                if (!ok) break;
+                const uint32_t src =
+                    smem_u32(smem + Cfg::kOffRaw + rs * 2 * Cfg::kRawBytes + (isv ? Cfg::kRawBytes : 0));
+                const uint32_t dst = (isv ? sV : sK) + st * Cfg::kKVBytes;
+                const int zero_from = (isv && j == end_tile) ? L - (t0 + j) * kPrefillKeys : kPrefillKeys;
+                // 8-element pieces: raw row r bytes 8c .. 8c + 7 -> 16-bit tile row r,
+                // 64-column box c / 8, 16-byte chunk c % 8 at its 128-byte-swizzle place
+                constexpr int kPieces = kPrefillKeys * HD / 8;
+#pragma unroll 4
+                for (int u = lane; u < kPieces; u += 32) {
+                    const int r = u / (HD / 8), c = u % (HD / 8);
+                    uint32_t w0, w1;
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(src + r * HD + c * 8));
+                    uint32_t h0, h1, h2, h3;
+                    e4m3x4_to_f16x4(w0, h0, h1);
+                    e4m3x4_to_f16x4(w1, h2, h3);
+                    if (r >= zero_from) h0 = h1 = h2 = h3 = 0u;
+                    const uint32_t a = dst + (c >> 3) * (kPrefillKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h0), "r"(h1), "r"(h2),
+                                 "r"(h3)
+                                 : "memory");
+                }
+                fence_proxy_async_smem();              // for the tensor core, and before the raw stage refills
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[(isv ? kVFull0 : kKFull0) + st]);
+                    if (isv && j == end_tile) mbar_arrive(&bars[kVFix0 + st]);
+                    mbar_arrive(&bars[kREmpty0 + rs]);
+                }
+            }
+            gj += n_kv;
+        }
     } else if (warp >= 4) {
         // ---------------- softmax + epilogue: two threads per row ----------------
         // warps 4-7 take keys (and output columns) of the first half of the tile,
@@ -442,6 +563,7 @@ __global__ void __launch_bounds__(384, 1)
         // exchange of the two halves' row maxima (by tile parity) and final sums
         float *xmax = reinterpret_cast<float *>(smem + Cfg::kOffXchg);          // [2][2][128]
         float *xsum = xmax + 2 * 2 * kPrefillRows;                               // [2][128]
+        float *xq = xsum + 2 * kPrefillRows;                                     // [2][128] (E4M3: Q maxima)
         // the two warps of this quadrant meet on an mbarrier, one phase per
         // tile plus one per item for the final sums (bounded waits, like every other)
         uint64_t *xbar = &bars[kXchg0 + quad];
@@ -493,6 +615,9 @@ __global__ void __launch_bounds__(384, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + k % kItemSlots]);
         };
+        // score factor of this thread's row (log2 domain): the scale; over an
+        // E4M3 cache also k_scale and the power of two that brought Q into f16
+        float sl2 = p.scale_log2;
         // this half of the item's Q row -> tensor memory (A operand of S = Q K^T),
         // zeros past the request
         auto load_q = [&](const volatile PfItem *it) {
@@ -507,6 +632,27 @@ __global__ void __launch_bounds__(384, 1)
                 qv[4 * c + 1] = w.y;
                 qv[4 * c + 2] = w.z;
                 qv[4 * c + 3] = w.w;
+            }
+            if constexpr (KV8) {
+                // the row scaled by 2^e into [2^14, 2^15) before rounding to f16 (exact
+                // but for parts below 2^-24 of its largest); the two halves agree on e
+                float a = 0.f;
+#pragma unroll
+                for (int e = 0; e < kHalfDims / 2; ++e)
+                    a = fmaxf(a, fmaxf(fabsf(__uint_as_float(qv[e] << 16)), fabsf(__uint_as_float(qv[e] & 0xFFFF0000u))));
+                xq[half * kPrefillRows + row] = a;
+                post();
+                if (!meet()) a = 0.f;                  // timed out: the status says so
+                a = fmaxf(a, xq[(half ^ 1) * kPrefillRows + row]);
+                const int ex = a > 0.f ? min(126, max(-114, 14 - ilogbf(a))) : 0;
+                const float u = __int_as_float((ex + 127) << 23);
+#pragma unroll
+                for (int e = 0; e < kHalfDims / 2; ++e) {
+                    const __half2 h = __floats2half2_rn(__uint_as_float(qv[e] << 16) * u,
+                                                        __uint_as_float(qv[e] & 0xFFFF0000u) * u);
+                    qv[e] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+                sl2 = p.scale_log2 * p.k_scale * __int_as_float((127 - ex) << 23);
             }
             if constexpr (kHalfDims / 2 == 32) {
                 tmem_st32(trow + Cfg::kColQ + half * 32, qv);
@@ -576,7 +722,7 @@ __global__ void __launch_bounds__(384, 1)
                 // exponential of the tile)
                 float psum = 0.f, psq = 0.f;
                 auto weights = [&](float ref) {
-                    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nref2 = f2_pack(-ref, -ref);
+                    const uint64_t sc2 = f2_pack(sl2, sl2), nref2 = f2_pack(-ref, -ref);
                     uint64_t ps2[4] = {0, 0, 0, 0}, pq2[4] = {0, 0, 0, 0};
 #pragma unroll
                     for (int c = 0; c < kHalfKeys; c += 2) {
@@ -614,7 +760,7 @@ __global__ void __launch_bounds__(384, 1)
                 xmax[(sb * 2 + half) * kPrefillRows + row] = mx;
                 post();
                 const bool first = m_ref == NEG_INF;       // O holds nothing yet for this row
-                const bool ready = first ? mx == NEG_INF : mx * p.scale_log2 <= m_ref + 8.f;
+                const bool ready = first ? mx == NEG_INF : mx * sl2 <= m_ref + 8.f;
                 const bool early = __all_sync(0xffffffffu, ready);
                 if (early) weights(first ? 0.f : m_ref);
                 ok = meet();
@@ -622,7 +768,7 @@ __global__ void __launch_bounds__(384, 1)
                 mx = fmaxf(mx, xmax[(sb * 2 + (half ^ 1)) * kPrefillRows + row]);
                 // log2-domain max (scale > 0 keeps the order of scores); both halves
                 // take the same decisions from the same values
-                const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+                const float m_new = fmaxf(m_ref, mx * sl2);
                 const bool grow = !first && m_new > m_ref + 8.f;
                 const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
                 if (first || grow) m_ref = m_new;
@@ -668,14 +814,12 @@ __global__ void __launch_bounds__(384, 1)
                 for (int c = 0; c < 2; ++c) {
                     uint32_t w[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]);
+                    for (int e = 0; e < 16; ++e) w[e] = pack_p<KV8>(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]);
                     tmem_st16(sbuf + half * 64 + 16 * c, w);
                     if (wneed) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const float a0 = x[32 * c + 2 * e], a1 = x[32 * c + 2 * e + 1];
-                            const float2 hb = __bfloat1622float2(__floats2bfloat162_rn(a0, a1));
-                            w[e] = pack_bf16x2(a0 - hb.x, a1 - hb.y);
+                            w[e] = pack_p_rest<KV8>(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]);
                         }
                     } else {
 #pragma unroll
@@ -709,7 +853,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (ok) {
                 tc_fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = l > 0.f ? (KV8 ? p.v_scale / l : 1.f / l) : 0.f;   // E4M3: V is code * v_scale
                 uint32_t v[kHalfDims / 32][32];
 #pragma unroll
                 for (int c = 0; c < kHalfDims / 32; ++c) tmem_ld32(trow + Cfg::kColO + half * kHalfDims + c * 32, v[c]);
@@ -783,23 +927,23 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int HD, bool CASCADE>
+template <int HD, bool CASCADE, bool KV8>
 static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, const void *query, int64_t q_stride,
                              int64_t grid, int dev, cudaStream_t stream) {
-    using Cfg = PrefillCfg<HD>;
+    using Cfg = PrefillCfg<HD, KV8>;
     static std::mutex mu;
     static uint64_t done_mask = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
         const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
         if (!bit || !(done_mask & bit)) {
-            if (cudaFuncSetAttribute(prefill_kernel<HD, CASCADE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(prefill_kernel<HD, CASCADE, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Cfg::kSmem) != cudaSuccess)
                 return PKV_ERR_CUDA;
             done_mask |= bit;
         }
     }
-    if (launch_pdl(prefill_kernel<HD, CASCADE>, dim3(static_cast<unsigned>(grid)), dim3(384), Cfg::kSmem, stream,
+    if (launch_pdl(prefill_kernel<HD, CASCADE, KV8>, dim3(static_cast<unsigned>(grid)), dim3(384), Cfg::kSmem, stream,
                    kvm, static_cast<const __nv_bfloat16 *>(query), q_stride, p) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
@@ -807,6 +951,8 @@ static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, con
 
 static int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
                          int32_t head_size);
+static int make_page_map_e4m3(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                              int32_t head_size);
 
 int launch_prefix(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
                   int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream) {
@@ -814,20 +960,24 @@ int launch_prefix(const PrefillParams &p, const void *query, int64_t q_stride, c
     CUtensorMap kvm;
     const int rc = make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
     if (rc) return rc;
-    if (head_size == 64) return launch_prefill_hd<64, true>(p, kvm, query, q_stride, grid, dev, stream);
-    return launch_prefill_hd<128, true>(p, kvm, query, q_stride, grid, dev, stream);
+    if (head_size == 64) return launch_prefill_hd<64, true, false>(p, kvm, query, q_stride, grid, dev, stream);
+    return launch_prefill_hd<128, true, false>(p, kvm, query, q_stride, grid, dev, stream);
 }
 
 int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
                    const void *kv_cache, int64_t num_blocks, int32_t head_size, int64_t grid, int dev,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, bool kv8) {
     (void)num_tokens;
     if (grid <= 0) return PKV_OK;
     CUtensorMap kvm;
-    const int rc = make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
+    const int rc = kv8 ? make_page_map_e4m3(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size)
+                       : make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
     if (rc) return rc;
-    if (head_size == 64) return launch_prefill_hd<64, false>(p, kvm, query, q_stride, grid, dev, stream);
-    return launch_prefill_hd<128, false>(p, kvm, query, q_stride, grid, dev, stream);
+    if (kv8)
+        return head_size == 64 ? launch_prefill_hd<64, false, true>(p, kvm, query, q_stride, grid, dev, stream)
+                               : launch_prefill_hd<128, false, true>(p, kvm, query, q_stride, grid, dev, stream);
+    if (head_size == 64) return launch_prefill_hd<64, false, false>(p, kvm, query, q_stride, grid, dev, stream);
+    return launch_prefill_hd<128, false, false>(p, kvm, query, q_stride, grid, dev, stream);
 }
 
 // Tensor map of the cache as {head_size, 16, 2, kv heads, blocks}; a box is
@@ -844,6 +994,26 @@ static int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blo
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     if (enc(kvm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+// Tensor map of an E4M3 cache as bytes {head_size, 16, 2, kv heads, blocks};
+// a box is the K (or V) rows of one page, unswizzled (the converter warps
+// widen them).
+static int make_page_map_e4m3(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                              int32_t head_size) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PKV_ERR_CUDA;
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2, static_cast<cuuint64_t>(num_kv_heads),
+                                static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t row = static_cast<cuuint64_t>(head_size);
+    const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * num_kv_heads};
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(head_size), kBlock, 1, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (enc(kvm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(kv_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PKV_ERR_CUDA;
     return PKV_OK;
