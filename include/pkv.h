@@ -239,8 +239,9 @@ int pkv_kv_write_fp8(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
  * pkv_paged_attn_fp8 — pkv_paged_attn over an E4M3 cache, with K_j and V_j
  * taken as value(code) * k_scale and value(code) * v_scale; arguments,
  * workspace and protocol (pkv_paged_attn_combine after it) as
- * pkv_paged_attn.  Every row, chunks included, runs on the streaming decode
- * kernel.  Scores, softmax and accumulation are fp32; the query enters the
+ * pkv_paged_attn.  Decode rows run on the streaming decode kernel, long
+ * chunks on the tensor-core kernel with K and V widened to f16 in shared
+ * memory.  Scores, softmax and accumulation are fp32; the query enters the
  * products as f16 after a per-row power-of-two scaling (exact for every
  * query element not below 2^-24 of its row's largest).
  */
