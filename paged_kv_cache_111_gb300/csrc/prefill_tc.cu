@@ -521,21 +521,31 @@ __global__ void __launch_bounds__(384, 1)
                     smem_u32(smem + Cfg::kOffRaw + rs * 2 * Cfg::kRawBytes + (isv ? Cfg::kRawBytes : 0));
                 const uint32_t dst = (isv ? sV : sK) + st * Cfg::kKVBytes;
                 const int zero_from = (isv && j == end_tile) ? L - (t0 + j) * kPrefillKeys : kPrefillKeys;
-                // 8-element pieces: raw row r bytes 8c .. 8c + 7 -> 16-bit tile row r,
-                // 64-column box c / 8, 16-byte chunk c % 8 at its 128-byte-swizzle place
-                constexpr int kPieces = kPrefillKeys * HD / 8;
+                // 16-element pieces: raw row r bytes 16c .. 16c + 15 -> 16-bit tile row r,
+                // 64-column box c / 4, 16-byte chunks 2c % 8 and 2c % 8 + 1 at their
+                // 128-byte-swizzle places
+                constexpr int kPieces = kPrefillKeys * HD / 16;
 #pragma unroll 4
                 for (int u = lane; u < kPieces; u += 32) {
-                    const int r = u / (HD / 8), c = u % (HD / 8);
-                    uint32_t w0, w1;
-                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(src + r * HD + c * 8));
-                    uint32_t h0, h1, h2, h3;
-                    e4m3x4_to_f16x4(w0, h0, h1);
-                    e4m3x4_to_f16x4(w1, h2, h3);
-                    if (r >= zero_from) h0 = h1 = h2 = h3 = 0u;
-                    const uint32_t a = dst + (c >> 3) * (kPrefillKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(h0), "r"(h1), "r"(h2),
-                                 "r"(h3)
+                    const int r = u / (HD / 16), c = u % (HD / 16);
+                    uint32_t w[4];
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                 : "r"(src + r * HD + c * 16));
+                    uint32_t h[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) e4m3x4_to_f16x4(w[e], h[2 * e], h[2 * e + 1]);
+                    if (r >= zero_from) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) h[e] = 0u;
+                    }
+                    const uint32_t row = dst + (c >> 2) * (kPrefillKeys * 128) + r * 128;
+                    const int c0 = (2 * c) & 7;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((c0 ^ (r & 7)) << 4)),
+                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((c0 + 1) ^ (r & 7)) << 4)),
+                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
                                  : "memory");
                 }
                 fence_proxy_async_smem();              // for the tensor core, and before the raw stage refills
