@@ -114,14 +114,13 @@ def shared_prefix_blocks(step: wl.Step) -> int:
 def launches_per_step(step: wl.Step, prefix_blocks: int, fp8: bool = False) -> int:
     """Kernels of one layer-step: kv_write, plan, decode, combine; the prefill
     kernel when some request has more than 64 rows (q_r * G) and the head
-    layout has a tensor-core tile; the shared-prefix kernel when asked for
-    (bf16 caches only)."""
+    layout has a tensor-core tile; the shared-prefix kernel when asked for."""
     G = step.num_q_heads // step.num_kv_heads
     tile_ok = step.head_size in (64, 128) and 128 % G == 0
     n = 4
     if tile_ok and step.max_query_len * G > 64:
         n += 1
-    if tile_ok and prefix_blocks > 0 and not fp8:
+    if tile_ok and prefix_blocks > 0:
         n += 1
     return n
 
@@ -252,8 +251,6 @@ def run_gpu(args, rank: int, world: int) -> dict:
         write(hk[a:b].to(dev), hv[a:b].to(dev), hs[a:b].to(dev))
     del hk, hv
     K = shared_prefix_blocks(step) if args.shared_prefix_blocks < 0 else args.shared_prefix_blocks
-    if fp8:
-        K = 0                        # the shared-prefix pass reads bf16 pages only
     if K:
         ws_bytes = pkv.paged_attn_shared_prefix_workspace_size(step.num_seqs, T, step.max_query_len,
                                                                step.max_seq_len, H, step.num_kv_heads, d, K)
@@ -266,7 +263,10 @@ def run_gpu(args, rank: int, world: int) -> dict:
     maxq, maxs = step.max_query_len, step.max_seq_len
 
     def attention(q, tables, lens, qsl):
-        if fp8:
+        if fp8 and K:
+            pkv.paged_attn_shared_prefix_fp8(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, scales[0],
+                                             scales[1], K, ws)
+        elif fp8:
             pkv.paged_attn_fp8(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, scales[0], scales[1], ws)
         elif K:
             pkv.paged_attn_shared_prefix(out, q, pool, tables, lens, qsl, maxq, maxs, step.scale, K, ws)
@@ -660,12 +660,12 @@ def main():
         # the profiled traffic ratio is the bf16 decode kernel's alone (no
         # shared-prefix pass, no prefill kernel in the call)
         line["roofline"]["traffic"] = None
-    if fp8:
-        line["roofline"]["kernel"] = line["roofline"]["kernel"].replace("decode", "E4M3 decode").replace(
-            "tcgen05 prefill", "E4M3-widening tcgen05 prefill")
-    elif r["shared_prefix_blocks"]:
+    if r["shared_prefix_blocks"]:
         line["roofline"]["kernel"] = line["roofline"]["kernel"].replace(
             "paged_attn (plan + decode", "paged_attn_shared_prefix (plan + decode + tcgen05 shared-prefix")
+    if fp8:
+        line["roofline"]["kernel"] = line["roofline"]["kernel"].replace(" decode", " E4M3 decode").replace(
+            "tcgen05", "E4M3-widening tcgen05")
     if args.graph:
         line["roofline"]["kernel"] = "whole layer-step (kv_write + paged_attn + combine), CUDA-graph replay"
         line["roofline"]["traffic"] = None

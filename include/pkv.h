@@ -258,6 +258,26 @@ int pkv_paged_attn_fp8(void *out, const void *query, int64_t query_token_stride,
                        void *stream);
 
 /*
+ * pkv_paged_attn_shared_prefix_fp8 — pkv_paged_attn_shared_prefix over an
+ * E4M3 cache, with K_j and V_j taken as value(code) * k_scale and
+ * value(code) * v_scale (as pkv_paged_attn_fp8): the shared prefix's keys are
+ * read once per kv head for all sharers, widened to f16 in shared memory.
+ * Arguments, workspace (sized as for pkv_paged_attn_shared_prefix) and
+ * protocol (pkv_paged_attn_combine after it) as pkv_paged_attn_shared_prefix.
+ */
+int pkv_paged_attn_shared_prefix_fp8(void *out, const void *query, int64_t query_token_stride,
+                                     const void *kv_cache, int64_t num_blocks,
+                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t *seq_lens, const int32_t *query_start_loc,
+                                     int32_t num_seqs, int32_t num_tokens,
+                                     int32_t max_query_len, int32_t max_seq_len,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                     int32_t block_size, float scale, float k_scale, float v_scale,
+                                     int32_t num_splits, int32_t shared_prefix_blocks,
+                                     void *workspace, size_t workspace_bytes, size_t *workspace_needed,
+                                     void *stream);
+
+/*
  * pkv_paged_attn_combine — the log-sum-exp merge of split rows.
  *
  * For every row (t, h) that pkv_paged_attn split into n parts with partial

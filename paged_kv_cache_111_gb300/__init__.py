@@ -15,7 +15,8 @@ Calls (same names as the C ABI without the ``pkv_`` prefix):
 * ``copy_blocks(kv_cache, block_mapping)`` (copy-on-write of shared blocks)
 * ``paged_attn_shared_prefix(..., shared_prefix_blocks, workspace)`` (cascade:
   a batch sharing a table prefix reads the shared blocks once)
-* ``kv_write_fp8`` / ``paged_attn_fp8`` (E4M3 cache with per-tensor K and V scales)
+* ``kv_write_fp8`` / ``paged_attn_fp8`` / ``paged_attn_shared_prefix_fp8`` (E4M3 cache with per-tensor
+  K and V scales)
 
 plus ``paged_attn_workspace_size(...)`` (the C call's size query) and
 ``workspace_status(workspace)`` (reads the device status word).
@@ -36,7 +37,7 @@ __all__ = [
     "BLOCK_SIZE", "PagedKVError", "load", "kv_write", "paged_attn", "paged_attn_combine",
     "paged_attn_workspace_size", "workspace_status", "STATUS_NAMES", "library_path", "copy_blocks",
     "paged_attn_noalloc", "paged_attn_shared_prefix", "paged_attn_shared_prefix_workspace_size",
-    "kv_write_fp8", "paged_attn_fp8", "workspace_schedule",
+    "kv_write_fp8", "paged_attn_fp8", "paged_attn_shared_prefix_fp8", "workspace_schedule",
 ]
 
 BLOCK_SIZE = 16
@@ -91,6 +92,11 @@ def load():
                                            i32, ctypes.c_float, ctypes.c_float, ctypes.c_float, i32, P,
                                            ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t), P]
         lib.pkv_paged_attn_fp8.restype = ctypes.c_int
+        lib.pkv_paged_attn_shared_prefix_fp8.argtypes = [P, P, i64, P, i64, P, i32, P, P, i32, i32, i32, i32, i32,
+                                                         i32, i32, i32, ctypes.c_float, ctypes.c_float,
+                                                         ctypes.c_float, i32, i32, P, ctypes.c_size_t,
+                                                         ctypes.POINTER(ctypes.c_size_t), P]
+        lib.pkv_paged_attn_shared_prefix_fp8.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -255,6 +261,33 @@ def paged_attn_fp8(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Tenso
         hkv, d, bs, ctypes.c_float(scale), ctypes.c_float(k_scale), ctypes.c_float(v_scale), int(num_splits),
         _ptr(workspace), workspace.numel() * workspace.element_size(), ctypes.byref(need), _stream(out, stream))
     _check(rc, "pkv_paged_attn_fp8")
+
+
+def paged_attn_shared_prefix_fp8(out: torch.Tensor, query: torch.Tensor, kv_cache: torch.Tensor,
+                                 block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                                 max_query_len: int, max_seq_len: int, scale: float, k_scale: float, v_scale: float,
+                                 shared_prefix_blocks: int, workspace: torch.Tensor, num_splits: int = 0,
+                                 stream=None) -> None:
+    """paged_attn_shared_prefix over an E4M3 cache; the workspace is sized as for paged_attn_shared_prefix."""
+    _need_cuda(out, query, kv_cache, block_tables, seq_lens, query_start_loc, workspace)
+    if kv_cache.element_size() != 1:
+        raise ValueError("an FP8 cache holds one byte per element")
+    nb, hkv, _, bs, d = kv_cache.shape
+    T, H = int(query.shape[0]), int(query.shape[1])
+    if query.stride(2) != 1 or query.stride(1) != d:
+        raise ValueError("query must be [T, H, d] with contiguous heads")
+    if not out.is_contiguous() or tuple(out.shape) != (T, H, d):
+        raise ValueError("out must be a contiguous [T, H, d] tensor")
+    if block_tables.dim() != 2 or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous [num_seqs, max_blocks] tensor")
+    need = ctypes.c_size_t(0)
+    rc = load().pkv_paged_attn_shared_prefix_fp8(
+        _ptr(out), _ptr(query), query.stride(0), _ptr(kv_cache), nb, _ptr(block_tables), int(block_tables.shape[1]),
+        _ptr(seq_lens), _ptr(query_start_loc), int(seq_lens.shape[0]), T, int(max_query_len), int(max_seq_len), H,
+        hkv, d, bs, ctypes.c_float(scale), ctypes.c_float(k_scale), ctypes.c_float(v_scale), int(num_splits),
+        int(shared_prefix_blocks), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(need), _stream(out, stream))
+    _check(rc, "pkv_paged_attn_shared_prefix_fp8")
 
 
 def paged_attn_combine(out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:

@@ -107,7 +107,8 @@ int launch_decode_path(const CUtensorMap &map, const AttnParams &ap, int32_t hea
 // attend once to those blocks' keys, cut into `prefix_parts` ranges of KV
 // tiles; range i is split i of each row.
 int launch_prefix(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
-                  int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream);
+                  int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream,
+                  bool kv8 = false);
 
 // Is the tensor-core prefill kernel available for this head layout?
 inline bool prefill_supported(int num_q_heads, int num_kv_heads, int head_size) {

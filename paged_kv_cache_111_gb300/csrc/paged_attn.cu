@@ -651,10 +651,10 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PKV_ERR_SHAPE;
     if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale > 3.0e38f || v_scale > 3.0e38f) return PKV_ERR_SHAPE;
 
-    // long chunks go to the tensor-core tile kernel (over an E4M3 cache too);
-    // the shared-prefix pass reads bf16 pages only
+    // long chunks and the shared-prefix pass go to the tensor-core tile kernel
+    // (which widens an E4M3 cache's pages to f16 itself)
     const bool prefill_ok = prefill_supported(num_q_heads, num_kv_heads, head_size);
-    if (!prefill_ok || kv8) prefix_blocks = 0;
+    if (!prefill_ok) prefix_blocks = 0;
     const WsLayout lay = ws_layout(num_seqs, num_tokens, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
                                    head_size, prefix_blocks);
     if (workspace_needed) *workspace_needed = static_cast<size_t>(lay.total);
@@ -747,7 +747,7 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
         rc = launch_prefix(fp, query, query_token_stride, kv_cache, num_blocks, head_size,
                            std::min<int64_t>(std::min(sms, kStatsCtas), (lay.max_crows + kPrefillRows - 1) / kPrefillRows * num_kv_heads *
                                                       lay.prefix_parts),
-                           dev, st);
+                           dev, st, kv8);
         if (rc) return rc;
     }
     if (!may_prefill) return PKV_OK;
@@ -783,6 +783,23 @@ extern "C" int pkv_paged_attn_shared_prefix(void *out, const void *query, int64_
                                 max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_tokens, max_query_len,
                                 max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale, num_splits,
                                 shared_prefix_blocks, workspace, workspace_bytes, workspace_needed, stream);
+}
+
+extern "C" int pkv_paged_attn_shared_prefix_fp8(void *out, const void *query, int64_t query_token_stride,
+                                                const void *kv_cache, int64_t num_blocks,
+                                                const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                const int32_t *seq_lens, const int32_t *query_start_loc,
+                                                int32_t num_seqs, int32_t num_tokens, int32_t max_query_len,
+                                                int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                                int32_t head_size, int32_t block_size, float scale, float k_scale,
+                                                float v_scale, int32_t num_splits, int32_t shared_prefix_blocks,
+                                                void *workspace, size_t workspace_bytes, size_t *workspace_needed,
+                                                void *stream) {
+    return pkv::paged_attn_impl(out, query, query_token_stride, kv_cache, num_blocks, block_tables,
+                                max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_tokens, max_query_len,
+                                max_seq_len, num_q_heads, num_kv_heads, head_size, block_size, scale, num_splits,
+                                shared_prefix_blocks, workspace, workspace_bytes, workspace_needed, stream, true,
+                                k_scale, v_scale);
 }
 
 extern "C" int pkv_paged_attn_combine(void *out, const void *workspace, size_t workspace_bytes, int32_t num_tokens,

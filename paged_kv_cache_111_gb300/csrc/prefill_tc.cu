@@ -193,7 +193,6 @@ template <int HD, bool CASCADE, bool KV8>
 __global__ void __launch_bounds__(384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16 *__restrict__ query,
                    const int64_t q_stride, const PrefillParams p) {
-    static_assert(!(CASCADE && KV8), "the shared-prefix pass reads bf16 pages");
     using Cfg = PrefillCfg<HD, KV8>;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -965,11 +964,15 @@ static int make_page_map_e4m3(CUtensorMap *kvm, const void *kv_cache, int64_t nu
                               int32_t head_size);
 
 int launch_prefix(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
-                  int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream) {
+                  int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream, bool kv8) {
     if (grid <= 0) return PKV_OK;
     CUtensorMap kvm;
-    const int rc = make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
+    const int rc = kv8 ? make_page_map_e4m3(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size)
+                       : make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
     if (rc) return rc;
+    if (kv8)
+        return head_size == 64 ? launch_prefill_hd<64, true, true>(p, kvm, query, q_stride, grid, dev, stream)
+                               : launch_prefill_hd<128, true, true>(p, kvm, query, q_stride, grid, dev, stream);
     if (head_size == 64) return launch_prefill_hd<64, true, false>(p, kvm, query, q_stride, grid, dev, stream);
     return launch_prefill_hd<128, true, false>(p, kvm, query, q_stride, grid, dev, stream);
 }

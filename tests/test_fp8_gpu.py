@@ -181,3 +181,39 @@ def test_fp8_argument_errors():
     with pytest.raises(pkv.PagedKVError):
         pkv.paged_attn_fp8(out, dev["query"], cache, dev["block_tables"], dev["seq_lens"], dev["query_start_loc"],
                            step.max_query_len, step.max_seq_len, step.scale, -1.0, 1.0, ws)
+
+
+def run_fp8_cascade(step, k_scale, v_scale, prefix_blocks, num_splits=0):
+    dev = to_dev(step)
+    cache = gpu_fp8_cache(step, k_scale, v_scale, dev)
+    n = pkv.paged_attn_shared_prefix_workspace_size(step.num_seqs, step.num_tokens, step.max_query_len,
+                                                    step.max_seq_len, step.num_q_heads, step.num_kv_heads,
+                                                    step.head_size, prefix_blocks)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    out = torch.full((step.num_tokens, step.num_q_heads, step.head_size), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    pkv.paged_attn_shared_prefix_fp8(out, dev["query"], cache, dev["block_tables"], dev["seq_lens"],
+                                     dev["query_start_loc"], step.max_query_len, step.max_seq_len, step.scale,
+                                     k_scale, v_scale, prefix_blocks, ws, num_splits=num_splits)
+    pkv.paged_attn_combine(out, ws)
+    torch.cuda.synchronize()
+    assert pkv.workspace_status(ws) == 0
+    return out
+
+
+def test_attention_fp8_shared_prefix_workload_full_size():
+    # 64 sharers of a 1024-token prefix plus forks: the prefix's E4M3 pages are
+    # widened once per kv head for every sharer on the tensor-core kernel
+    step = wl.make_workload("llama3-70b-prefix")
+    out = run_fp8_cascade(step, 0.011, 0.009, 64)
+    _, ref, _ = oracle.run_step_fp8(step, 0.011, 0.009)
+    check_close(out, ref, "70b prefix cascade fp8")
+
+
+@pytest.mark.parametrize("splits", [0, 3, 32])
+def test_attention_fp8_shared_prefix_with_multi_token_rows(splits):
+    specs = [wl.RequestSpec(300, 1), wl.RequestSpec(170, 2), wl.RequestSpec(520, 1), wl.RequestSpec(128, 2)]
+    step = wl.build_step("fp8 cascade", specs, 16, 4, 64, 256, 71, shared_prefix_len=128)
+    out = run_fp8_cascade(step, 0.02, 0.03, 8, num_splits=splits)
+    _, ref, _ = oracle.run_step_fp8(step, 0.02, 0.03)
+    check_close(out, ref, f"fp8 cascade splits={splits}")
