@@ -27,7 +27,8 @@
 // next costs about a third of the tensor pipe's rate.
 // Warp roles: warp 0 loads (TMA: K and V pages through the block table into
 // a three-stage ring), warp 1 issues the MMAs, warp 2 owns the
-// tensor-memory allocation, warps 4-11 do softmax and the epilogue.
+// tensor-memory allocation, warps 4-11 do softmax and the epilogue; over an
+// E4M3 cache warps 2, 3, 12 and 13 widen the raw pages to f16.
 //
 // When any row of the tile puts a large share of its weight on few keys of
 // a KV tile (rows with few visible keys, or a peaked softmax), that tile's P
@@ -190,7 +191,7 @@ static_assert(kItemSlots * sizeof(PfItem) <= 256, "item ring fits its 256 bytes"
 // across items, so the loads, the first products and the Q of the next item
 // overlap the epilogue of the current one.
 template <int HD, bool CASCADE, bool KV8>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16 *__restrict__ query,
                    const int64_t q_stride, const PrefillParams p) {
     using Cfg = PrefillCfg<HD, KV8>;
@@ -228,8 +229,11 @@ __global__ void __launch_bounds__(384, 1)
             int count = 1;
             if (b == kPFull0 || b == kPFull1 || b == kQFull || b == kOFree) count = 8;
             else if (b >= kXchg0 && b <= kXchg3) count = 2;
-            else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = KV8 ? 11 : 9;   // + converters
-            else if (b == kREmpty0 || b == kREmpty1) count = 2;      // both converter warps
+            else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = KV8 ? 13 : 9;   // + converters
+            else if (b == kREmpty0 || b == kREmpty1) count = 4;      // every converter warp
+            else if (KV8 && (b == kKFull0 || b == kKFull1 || b == kKFull2 || b == kVFull0 || b == kVFull1 ||
+                             b == kVFull2 || b == kVFix0 || b == kVFix1 || b == kVFix2))
+                count = 2;                                           // the two converters of K (of V)
             mbar_init(&bars[b], count);
         }
         tma_prefetch_desc(&kv_map);
@@ -489,11 +493,14 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
         __syncwarp();
-    } else if (KV8 && (warp == 2 || warp == 3)) {
+    } else if (KV8 && (warp == 2 || warp == 3 || warp >= 12)) {
         // ---------------- converters (E4M3 cache): raw tiles -> f16 tiles ----------------
-        // warp 2 widens K, warp 3 widens V and zeroes V rows past the sequence
-        // end (its scores there are masked, but NaN times a zero weight is NaN)
-        const bool isv = warp == 3;
+        // warps 2 and 12 widen K, 3 and 13 widen V (and zero V rows past the
+        // sequence end: their scores are masked, but NaN times a zero weight
+        // is NaN); warps 2 and 3 take the tile's first 64 keys, 12 and 13 the
+        // rest.  They sit on four different schedulers.
+        const bool isv = (warp & 1) != 0;
+        const int row0 = warp >= 12 ? kPrefillKeys / 2 : 0;
         bool ok = true;
         int gj = 0;
         for (int k = 0; ok; ++k) {
@@ -523,10 +530,10 @@ __global__ void __launch_bounds__(384, 1)
                 // 16-element pieces: raw row r bytes 16c .. 16c + 15 -> 16-bit tile row r,
                 // 64-column box c / 4, 16-byte chunks 2c % 8 and 2c % 8 + 1 at their
                 // 128-byte-swizzle places
-                constexpr int kPieces = kPrefillKeys * HD / 16;
+                constexpr int kPieces = kPrefillKeys / 2 * HD / 16;      // this warp's half of the rows
 #pragma unroll 4
                 for (int u = lane; u < kPieces; u += 32) {
-                    const int r = u / (HD / 16), c = u % (HD / 16);
+                    const int r = row0 + u / (HD / 16), c = u % (HD / 16);
                     uint32_t w[4];
                     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
@@ -557,7 +564,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             gj += n_kv;
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
         // ---------------- softmax + epilogue: two threads per row ----------------
         // warps 4-7 take keys (and output columns) of the first half of the tile,
         // warps 8-11 the second half; warp w reads tensor-memory lanes of quadrant
@@ -952,7 +959,7 @@ static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, con
             done_mask |= bit;
         }
     }
-    if (launch_pdl(prefill_kernel<HD, CASCADE, KV8>, dim3(static_cast<unsigned>(grid)), dim3(384), Cfg::kSmem, stream,
+    if (launch_pdl(prefill_kernel<HD, CASCADE, KV8>, dim3(static_cast<unsigned>(grid)), dim3(KV8 ? 448 : 384), Cfg::kSmem, stream,
                    kvm, static_cast<const __nv_bfloat16 *>(query), q_stride, p) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
