@@ -27,15 +27,21 @@
 // next costs about a third of the tensor pipe's rate.
 // Warp roles: warp 0 loads (TMA: K and V pages through the block table into
 // a three-stage ring), warp 1 issues the MMAs, warp 2 owns the
-// tensor-memory allocation, warps 4-11 do softmax and the epilogue; over an
-// E4M3 cache warps 2, 3, 12 and 13 widen the raw pages to f16.
+// tensor-memory allocation, warps 4-11 do softmax and the epilogue.
+//
+// Over an E4M3 cache (KV8) the pages land raw in a ring of their own, and
+// warps 2, 3, 12 and 13 widen them to f16 (exact) into the 16-bit ring; Q
+// rows are scaled by a power of two into f16, P is f16, and the products
+// are kind::f16 with f16 operands.  k_scale enters the score factor and
+// v_scale the epilogue.
 //
 // When any row of the tile puts a large share of its weight on few keys of
 // a KV tile (rows with few visible keys, or a peaked softmax), that tile's P
-// also enters P V as its bf16 remainder (a second MMA), keeping ~16 bits per
-// weight; other tiles' weights are each small and bf16 P is enough.  V rows past the sequence end in
-// its last page are zeroed before P V, so NaN in unwritten cache slots never
-// meets a zero weight.  Every wait is bounded.
+// also enters P V as its 16-bit remainder (a second MMA), keeping ~16 bits
+// per weight; other tiles' weights are each small and one 16-bit P is
+// enough.  V rows past the sequence end in its last page are zeroed before
+// P V, so NaN in unwritten cache slots never meets a zero weight.  Every
+// wait is bounded.
 #include <mutex>
 
 #include "attn_internal.cuh"
