@@ -456,10 +456,11 @@ def oracle_sample(step: wl.Step, n_req: int, seed: int) -> wl.Step:
     return step.subset(sorted(idx.tolist()))
 
 
-def time_oracle_step(sub: wl.Step, fp8_scales=None):
+def time_oracle_step(sub: wl.Step, fp8_scales=None, num_threads: int = 0):
     """One oracle step on ``sub``: cache write of the new tokens + attention
-    (over an E4M3 cache when fp8_scales = (k_scale, v_scale) is given).
-    Returns (seconds, algorithmic bytes of the sample, threads)."""
+    (over an E4M3 cache when fp8_scales = (k_scale, v_scale) is given), on
+    num_threads host threads (0: all).  Returns (seconds, algorithmic bytes
+    of the sample, threads)."""
     import oracle
     if fp8_scales is None:
         cache = oracle.new_cache(sub.num_blocks, sub.num_kv_heads, sub.head_size)
@@ -467,18 +468,18 @@ def time_oracle_step(sub: wl.Step, fp8_scales=None):
         t0 = time.perf_counter()
         oracle.kv_write(cache, sub.key, sub.value, sub.slot_mapping)
         oracle.paged_attn(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
-                          sub.num_q_heads, sub.scale)
+                          sub.num_q_heads, sub.scale, num_threads)
         dt = time.perf_counter() - t0
-        return dt, algorithmic_bytes(sub)["step"], oracle.max_threads()
+        return dt, algorithmic_bytes(sub)["step"], num_threads or oracle.max_threads()
     ks, vs = fp8_scales
     cache = oracle.new_cache_fp8(sub.num_blocks, sub.num_kv_heads, sub.head_size)
     oracle.kv_write_fp8(cache, sub.hist_key, sub.hist_value, sub.hist_slot_mapping, ks, vs)
     t0 = time.perf_counter()
     oracle.kv_write_fp8(cache, sub.key, sub.value, sub.slot_mapping, ks, vs)
     oracle.paged_attn_fp8(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
-                          sub.num_q_heads, sub.scale, ks, vs)
+                          sub.num_q_heads, sub.scale, ks, vs, num_threads)
     dt = time.perf_counter() - t0
-    return dt, algorithmic_bytes(sub, 1)["step"], oracle.max_threads()
+    return dt, algorithmic_bytes(sub, 1)["step"], num_threads or oracle.max_threads()
 
 
 def fp8_scales(step: wl.Step):
@@ -504,10 +505,23 @@ def cpu_baseline(step: wl.Step, budget_s: float = 10.0, scales=None) -> dict:
         if len(times) >= 50:
             break
     mean = sum(times) / len(times)
+    # the same oracle on one host thread, on a smaller sample (a sixteenth of the requests)
+    sub1 = oracle_sample(step, max(1, step.num_seqs // 16), 8)
+    t1, n1 = [], 0
+    t_end = time.perf_counter() + budget_s / 2
+    while len(t1) < 2 or time.perf_counter() < t_end:
+        dt, n1, _ = time_oracle_step(sub1, scales, num_threads=1)
+        t1.append(dt)
+        if len(t1) >= 20:
+            break
+    mean1 = sum(t1) / len(t1)
     return {"value": nbytes / mean / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{sub.num_seqs} of {step.num_seqs} requests ({sub.num_tokens} query tokens), "
                       f"{len(times)} timed oracle steps (cache write + attention), mean {mean * 1e3:.1f} ms",
-            "tokens_per_s": sub.num_tokens / mean}
+            "tokens_per_s": sub.num_tokens / mean,
+            "single_thread": {"value": n1 / mean1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{sub1.num_seqs} of {step.num_seqs} requests, {len(t1)} timed oracle steps, "
+                                        f"mean {mean1 * 1e3:.1f} ms"}}
 
 
 def run_reference(args, rank: int, world: int) -> None:
