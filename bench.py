@@ -111,7 +111,7 @@ def shared_prefix_blocks(step: wl.Step) -> int:
     return min(k, ctx_min // step.block_size)
 
 
-def launches_per_step(step: wl.Step, prefix_blocks: int, fp8: bool = False) -> int:
+def launches_per_step(step: wl.Step, prefix_blocks: int) -> int:
     """Kernels of one layer-step: kv_write, plan, decode, combine; the prefill
     kernel when some request has more than 64 rows (q_r * G) and the head
     layout has a tensor-core tile; the shared-prefix kernel when asked for."""
@@ -439,7 +439,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
         probe_gbs = 2 * n * 2 / (best * 1e-3) / 1e9
         del a, b
 
-    return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K, fp8),
+    return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K),
             "fp8_scales": scales,
             "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
             "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "probe_gbs": probe_gbs,

@@ -52,8 +52,8 @@ __device__ __forceinline__ KvVec kv_vec(int64_t i, bool narrow, int per_tok, int
     return v;
 }
 
-// Cache index (in vectors of `per_vec_bytes`) of vector rr of K or V of a
-// token written to `slot`.
+// Cache index, in units of one vector per 8 elements (16 bytes of bf16, 8
+// bytes of E4M3), of vector rr of K or V of a token written to `slot`.
 __device__ __forceinline__ int64_t kv_dst(const KvWriteParams &p, int64_t slot, int which, int rr) {
     const int vpr = 1 << p.vec_shift;
     const int64_t blk = slot / kBlock;
