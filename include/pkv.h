@@ -327,9 +327,9 @@ int pkv_copy_blocks(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
  *
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate GPU memory where they run attention (for example code
- * under a strict no-allocation policy while a CUDA graph is captured, or a
- * plugin whose host engine owns all device memory and passes in only inputs
- * and outputs).  It computes exactly what pkv_paged_attn followed by
+ * in a serving loop under a strict no-allocation policy, or a plugin whose
+ * host engine owns all device memory and passes in only inputs and
+ * outputs).  It computes exactly what pkv_paged_attn followed by
  * pkv_paged_attn_combine computes, with the same arguments except the
  * workspace: the scratch lives in a fixed array of this library's own device
  * memory, PKV_NOALLOC_SCRATCH_BYTES (256 MiB) on every GPU where the call's

@@ -1,10 +1,10 @@
 // Paged attention for callers that cannot allocate GPU memory.
 //
 // Some callers cannot call cudaMalloc (or any allocator) at the point where
-// they run attention: code running inside a region being captured into a
-// CUDA graph with a strict no-allocation policy, plugins of a host engine
-// that owns all device memory and hands out only inputs and outputs, or
-// embedded runtimes that forbid allocation after start-up.  For them this
+// they run attention: code in a serving loop under a strict no-allocation
+// policy, plugins of a host engine that owns all device memory and hands
+// out only inputs and outputs, or embedded runtimes that forbid allocation
+// after start-up.  For them this
 // file offers one entry point that needs no workspace from the caller: the
 // scratch that pkv_paged_attn keeps in its workspace lives instead in a
 // fixed-size array of this library's own device memory.

@@ -1,8 +1,8 @@
 """The allocation-free entry point, pkv_paged_attn_noalloc.
 
 It serves callers that cannot allocate GPU memory where they run attention
-(a strict no-allocation region while a CUDA graph is captured, or a plugin
-whose host engine hands it only inputs and outputs): instead of a caller
+(code under a strict no-allocation policy, or a plugin whose host engine
+hands it only inputs and outputs): instead of a caller
 workspace it uses a fixed scratch array inside the library.  These tests
 call it through the C ABI and compare it with the workspace path
 (pkv_paged_attn + pkv_paged_attn_combine) on the same inputs, on two calls
