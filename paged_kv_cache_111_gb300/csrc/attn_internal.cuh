@@ -90,9 +90,10 @@ struct AttnParams {
     uint8_t *ws;
 };
 
-// Decode grid: persistent CTAs of kDecodeWarps warps, kDecodeCtasPerSm per SM.
+// Decode grid: persistent CTAs of kDecodeWarps warps, decode_ctas_per_sm()
+// per SM (set by the tiling of the head size and cache type).
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeCtasPerSm = 2;
+int decode_ctas_per_sm(int32_t head_size, bool kv8);
 
 // Tensor map of the cache for the decode kernel (bf16 or E4M3 pages).
 int make_decode_map(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,

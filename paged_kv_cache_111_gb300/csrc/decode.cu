@@ -139,8 +139,24 @@ __device__ __forceinline__ void widen_e4m3_values(uint32_t src, uint32_t dst, in
     }
 }
 
+// Decode tiling per head size and cache type: warps per CTA, ring stages per
+// warp, resident CTAs per SM (the launch bound, so the registers fit).  At
+// d = 64 a bf16 page is 4 KiB: four CTAs of three-stage rings (16 warps of
+// independent page chains, 128 registers) keep more chunks in flight than
+// two CTAs of six stages.
+template <int HD, bool KV8 = false> struct DecodeTiling;
+template <> struct DecodeTiling<64> { static constexpr int NW = 4, DEPTH = 3, CTAS_PER_SM = 4; };
+template <> struct DecodeTiling<128> { static constexpr int NW = 4, DEPTH = 3, CTAS_PER_SM = 2; };
+// E4M3 pages are half the bytes: more stages in flight, plus one staging page per warp
+template <> struct DecodeTiling<64, true> { static constexpr int NW = 4, DEPTH = 8, CTAS_PER_SM = 2; };
+template <> struct DecodeTiling<128, true> { static constexpr int NW = 4, DEPTH = 4, CTAS_PER_SM = 2; };
+
+static_assert(DecodeTiling<64>::NW == kDecodeWarps && DecodeTiling<128>::NW == kDecodeWarps &&
+                  DecodeTiling<64, true>::NW == kDecodeWarps && DecodeTiling<128, true>::NW == kDecodeWarps,
+              "every decode tiling has kDecodeWarps warps per CTA");
+
 template <int HD, int NW, int DEPTH, bool KV8>
-__global__ void __launch_bounds__(NW * 32, 1)
+__global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
     using Cfg = DecodeCfg<HD, NW, DEPTH, KV8>;
     using Math = DecodeMath<KV8>;
@@ -569,6 +585,9 @@ static int make_kv_map_e4m3(CUtensorMap *map, const void *kv_cache, int64_t num_
 template <int HD, int NW, int DEPTH, bool KV8>
 static int launch_decode(const CUtensorMap &map, const AttnParams &p, int grid, int dev, cudaStream_t stream) {
     using Cfg = DecodeCfg<HD, NW, DEPTH, KV8>;
+    // 228 KiB of shared memory per SM, 1 KiB of it reserved per resident CTA
+    static_assert((Cfg::kSmem + 1024) * DecodeTiling<HD, KV8>::CTAS_PER_SM <= 228 * 1024,
+                  "the tiling's CTAs fit one SM's shared memory");
     static std::mutex mu;
     static uint64_t done_mask = 0;       // devices whose shared-memory limit is already raised
     {
@@ -587,25 +606,16 @@ static int launch_decode(const CUtensorMap &map, const AttnParams &p, int grid, 
     return PKV_OK;
 }
 
-// decode tiling per head size: warps per CTA, ring stages per warp, CTAs per SM
-template <int HD, bool KV8 = false> struct DecodeTiling;
-template <> struct DecodeTiling<64> { static constexpr int NW = 4, DEPTH = 6, CTAS_PER_SM = 2; };
-template <> struct DecodeTiling<128> { static constexpr int NW = 4, DEPTH = 3, CTAS_PER_SM = 2; };
-// E4M3 pages are half the bytes: more stages in flight, plus one staging page per warp
-template <> struct DecodeTiling<64, true> { static constexpr int NW = 4, DEPTH = 8, CTAS_PER_SM = 2; };
-template <> struct DecodeTiling<128, true> { static constexpr int NW = 4, DEPTH = 4, CTAS_PER_SM = 2; };
-
-
-static_assert(DecodeTiling<64>::NW == kDecodeWarps && DecodeTiling<128>::NW == kDecodeWarps &&
-                  DecodeTiling<64, true>::NW == kDecodeWarps && DecodeTiling<128, true>::NW == kDecodeWarps,
-              "every decode tiling has kDecodeWarps warps per CTA");
-static_assert(DecodeTiling<64>::CTAS_PER_SM == kDecodeCtasPerSm && DecodeTiling<128>::CTAS_PER_SM == kDecodeCtasPerSm,
-              "bf16 decode tilings fit kDecodeCtasPerSm CTAs per SM");
 
 int make_decode_map(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
                     int32_t head_size, bool kv8) {
     return kv8 ? make_kv_map_e4m3(map, kv_cache, num_blocks, num_kv_heads, head_size)
                : make_kv_map(map, kv_cache, num_blocks, num_kv_heads, head_size);
+}
+
+int decode_ctas_per_sm(int32_t head_size, bool kv8) {
+    if (kv8) return head_size == 64 ? DecodeTiling<64, true>::CTAS_PER_SM : DecodeTiling<128, true>::CTAS_PER_SM;
+    return head_size == 64 ? DecodeTiling<64>::CTAS_PER_SM : DecodeTiling<128>::CTAS_PER_SM;
 }
 
 int launch_decode_path(const CUtensorMap &map, const AttnParams &ap, int32_t head_size, bool kv8, int grid, int dev,

@@ -681,7 +681,7 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     if (rc) return rc;
 
     const int nw = kDecodeWarps;
-    const int per_sm = kDecodeCtasPerSm;
+    const int per_sm = decode_ctas_per_sm(head_size, kv8);
     int64_t grid = static_cast<int64_t>(sms) * per_sm;
     const int64_t max_items = lay.max_chunks * num_kv_heads;
     if (grid > (max_items + nw - 1) / nw) grid = (max_items + nw - 1) / nw;
