@@ -217,3 +217,30 @@ def test_attention_fp8_shared_prefix_with_multi_token_rows(splits):
     out = run_fp8_cascade(step, 0.02, 0.03, 8, num_splits=splits)
     _, ref, _ = oracle.run_step_fp8(step, 0.02, 0.03)
     check_close(out, ref, f"fp8 cascade splits={splits}")
+
+
+@pytest.mark.parametrize("bad_request", [0, 1])
+def test_fp8_out_of_pool_block_is_reported(bad_request):
+    """A block id past the pool, in a decode row (request 0) or in a chunk on
+    the widening tensor-core kernel (request 1), loads as zeros and is
+    reported; the other request's rows are unaffected."""
+    step = custom([(40, 1), (10, 150)], 8, 2, 128, seed=13)
+    ks, vs = 0.011, 0.019
+    dev = to_dev(step)
+    cache = gpu_fp8_cache(step, ks, vs, dev)
+    n = pkv.paged_attn_workspace_size(step.num_seqs, step.num_tokens, step.max_query_len, step.max_seq_len,
+                                      8, 2, 128)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    bt = dev["block_tables"].clone()
+    bt[bad_request, 2] = step.num_blocks + 1000
+    out = torch.zeros(step.num_tokens, 8, 128, dtype=torch.bfloat16, device="cuda")
+    pkv.paged_attn_fp8(out, dev["query"], cache, bt, dev["seq_lens"], dev["query_start_loc"], step.max_query_len,
+                       step.max_seq_len, step.scale, ks, vs, ws)
+    pkv.paged_attn_combine(out, ws)
+    torch.cuda.synchronize()
+    assert pkv.workspace_status(ws) == 7          # PKV_ERR_DEVICE_INDEX
+    good = 1 - bad_request
+    q0, q1 = int(step.query_start_loc[good]), int(step.query_start_loc[good + 1])
+    _, ref, _ = oracle.run_step_fp8(step.subset([good]), ks, vs)
+    check_close(out[q0:q1], ref, "request beside the bad block")
+

@@ -187,6 +187,28 @@ def test_device_errors_are_reported_without_a_fault():
     assert (other == 0).all()
 
 
+def test_out_of_pool_block_in_a_tensor_core_chunk_is_reported():
+    """A block id past the pool in a chunk on the tensor-core kernel loads as
+    zeros (the TMA box lies outside the tensor map) and is reported; the other
+    request's row is unaffected."""
+    step = custom([(40, 1), (10, 150)], 8, 2, 128, seed=12)          # request 1: 600 rows, tcgen05 tiles
+    dev = to_dev(step)
+    pool = new_pool(step)
+    write_history(step, pool, dev)
+    pkv.kv_write(pool, dev["key"], dev["value"], dev["slot_mapping"])
+    ws = workspace_for(step)
+    bt = dev["block_tables"].clone()
+    bt[1, 3] = step.num_blocks + 1000
+    out = torch.zeros(step.num_tokens, 8, 128, dtype=torch.bfloat16, device="cuda")
+    pkv.paged_attn(out, dev["query"], pool, bt, dev["seq_lens"], dev["query_start_loc"],
+                   step.max_query_len, step.max_seq_len, step.scale, ws)
+    pkv.paged_attn_combine(out, ws)
+    torch.cuda.synchronize()
+    assert pkv.workspace_status(ws) == 7          # PKV_ERR_DEVICE_INDEX
+    _, ref, _ = oracle.run_step(step.subset([0]))
+    check_close(out[:1], ref, "request beside the bad chunk")
+
+
 def test_workspace_query_and_too_small_workspace():
     step = custom([(40, 1)], 4, 2, 64, seed=12)
     need = pkv.paged_attn_workspace_size(1, 1, 1, 41, 4, 2, 64)
