@@ -208,27 +208,33 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 }
 
 // Exclusive scan of `count[b]` in descending bin order into `cursor[b]`, by
-// one warp (8 bins per lane); returns the total.
+// one warp; returns the total.  Lane l holds the 8 bins 248 - 8l .. 255 - 8l
+// (two 16-byte shared-memory accesses each way, free of bank conflicts), so
+// lane 0 holds the largest sizes and its prefix is the warp scan's.
+static_assert(kSizeBins == 32 * 8, "one warp scans the size bins, 8 per lane");
 __device__ int scan_bins_desc(const int *count, int *cursor, int lane) {
-    int local[8];
-    int sum = 0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        local[e] = count[kSizeBins - 1 - (lane * 8 + e)];
-        sum += local[e];
-    }
+    const int base = kSizeBins - 8 * (lane + 1);
+    const int4 lo = *reinterpret_cast<const int4 *>(count + base);        // bins base .. base + 3
+    const int4 hi = *reinterpret_cast<const int4 *>(count + base + 4);    // bins base + 4 .. base + 7
+    const int sum = lo.x + lo.y + lo.z + lo.w + hi.x + hi.y + hi.z + hi.w;
     int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
     }
-    int acc = incl - sum;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        cursor[kSizeBins - 1 - (lane * 8 + e)] = acc;
-        acc += local[e];
-    }
+    int acc = incl - sum;                 // sizes above this lane's bins
+    int4 chi, clo;                        // descending: base + 7 first
+    chi.w = acc; acc += hi.w;
+    chi.z = acc; acc += hi.z;
+    chi.y = acc; acc += hi.y;
+    chi.x = acc; acc += hi.x;
+    clo.w = acc; acc += lo.w;
+    clo.z = acc; acc += lo.z;
+    clo.y = acc; acc += lo.y;
+    clo.x = acc;
+    *reinterpret_cast<int4 *>(cursor + base) = clo;
+    *reinterpret_cast<int4 *>(cursor + base + 4) = chi;
     return __shfl_sync(0xffffffffu, incl, 31);
 }
 
@@ -300,10 +306,11 @@ __device__ int4 block_scan4(int a, int b, int c, int d, int4 *warp_tot, int4 *to
 constexpr int kPlanStagedSeqs = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
-    __shared__ int bin_count[kSizeBins];
-    __shared__ int bin_cursor[kSizeBins];
-    __shared__ int pbin_count[kSizeBins];
-    __shared__ int pbin_cursor[kSizeBins];
+    __shared__ __align__(16) int bin_count[kSizeBins];
+    __shared__ __align__(16) int bin_cursor[kSizeBins];
+    __shared__ __align__(16) int pbin_count[kSizeBins];
+    __shared__ __align__(16) int pbin_cursor[kSizeBins];
+    __shared__ int bin_total[2];
     __shared__ int4 warp_tot[kPlanThreads / 32];
     __shared__ int4 totals;
     __shared__ unsigned long long total_pages;
@@ -482,17 +489,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         else agg_inc(bin_count, min(pg.y - pg.x, kSizeBins - 1));
     }
     __syncthreads();
-    if (tid < 32) {                                   // largest first
-        const int acc = scan_bins_desc(bin_count, bin_cursor, tid);
-        const int pacc = scan_bins_desc(pbin_count, pbin_cursor, tid);
-        if (tid == 0) {
-            const bool ok = fits && acc <= p.lay.max_chunks && pacc <= p.lay.max_ptiles;
-            hdr->n_chunks = ok ? acc : 0;
-            hdr->n_ptiles = ok ? pacc : 0;
-            if (!fits) bad = 1;
-        }
+    if (tid < 64) {                                   // largest first; warp 0 decode chunks, warp 1 tiles
+        const bool tiles = tid >= 32;
+        const int acc = scan_bins_desc(tiles ? pbin_count : bin_count, tiles ? pbin_cursor : bin_cursor, tid & 31);
+        if ((tid & 31) == 0) bin_total[tiles ? 1 : 0] = acc;
     }
     __syncthreads();
+    if (tid == 0) {
+        const bool ok = fits && bin_total[0] <= p.lay.max_chunks && bin_total[1] <= p.lay.max_ptiles;
+        hdr->n_chunks = ok ? bin_total[0] : 0;
+        hdr->n_ptiles = ok ? bin_total[1] : 0;
+        if (!fits) bad = 1;
+    }
 
     // pass 4: emit every chunk at its sorted position
     for (int c = tid; c < n_emit; c += nthr) {
