@@ -48,6 +48,12 @@ DECODE_TRAFFIC = {"sources_sha256_16": "9fccdd05fa44c3f6", "ratio": (1.042259 + 
                   "profile": "profiles/decode_kernel_llama13b-decode-64req.md"}
 
 
+def percentiles(values, fractions=(0.1, 0.5, 0.9)):
+    """Nearest-rank percentiles of a non-empty list (each fraction in [0, 1])."""
+    q = sorted(values)
+    return [q[min(len(q) - 1, max(0, math.ceil(f * len(q)) - 1))] for f in fractions]
+
+
 def decode_sources_hash() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -325,7 +331,8 @@ def run_gpu(args, rank: int, world: int) -> dict:
         torch.sum(flush_bufs[1], dim=0, out=flush_sink)
 
     def run_steps(n_steps, phase_events):
-        """Time n_steps steps on the device; returns (mean ms per step, phase ms or None)."""
+        """Time n_steps steps on the device; returns (mean ms per step, phase ms or None,
+        per-step ms or None)."""
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
@@ -346,6 +353,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
             per = [e[0].elapsed_time(e[-1]) for e in ev]
             mean = sum(per) / n_steps
         else:
+            per = None
             ev[0][0].record(stream)
             for _ in range(n_steps):
                 if graph is not None:
@@ -360,19 +368,20 @@ def run_gpu(args, rank: int, world: int) -> dict:
         phases = None
         if phase_events and graph is None:
             phases = tuple(sum(e[k].elapsed_time(e[k + 1]) for e in ev) / n_steps for k in range(3))
-        return mean, phases
+        return mean, phases, per
 
     # the headline: steps back to back (no event between the kernels of a step)
     with ClockSampler(dev.index) as clk:
-        step_ms, _ = run_steps(args.steps, False)
+        step_ms, _, _ = run_steps(args.steps, False)
     total_ms = step_ms * args.steps
     # the phase breakdown (kv_write, paged_attn, combine), events between the calls
     if graph is None:
-        _, (kvw_ms, attn_ms, comb_ms) = run_steps(min(args.steps, 300), True)
+        _, (kvw_ms, attn_ms, comb_ms), phase_per = run_steps(min(args.steps, 300), True)
     else:
         # one graph per step: the phases are not separable; attribute the step
         kvw_ms = comb_ms = float("nan")
         attn_ms = step_ms
+        phase_per = None
     status = pkv.workspace_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {pkv.STATUS_NAMES.get(status, status)}")
@@ -457,6 +466,7 @@ def run_gpu(args, rank: int, world: int) -> dict:
     return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K),
             "fp8_scales": scales,
             "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
+            "phase_step_ms": phase_per,
             "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "probe_gbs": probe_gbs,
             "l2_flush": flush, "l2_bytes": l2_bytes}
 
@@ -677,6 +687,9 @@ def main():
         "us_per_step": {k: (v * 1e3 if v == v else None) for k, v in
                         (("kv_write", r["kvw_ms"]), ("paged_attn", r["attn_ms"]), ("combine", r["comb_ms"]),
                          ("total", ms_per_step))},
+        # the phase pass times each step on its own: its spread (events between the calls included)
+        "phase_pass_step_us_p10_p50_p90": ([round(v * 1e3, 2) for v in percentiles(r["phase_step_ms"])]
+                                           if r["phase_step_ms"] else None),
         "roofline": roofline(ab, r["attn_ms"], pk),
         "copy_probe_gbs": r["probe_gbs"],
         "e2e": ({"value": job_throughput(ab["step"], world, e2e_max), "unit": "GB/s",

@@ -57,3 +57,9 @@ def test_job_throughput_counts_every_rank():
     assert bench.job_throughput(1e9, 1, 1.0) == pytest.approx(1000.0)
     assert bench.job_throughput(1e9, 4, 2.0) == pytest.approx(2000.0)
     assert bench.max_over_ranks([1.5, 2.5], 1) == [1.5, 2.5]
+
+
+def test_step_percentiles_are_nearest_rank():
+    assert bench.percentiles(list(range(1, 11))) == [1, 5, 9]
+    assert bench.percentiles([7.5]) == [7.5, 7.5, 7.5]
+    assert bench.percentiles([3.0, 1.0, 2.0], (0.0, 1.0)) == [1.0, 3.0]
