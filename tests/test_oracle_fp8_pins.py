@@ -90,6 +90,9 @@ def test_encode_matches_brute_force_search():
 def test_saturation_and_signed_zero():
     assert oracle.e4m3_encode(448.0) == 0x7E
     assert oracle.e4m3_encode(464.0) == 0x7E
+    # past the tie at 464 the nearest step up (480) is no E4M3 value: held at 448, never the NaN code
+    for v in (464.5, 470.0, 479.0, 479.99, 480.0, 500.0):
+        assert oracle.e4m3_encode(v) == 0x7E and oracle.e4m3_encode(-v) == 0xFE
     assert oracle.e4m3_encode(1.0e30) == 0x7E
     assert oracle.e4m3_encode(float("inf")) == 0x7E
     assert oracle.e4m3_encode(-float("inf")) == 0xFE

@@ -48,6 +48,11 @@ MUTANTS = [
     ("e4m3 mantissa truncated", "const int m = (int)nearbyint((2.0 * fr - 1.0) * 8.0);",
      "const int m = (int)floor((2.0 * fr - 1.0) * 8.0);"),
     ("e4m3 subnormal step", "code = (int)nearbyint(ldexp(a, 9));", "code = (int)nearbyint(ldexp(a, 8));"),
+    ("e4m3 ties away from zero", "const int m = (int)nearbyint((2.0 * fr - 1.0) * 8.0);",
+     "const int m = (int)round((2.0 * fr - 1.0) * 8.0);"),
+    ("e4m3 saturation threshold at 480", "if (a >= 448.0)\n        return sign | 0x7E;",
+     "if (a >= 480.0)\n        return sign | 0x7E;"),
+    ("e4m3 subnormal range one binade short", "if (a < ldexp(1.0, -6)) {", "if (a < ldexp(1.0, -7)) {"),
     ("e4m3 zero loses its sign", "const uint8_t sign = signbit(x) ? 0x80 : 0x00;",
      "const uint8_t sign = x < 0 ? 0x80 : 0x00;"),
     ("fp8 write ignores the K scale", "quotient_f32((float)bf16_bits_to_double(key[src + e]), k_scale)",
