@@ -53,6 +53,12 @@ MUTANTS = [
     ("e4m3 saturation threshold at 480", "if (a >= 448.0)\n        return sign | 0x7E;",
      "if (a >= 480.0)\n        return sign | 0x7E;"),
     ("e4m3 subnormal range one binade short", "if (a < ldexp(1.0, -6)) {", "if (a < ldexp(1.0, -7)) {"),
+    ("slot 0 taken for padding", "if (slot < 0)\n            continue; /* padding token */",
+     "if (slot <= 0)\n            continue; /* padding token */"),
+    ("query row ignores its index", "const int64_t t = (int64_t)p->query_start_loc[r] + i;",
+     "const int64_t t = (int64_t)p->query_start_loc[r];"),
+    ("query head taken as the kv head", "(size_t)p->num_q_heads + (size_t)h) * (size_t)d;",
+     "(size_t)p->num_q_heads + (size_t)g) * (size_t)d;"),
     ("e4m3 zero loses its sign", "const uint8_t sign = signbit(x) ? 0x80 : 0x00;",
      "const uint8_t sign = x < 0 ? 0x80 : 0x00;"),
     ("fp8 write ignores the K scale", "quotient_f32((float)bf16_bits_to_double(key[src + e]), k_scale)",
