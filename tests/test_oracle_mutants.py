@@ -57,6 +57,10 @@ MUTANTS = [
      "if (slot <= 0)\n            continue; /* padding token */"),
     ("query row ignores its index", "const int64_t t = (int64_t)p->query_start_loc[r] + i;",
      "const int64_t t = (int64_t)p->query_start_loc[r];"),
+    ("block copy reversed", "memcpy(cache + (size_t)dst * block_elems, cache + (size_t)src * block_elems,",
+     "memcpy(cache + (size_t)src * block_elems, cache + (size_t)dst * block_elems,"),
+    ("block copy of half a block", "               block_elems * sizeof(uint16_t));",
+     "               block_elems / 2 * sizeof(uint16_t));"),
     ("query head taken as the kv head", "(size_t)p->num_q_heads + (size_t)h) * (size_t)d;",
      "(size_t)p->num_q_heads + (size_t)g) * (size_t)d;"),
     ("e4m3 zero loses its sign", "const uint8_t sign = signbit(x) ? 0x80 : 0x00;",
