@@ -37,15 +37,26 @@ import workloads as wl  # noqa: E402
 
 METRIC = "decode paged-attn achieved HBM GB/s (% of peak), tokens/s per layer-step"
 FALLBACK_HBM_GBS = 6800.0
+SETTLE_S = 1.5          # seconds of untimed steps under the clock sampler before the timed passes
 
-# DRAM bytes (read + write) per algorithmic byte of the attention launch, from
-# the ncu capture summarised in profiles/decode_kernel_llama13b-decode-64req.md
-# (64-request case of the 13B batch: 1.0477 GB of traffic for 1.0339 GB of
-# algorithmic bytes).  Traffic grows with the KV bytes read, so the full
-# launch's traffic is this ratio times its algorithmic bytes.  It holds only
-# for the decode kernel sources it was measured on (hash below); otherwise null.
-DECODE_TRAFFIC = {"sources_sha256_16": "9fccdd05fa44c3f6", "ratio": (1.042259 + 0.004871) / 1.033885,
-                  "profile": "profiles/decode_kernel_llama13b-decode-64req.md"}
+# DRAM bytes (read + write) per algorithmic byte of the attention call, from
+# ncu captures (dram__bytes_read.sum + dram__bytes_write.sum of the kernels
+# of one call, over the call's algorithmic bytes) of smaller cases of the same
+# kernels.  Traffic grows with the KV bytes read, so a full launch's traffic is
+# the ratio times its algorithmic bytes.  A ratio holds only for the kernel
+# sources it was measured on (hash of the files below); otherwise null.
+TRAFFIC_SOURCES = ("decode.cu", "pkv_common.cuh", "paged_attn.cu", "prefill_tc.cu", "tc_common.cuh",
+                   "attn_internal.cuh")
+TRAFFIC = {
+    # "<cache> <kernels of the call>": decode (plan + decode), cascade (plus the
+    # shared-prefix pass), prefill (plus the tcgen05 chunk kernel)
+    "bf16 decode": {"sources_sha256_16": "", "ratio": None, "source": ""},
+    "e4m3 decode": {"sources_sha256_16": "", "ratio": None, "source": ""},
+    "bf16 cascade": {"sources_sha256_16": "", "ratio": None, "source": ""},
+    "e4m3 cascade": {"sources_sha256_16": "", "ratio": None, "source": ""},
+    "bf16 prefill": {"sources_sha256_16": "", "ratio": None, "source": ""},
+    "e4m3 prefill": {"sources_sha256_16": "", "ratio": None, "source": ""},
+}
 
 
 def percentiles(values, fractions=(0.1, 0.5, 0.9)):
@@ -54,10 +65,10 @@ def percentiles(values, fractions=(0.1, 0.5, 0.9)):
     return [q[min(len(q) - 1, max(0, math.ceil(f * len(q)) - 1))] for f in fractions]
 
 
-def decode_sources_hash() -> str:
+def attention_sources_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("decode.cu", "pkv_common.cuh"):
+    for f in TRAFFIC_SOURCES:
         with open(os.path.join(ROOT, "paged_kv_cache_111_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -163,7 +174,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
@@ -370,9 +381,23 @@ def run_gpu(args, rank: int, world: int) -> dict:
             phases = tuple(sum(e[k].elapsed_time(e[k + 1]) for e in ev) / n_steps for k in range(3))
         return mean, phases, per
 
+    # The clock sampler runs from an untimed settle loop of the same step (at
+    # least SETTLE_S seconds, so the record holds many samples taken under
+    # this load) through the headline, phase and end-to-end passes.
+    clk = ClockSampler(dev.index)
+    clk.__enter__()
+    t_settle = time.perf_counter() + SETTLE_S
+    n_settle = 0
+    while time.perf_counter() < t_settle:
+        for _ in range(16):
+            if graph is not None:
+                graph.replay()
+            else:
+                one_step()
+        n_settle += 16
+        torch.cuda.synchronize(dev)
     # the headline: steps back to back (no event between the kernels of a step)
-    with ClockSampler(dev.index) as clk:
-        step_ms, _, _ = run_steps(args.steps, False)
+    step_ms, _, _ = run_steps(args.steps, False)
     total_ms = step_ms * args.steps
     # the phase breakdown (kv_write, paged_attn, combine), events between the calls
     if graph is None:
@@ -445,8 +470,14 @@ def run_gpu(args, rank: int, world: int) -> dict:
             torch.cuda.synchronize(dev)
             e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
+    clk.__exit__(None, None, None)
+    clocks = clk.summary()
+    clocks["window"] = (f"untimed settle loop of {n_settle} steps (>= {SETTLE_S:g} s), then the headline, phase "
+                        f"and end-to-end passes")
+
     # ---- same-run copy probe (device-to-device copy, read + write bytes) ------
-    probe_gbs = None
+    # and a read-only probe (a sum over a 4 GiB buffer: read bytes only)
+    probe_gbs = read_gbs = None
     if args.copy_probe:
         n = 1 << 30
         a = torch.empty(n, dtype=torch.bfloat16, device=dev)
@@ -462,12 +493,25 @@ def run_gpu(args, rank: int, world: int) -> dict:
             best = min(best, s0.elapsed_time(s1))
         probe_gbs = 2 * n * 2 / (best * 1e-3) / 1e9
         del a, b
+        x = torch.ones(1 << 30, dtype=torch.float32, device=dev)
+        acc = torch.empty((), dtype=torch.float32, device=dev)
+        best = math.inf
+        for _ in range(10):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            torch.sum(x, dim=0, out=acc)
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            best = min(best, s0.elapsed_time(s1))
+        read_gbs = x.numel() * 4 / (best * 1e-3) / 1e9
+        del x
 
     return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K),
             "fp8_scales": scales,
             "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
             "phase_step_ms": phase_per,
-            "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "probe_gbs": probe_gbs,
+            "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clocks, "probe_gbs": probe_gbs,
+            "read_probe_gbs": read_gbs,
             "l2_flush": flush, "l2_bytes": l2_bytes}
 
 
@@ -481,30 +525,44 @@ def oracle_sample(step: wl.Step, n_req: int, seed: int) -> wl.Step:
     return step.subset(sorted(idx.tolist()))
 
 
-def time_oracle_step(sub: wl.Step, fp8_scales=None, num_threads: int = 0):
-    """One oracle step on ``sub``: cache write of the new tokens + attention
-    (over an E4M3 cache when fp8_scales = (k_scale, v_scale) is given), on
-    num_threads host threads (0: all).  Returns (seconds, algorithmic bytes
-    of the sample, threads)."""
+def time_oracle_step(sub: wl.Step, fp8_scales=None, num_threads: int = 0) -> dict:
+    """One oracle step on ``sub``: cache write of the new tokens, then
+    attention (over an E4M3 cache when fp8_scales = (k_scale, v_scale) is
+    given), on num_threads host threads (0: all), each phase timed on its own.
+    Returns {"s", "kv_write_s", "attention_s", "bytes", "threads"} (bytes: the
+    sample's algorithmic bytes of the whole step)."""
     import oracle
     if fp8_scales is None:
         cache = oracle.new_cache(sub.num_blocks, sub.num_kv_heads, sub.head_size)
         oracle.kv_write(cache, sub.hist_key, sub.hist_value, sub.hist_slot_mapping)
         t0 = time.perf_counter()
         oracle.kv_write(cache, sub.key, sub.value, sub.slot_mapping)
+        t1 = time.perf_counter()
         oracle.paged_attn(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
                           sub.num_q_heads, sub.scale, num_threads)
-        dt = time.perf_counter() - t0
-        return dt, algorithmic_bytes(sub)["step"], num_threads or oracle.max_threads()
-    ks, vs = fp8_scales
-    cache = oracle.new_cache_fp8(sub.num_blocks, sub.num_kv_heads, sub.head_size)
-    oracle.kv_write_fp8(cache, sub.hist_key, sub.hist_value, sub.hist_slot_mapping, ks, vs)
-    t0 = time.perf_counter()
-    oracle.kv_write_fp8(cache, sub.key, sub.value, sub.slot_mapping, ks, vs)
-    oracle.paged_attn_fp8(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
-                          sub.num_q_heads, sub.scale, ks, vs, num_threads)
-    dt = time.perf_counter() - t0
-    return dt, algorithmic_bytes(sub, 1)["step"], num_threads or oracle.max_threads()
+        t2 = time.perf_counter()
+        nbytes = algorithmic_bytes(sub)["step"]
+    else:
+        ks, vs = fp8_scales
+        cache = oracle.new_cache_fp8(sub.num_blocks, sub.num_kv_heads, sub.head_size)
+        oracle.kv_write_fp8(cache, sub.hist_key, sub.hist_value, sub.hist_slot_mapping, ks, vs)
+        t0 = time.perf_counter()
+        oracle.kv_write_fp8(cache, sub.key, sub.value, sub.slot_mapping, ks, vs)
+        t1 = time.perf_counter()
+        oracle.paged_attn_fp8(cache, sub.query, sub.block_tables, sub.seq_lens, sub.query_start_loc,
+                              sub.num_q_heads, sub.scale, ks, vs, num_threads)
+        t2 = time.perf_counter()
+        nbytes = algorithmic_bytes(sub, 1)["step"]
+    return {"s": t2 - t0, "kv_write_s": t1 - t0, "attention_s": t2 - t1, "bytes": nbytes,
+            "threads": num_threads or oracle.max_threads()}
+
+
+def phase_summary(runs) -> dict:
+    """Mean ms per sampled step of each phase over a list of time_oracle_step results."""
+    n = len(runs)
+    return {"kv_write": sum(r["kv_write_s"] for r in runs) / n * 1e3,
+            "attention": sum(r["attention_s"] for r in runs) / n * 1e3,
+            "total": sum(r["s"] for r in runs) / n * 1e3}
 
 
 def fp8_scales(step: wl.Step):
@@ -522,31 +580,32 @@ def cpu_baseline(step: wl.Step, budget_s: float = 10.0, scales=None) -> dict:
     oracle.build()
     n_req = max(1, step.num_seqs // 4)
     sub = oracle_sample(step, n_req, 7)
-    times, nbytes, threads = [], 0, 1
+    runs = []
     t_end = time.perf_counter() + budget_s
-    while len(times) < 3 or time.perf_counter() < t_end:
-        dt, nbytes, threads = time_oracle_step(sub, scales)
-        times.append(dt)
-        if len(times) >= 50:
+    while len(runs) < 3 or time.perf_counter() < t_end:
+        runs.append(time_oracle_step(sub, scales))
+        if len(runs) >= 50:
             break
-    mean = sum(times) / len(times)
+    ph = phase_summary(runs)
+    nbytes, threads = runs[0]["bytes"], runs[0]["threads"]
     # the same oracle on one host thread, on a smaller sample (a sixteenth of the requests)
     sub1 = oracle_sample(step, max(1, step.num_seqs // 16), 8)
-    t1, n1 = [], 0
+    runs1 = []
     t_end = time.perf_counter() + budget_s / 2
-    while len(t1) < 2 or time.perf_counter() < t_end:
-        dt, n1, _ = time_oracle_step(sub1, scales, num_threads=1)
-        t1.append(dt)
-        if len(t1) >= 20:
+    while len(runs1) < 2 or time.perf_counter() < t_end:
+        runs1.append(time_oracle_step(sub1, scales, num_threads=1))
+        if len(runs1) >= 20:
             break
-    mean1 = sum(t1) / len(t1)
-    return {"value": nbytes / mean / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+    ph1 = phase_summary(runs1)
+    return {"value": nbytes / (ph["total"] * 1e-3) / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{sub.num_seqs} of {step.num_seqs} requests ({sub.num_tokens} query tokens), "
-                      f"{len(times)} timed oracle steps (cache write + attention), mean {mean * 1e3:.1f} ms",
-            "tokens_per_s": sub.num_tokens / mean,
-            "single_thread": {"value": n1 / mean1 / 1e9, "unit": "GB/s", "cores": 1,
-                              "sample": f"{sub1.num_seqs} of {step.num_seqs} requests, {len(t1)} timed oracle steps, "
-                                        f"mean {mean1 * 1e3:.1f} ms"}}
+                      f"{len(runs)} timed oracle steps (cache write, then attention), mean {ph['total']:.1f} ms",
+            "ms_per_sampled_step": ph,
+            "tokens_per_s": sub.num_tokens / (ph["total"] * 1e-3),
+            "single_thread": {"value": runs1[0]["bytes"] / (ph1["total"] * 1e-3) / 1e9, "unit": "GB/s", "cores": 1,
+                              "ms_per_sampled_step": ph1,
+                              "sample": f"{sub1.num_seqs} of {step.num_seqs} requests, {len(runs1)} timed oracle "
+                                        f"steps, mean {ph1['total']:.1f} ms"}}
 
 
 def run_reference(args, rank: int, world: int) -> None:
@@ -557,20 +616,23 @@ def run_reference(args, rank: int, world: int) -> None:
     step = wl.make_workload(args.workload)
     # size one step's sample so that warmup + steps finish in about two minutes
     probe = oracle_sample(step, 4, 11)
-    dt, _, _ = time_oracle_step(probe)
+    dt = time_oracle_step(probe)["s"]
     per_req = max(dt / probe.num_seqs, 1e-4)
     budget_step = 120.0 / max(1, args.steps + args.warmup)
     n_req = int(max(1, min(step.num_seqs, budget_step / per_req)))
     samples = [oracle_sample(step, n_req, 100 + i) for i in range(min(4, args.steps + args.warmup))]
     for i in range(args.warmup):
         time_oracle_step(samples[i % len(samples)])
-    tot_t, tot_b, tot_tok, threads = 0.0, 0, 0, 1
+    runs = []
+    tot_tok = 0
     for i in range(args.steps):
         s = samples[i % len(samples)]
-        dt, nb, threads = time_oracle_step(s)
-        tot_t += dt
-        tot_b += nb
+        runs.append(time_oracle_step(s))
         tot_tok += s.num_tokens
+    tot_t = sum(r["s"] for r in runs)
+    tot_b = sum(r["bytes"] for r in runs)
+    threads = runs[0]["threads"]
+    ph = phase_summary(runs)
     value = tot_b / tot_t / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
@@ -579,6 +641,8 @@ def run_reference(args, rank: int, world: int) -> None:
         "config": {"workload": args.workload, "sample_requests_per_step": n_req},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{n_req} of {step.num_seqs} requests per step, {args.steps} steps"},
+        "us_per_step": {"kv_write": ph["kv_write"] * 1e3, "paged_attn": ph["attention"] * 1e3,
+                        "total": ph["total"] * 1e3},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "tokens_per_s": tot_tok / tot_t,
     }
@@ -587,7 +651,28 @@ def run_reference(args, rank: int, world: int) -> None:
 
 # ---------------------------------------------------------------------------
 
-def roofline(ab: dict, attn_ms: float, pk: dict) -> dict:
+def traffic_key(step: wl.Step, fp8: bool, prefix_blocks: int) -> str:
+    """Which kernels the attention call runs (the key of TRAFFIC)."""
+    kind = "decode"
+    if prefix_blocks:
+        kind = "cascade"
+    elif launches_per_step(step, 0) > 4:
+        kind = "prefill"
+    return ("e4m3 " if fp8 else "bf16 ") + kind
+
+
+def traffic_of(key: str, ab: dict):
+    """(DRAM bytes per call, where the ratio comes from) for the call's kernels,
+    or (None, why) when no capture of the current sources covers them."""
+    t = TRAFFIC.get(key)
+    if not t or t["ratio"] is None:
+        return None, f"no ncu capture of the {key} call"
+    if attention_sources_hash() != t["sources_sha256_16"]:
+        return None, f"kernel sources changed since the {key} capture"
+    return t["ratio"] * ab["attention"], t["source"] + " (ratio scaled by this call's algorithmic bytes)"
+
+
+def roofline(ab: dict, attn_ms: float, pk: dict, traffic_key: str) -> dict:
     """Roofline of the paged_attn call: HBM-bound (decode) unless its
     algorithmic flops at the tensor peak take longer than its bytes at the
     HBM peak (a prefill chunk), then tensor-bound."""
@@ -598,14 +683,14 @@ def roofline(ab: dict, attn_ms: float, pk: dict) -> dict:
         ach = ab["flops"] / t / 1e12
         return {"bound": "tensor", "kernel": "paged_attn (plan + decode + tcgen05 prefill kernels)",
                 "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"],
-                "peak_source": pk["source"], "algorithmic_flops_per_launch": ab["flops"], "traffic": None}
+                "peak_source": pk["source"], "algorithmic_flops_per_launch": ab["flops"],
+                "traffic": traffic_of(traffic_key, ab)[0], "traffic_source": traffic_of(traffic_key, ab)[1]}
     ach = ab["attention"] / t / 1e9
+    traffic, why = traffic_of(traffic_key, ab)
     return {"bound": "hbm", "kernel": "paged_attn (plan + decode kernels)",
             "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
             "peak_source": pk["source"], "algorithmic_bytes_per_launch": ab["attention"],
-            "traffic": (DECODE_TRAFFIC["ratio"] * ab["attention"]
-                        if decode_sources_hash() == DECODE_TRAFFIC["sources_sha256_16"] else None),
-            "traffic_source": DECODE_TRAFFIC["profile"] + " (scaled by algorithmic bytes)"}
+            "traffic": traffic, "traffic_source": why}
 
 
 def main():
@@ -690,18 +775,18 @@ def main():
         # the phase pass times each step on its own: its spread (events between the calls included)
         "phase_pass_step_us_p10_p50_p90": ([round(v * 1e3, 2) for v in percentiles(r["phase_step_ms"])]
                                            if r["phase_step_ms"] else None),
-        "roofline": roofline(ab, r["attn_ms"], pk),
+        "roofline": roofline(ab, r["attn_ms"], pk, traffic_key(step, fp8, r["shared_prefix_blocks"])),
         "copy_probe_gbs": r["probe_gbs"],
+        "read_probe_gbs": r["read_probe_gbs"],
+        # the call against the same run's probes: decode reads far more than it writes
+        "attn_frac_of_probe": ({"copy": attn_gbs / r["probe_gbs"], "read_only": attn_gbs / r["read_probe_gbs"]}
+                               if r["probe_gbs"] and r["read_probe_gbs"] else None),
         "e2e": ({"value": job_throughput(ab["step"], world, e2e_max), "unit": "GB/s",
                  "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": e2e_max}
                 if e2e_max == e2e_max else None),
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
     }
-    if fp8 or r["launches_per_step"] != 4:
-        # the profiled traffic ratio is the bf16 decode kernel's alone (no
-        # shared-prefix pass, no prefill kernel in the call)
-        line["roofline"]["traffic"] = None
     if r["shared_prefix_blocks"]:
         line["roofline"]["kernel"] = line["roofline"]["kernel"].replace(
             "paged_attn (plan + decode", "paged_attn_shared_prefix (plan + decode + tcgen05 shared-prefix")
@@ -711,6 +796,7 @@ def main():
     if args.graph:
         line["roofline"]["kernel"] = "whole layer-step (kv_write + paged_attn + combine), CUDA-graph replay"
         line["roofline"]["traffic"] = None
+        line["roofline"]["traffic_source"] = "graph replay: no per-call capture"
     if ab["kv_logical"] != ab["kv_unique"]:
         line["logical_kv_gbs_incl_l2_reuse"] = ab["kv_logical"] / (r["attn_ms"] * 1e-3) / 1e9
     if not args.no_cpu_baseline and world == 1:      # the oracle's baseline: rank 0 of a 1-GPU run only

@@ -340,16 +340,22 @@ int pkv_copy_blocks(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
  *    exceeds PKV_NOALLOC_SCRATCH_BYTES are refused with PKV_ERR_WORKSPACE
  *    before anything is enqueued; argument errors return the same codes as
  *    pkv_paged_attn.
- *  - The first call on each device looks up the array's device address
- *    (and, under lazy module loading, loads this code onto the device); make
- *    that first call before any stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (a host-side query that enqueues nothing).  Under lazy module loading
+ *    the first call on each device also loads this code onto the device;
+ *    make that first call before any stream capture.
  *  - Every call on a device shares the one array and leaves its contents
  *    behind; each call rewrites all of the scratch it later reads, so nothing
  *    needs clearing between calls.  Calls that overlap on the GPU (other
  *    streams, other threads' streams) race on the array: keep them ordered,
  *    e.g. on one stream.
- *  - device_status: optional int32 device word; after the call's kernels it
- *    receives the device status (PKV_OK or a PKV_ERR_DEVICE_* code).
+ *  - device_status: optional int32 device word.  After the call's kernels,
+ *    an error the GPU found (a PKV_ERR_DEVICE_* code, or PKV_ERR_PROTOCOL)
+ *    is stored there unless the word already holds an error: as for the
+ *    other calls' status words, the first error stays and the library never
+ *    clears the word, so the caller zeroes it beforehand.  A call that finds
+ *    no error, or that has no requests (num_seqs == 0, nothing enqueued),
+ *    leaves the word as it was.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (256u << 20)
 

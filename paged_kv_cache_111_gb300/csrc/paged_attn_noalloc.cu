@@ -14,31 +14,24 @@
 // the process exits.  With CUDA's default lazy module loading that happens
 // the first time this entry point runs on a device; with eager loading it
 // happens when the library is loaded.  Host code cannot use the array's name
-// as a device address: the entry point looks the address up once per device
-// with cudaGetSymbolAddress and passes it to the kernels.
-#include <mutex>
-
+// as a device address: every call looks the address up with
+// cudaGetSymbolAddress, with the call's device current, and passes it to the
+// kernels.  The lookup is a host-side query that enqueues nothing; doing it
+// on every call (instead of caching it) keeps the address right after the
+// device's context has been torn down and the module loaded again.
 #include "pkv_common.cuh"
 
 namespace pkv {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-
-// Device address of the scratch array on the current device (looked up once
-// per device, with that device current); nullptr on failure.
-static void *noalloc_scratch_address(int dev) {
-    static std::mutex mu;
-    static void *addr[kMaxDevices] = {};
-    if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+// The call's device status (the scratch's first word) into the caller's
+// word, by the rule of every other status word of this library: the first
+// error stored there stays, and the word is never cleared.
+__global__ void forward_status_kernel(const int32_t *scratch_status, int32_t *device_status) {
+    pdl_wait();       // the combine (and everything before it) has completed
+    const int32_t s = *reinterpret_cast<const volatile int32_t *>(scratch_status);
+    if (s != PKV_OK) atomicCAS(device_status, 0, s);
 }
 
 }  // namespace pkv
@@ -62,10 +55,10 @@ extern "C" int pkv_paged_attn_noalloc(void *out, const void *query, int64_t quer
     if (rc != PKV_ERR_WORKSPACE) return rc;       // an argument error
     if (need > static_cast<size_t>(PKV_NOALLOC_SCRATCH_BYTES)) return PKV_ERR_WORKSPACE;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-    void *scratch = noalloc_scratch_address(dev);
-    if (!scratch) return PKV_ERR_CUDA;
+    // the array's address on the current device (the host-side name is only
+    // a stand-in, never a device address)
+    void *scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch) return PKV_ERR_CUDA;
 
     rc = pkv_paged_attn(out, query, query_token_stride, kv_cache, num_blocks, block_tables, max_blocks_per_seq,
                         seq_lens, query_start_loc, num_seqs, num_tokens, max_query_len, max_seq_len, num_q_heads,
@@ -76,8 +69,8 @@ extern "C" int pkv_paged_attn_noalloc(void *out, const void *query, int64_t quer
                                 stream);
     if (rc) return rc;
     if (device_status &&
-        cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        launch_pdl(forward_status_kernel, dim3(1), dim3(1), 0, static_cast<cudaStream_t>(stream),
+                   static_cast<const int32_t *>(scratch), device_status) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }

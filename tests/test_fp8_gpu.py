@@ -110,17 +110,18 @@ def test_attention_fp8_mixed_step_with_a_long_chunk():
     check_close(out, ref, "mixed fp8")
 
 
-def test_attention_fp8_llama13b_sampled_rows():
+def test_attention_fp8_llama13b_every_row():
+    """The 13B batch over an E4M3 cache, every output row against the
+    oracle's attention over the same codes (pool compacted to the used
+    blocks on the host)."""
     step = wl.make_workload("llama13b-decode")
     k_scale, v_scale = 0.02, 0.02
     _, out = run_fp8(step, k_scale, v_scale)
-    rng = np.random.default_rng(5)
-    reqs = sorted(set(rng.choice(step.num_seqs, size=24, replace=False).tolist())
-                  | {int(torch.argmax(step.seq_lens)), int(torch.argmin(step.seq_lens))})
-    sub = step.subset(reqs)
+    out = out.cpu()
+    sub = step.subset(range(step.num_seqs))
+    assert torch.equal(sub.query, step.query)
     _, ref, _ = oracle.run_step_fp8(sub, k_scale, v_scale)
-    rows = torch.cat([torch.arange(int(step.query_start_loc[r]), int(step.query_start_loc[r + 1])) for r in reqs])
-    check_close(out[rows.cuda()], ref, "llama13b fp8 sampled")
+    check_close(out, ref, "llama13b fp8 every row")
 
 
 EDGE = [

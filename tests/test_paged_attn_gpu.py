@@ -36,20 +36,20 @@ def test_named_workloads_full_size(name):
     compare(wl.make_workload(name))
 
 
-def test_llama13b_full_size_sampled_rows():
-    """The 13B batch runs whole on the GPU; the oracle checks a sample of requests."""
+def test_llama13b_full_size_every_row():
+    """The 13B batch (256 requests, 100000-block cache) runs whole on the GPU,
+    and every one of its output rows is checked against the oracle.  The
+    oracle runs on the same batch with its pool compacted to the blocks the
+    tables use (about 4 GB on the host); each request sees the same keys,
+    values and queries, so the rows compare one to one."""
     step = wl.make_workload("llama13b-decode")
     _, out, status = run_step(step)
     assert status == 0
-    rng = np.random.default_rng(3)
-    S = step.num_seqs
-    reqs = sorted(set(rng.choice(S, size=32, replace=False).tolist())
-                  | {int(torch.argmax(step.seq_lens)), int(torch.argmin(step.seq_lens))})
-    sub = step.subset(reqs)
+    out = out.cpu()
+    sub = step.subset(range(step.num_seqs))
+    assert torch.equal(sub.query, step.query)
     _, ref, _ = oracle.run_step(sub)
-    rows = torch.cat([torch.arange(int(step.query_start_loc[r]), int(step.query_start_loc[r + 1]))
-                      for r in reqs])
-    check_close(out[rows.cuda()], ref, "llama13b sampled")
+    check_close(out, ref, "llama13b every row")
 
 
 EDGE = [

@@ -6,8 +6,10 @@ hands it only inputs and outputs): instead of a caller
 workspace it uses a fixed scratch array inside the library.  These tests
 call it through the C ABI and compare it with the workspace path
 (pkv_paged_attn + pkv_paged_attn_combine) on the same inputs, on two calls
-in a row, within the attention tolerance of the other GPU tests.  The file
-is named to be collected last.
+in a row, within the attention tolerance of the other GPU tests, and with
+the fp64 oracle directly; they also check that an error the GPU finds
+reaches the caller's status word and that a clean call after it is clean.
+The file is named to be collected last.
 """
 
 import ctypes
@@ -15,10 +17,11 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_111_gb300 as pkv
 import workloads as wl
 from paged_kv_cache_111_gb300 import _build
-from tolerance import ATOL, RTOL
+from tolerance import ATOL, RTOL, check_close
 
 pytestmark = pytest.mark.gpu
 
@@ -46,10 +49,11 @@ def _setup(step):
     return dev, pool
 
 
-def _call_noalloc(lib, step, dev, pool, out, status, num_splits=0):
+def _call_noalloc(lib, step, dev, pool, out, status, num_splits=0, block_tables=None):
+    bt = dev["block_tables"] if block_tables is None else block_tables
     return lib.pkv_paged_attn_noalloc(
         out.data_ptr(), dev["query"].data_ptr(), dev["query"].stride(0), pool.data_ptr(), step.num_blocks,
-        dev["block_tables"].data_ptr(), step.max_blocks_per_seq, dev["seq_lens"].data_ptr(),
+        bt.data_ptr(), step.max_blocks_per_seq, dev["seq_lens"].data_ptr(),
         dev["query_start_loc"].data_ptr(), step.num_seqs, step.num_tokens, step.max_query_len, step.max_seq_len,
         step.num_q_heads, step.num_kv_heads, step.head_size, step.block_size, ctypes.c_float(step.scale),
         num_splits, status.data_ptr(), torch.cuda.current_stream().cuda_stream)
@@ -82,10 +86,9 @@ def test_noalloc_matches_workspace_path_on_two_calls_in_a_row(num_splits):
                                      wl.RequestSpec(1500, 1)], 16, 2, 128, 256, 77)
     dev, pool = _setup(step)
     ref = _workspace_path(step, dev, pool, num_splits)
-    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(2):
         out = torch.full_like(ref, float("nan"))
-        status.fill_(-1)
         assert _call_noalloc(lib, step, dev, pool, out, status, num_splits) == 0
         torch.cuda.synchronize()
         assert int(status.item()) == 0
@@ -116,3 +119,54 @@ def test_noalloc_refuses_sizes_beyond_its_scratch():
     rc = lib.pkv_paged_attn_noalloc(fake, fake, 32 * 128, fake, 1 << 20, fake, 256, fake, fake, 1 << 20, 1 << 20,
                                     1, 4096, 32, 32, 128, 16, ctypes.c_float(0.1), 0, None, None)
     assert rc == 5                                # PKV_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("kind", ["decode only", "mixed with a chunk"])
+def test_noalloc_matches_the_oracle(kind):
+    lib = _lib()
+    if kind == "decode only":
+        step = wl.build_step("noalloc-decode", [wl.RequestSpec(c, 1) for c in (0, 15, 16, 300, 1100, 2047)],
+                             32, 4, 64, 512, 91)
+    else:
+        step = wl.build_step("noalloc-mixed", [wl.RequestSpec(700, 1), wl.RequestSpec(0, 200),
+                                               wl.RequestSpec(45, 3), wl.RequestSpec(1500, 1)], 32, 8, 128, 512, 92)
+    dev, pool = _setup(step)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((step.num_tokens, step.num_q_heads, step.head_size), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    assert _call_noalloc(lib, step, dev, pool, out, status) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _, ref, _ = oracle.run_step(step)
+    check_close(out, ref, f"noalloc {kind}")
+
+
+def test_noalloc_forwards_a_device_error_then_a_clean_call_is_clean():
+    lib = _lib()
+    step = wl.build_step("noalloc-err", [wl.RequestSpec(40, 1), wl.RequestSpec(10, 1)], 4, 2, 64, 64, 11)
+    dev, pool = _setup(step)
+    # a block id outside the pool: loaded as zeros by the bounded TMA, reported
+    bad = dev["block_tables"].clone()
+    bad[0, 1] = step.num_blocks + 1000
+    out = torch.zeros(step.num_tokens, 4, 64, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert _call_noalloc(lib, step, dev, pool, out, status, block_tables=bad) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 7                # PKV_ERR_DEVICE_INDEX
+    # the word keeps the first error: a clean call does not clear it
+    assert _call_noalloc(lib, step, dev, pool, out, status) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 7
+    # a clean call into a cleared word: the shared scratch carries no stale status
+    status.zero_()
+    out.fill_(float("nan"))
+    assert _call_noalloc(lib, step, dev, pool, out, status) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _, ref, _ = oracle.run_step(step)
+    check_close(out, ref, "noalloc after an error")
+    # an earlier error in the caller's word (say, from the cache write) is kept
+    status.fill_(8)
+    assert _call_noalloc(lib, step, dev, pool, out, status, block_tables=bad) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 8
