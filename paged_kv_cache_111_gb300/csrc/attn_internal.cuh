@@ -74,6 +74,69 @@ struct PrefillParams {
     uint8_t *ws;
 };
 
+// Log-sum-exp merge of one split row by one warp: the row's n partial
+// outputs (part_o rows base .. base + n - 1, each normalised over its own
+// keys) and their natural log-sum-exps (part_lse) give
+//     M = max_s lse_s,  w_s = e^{lse_s - M},  out = sum_s w_s o_s / sum_s w_s
+// (a part with lse = -inf weighs 0), written to dst as bf16.  The partials
+// are read through L2 (ld.global.cg).  The log-sum-exps and a batch of partial rows (16 at head size
+// 64, 8 at 128) are loaded together before any arithmetic: the merge is a
+// short chain of dependent loads, bound by their latency.  n <= 32.
+template <int HD>
+__device__ __forceinline__ void merge_split_row(const float *part_o, const float *part_lse, int64_t base, int n,
+                                                __nv_bfloat16 *dst, int lane) {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    constexpr int PER = HD / 32;              // dims per lane (2 or 4)
+    constexpr int U = HD == 64 ? 16 : 8;
+    auto load = [&](int64_t prow) -> float4 {
+        const float *src = part_o + prow * HD + lane * PER;
+        if constexpr (PER == 4) {
+            return __ldcg(reinterpret_cast<const float4 *>(src));
+        } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+            return make_float4(v.x, v.y, 0.f, 0.f);
+        }
+    };
+    const float lse = lane < n ? __ldcg(part_lse + base + lane) : NEG_INF;
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = u < n ? load(base + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mx = lse;
+#pragma unroll
+    for (int s = 16; s; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    const float w = (lse == NEG_INF) ? 0.f : __expf(lse - mx);
+    float wsum = w;
+#pragma unroll
+    for (int s = 16; s; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int s0 = 0;;) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float wt = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);   // 0 past the last split
+            acc[0] += wt * v[u].x;
+            acc[1] += wt * v[u].y;
+            if constexpr (PER == 4) {
+                acc[2] += wt * v[u].z;
+                acc[3] += wt * v[u].w;
+            }
+        }
+        s0 += U;
+        if (s0 >= n) break;
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = s0 + u < n ? load(base + s0 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __nv_bfloat16 *d = dst + lane * PER;
+    if constexpr (PER == 4) {
+        *reinterpret_cast<uint2 *>(d) =
+            make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+    } else {
+        *reinterpret_cast<uint32_t *>(d) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+}
+
 // Parameters of the decode kernel (decode.cu).
 struct AttnParams {
     __nv_bfloat16 *out;
@@ -103,13 +166,16 @@ int make_decode_map(CUtensorMap *map, const void *kv_cache, int64_t num_blocks, 
 int launch_decode_path(const CUtensorMap &map, const AttnParams &ap, int32_t head_size, bool kv8, int grid, int dev,
                        cudaStream_t st);
 
-// The shared-prefix (cascade) pass on the same kernel: rows of every request
-// that shares the first `prefix_blocks` blocks of its table with request 0
-// attend once to those blocks' keys, cut into `prefix_parts` ranges of KV
-// tiles; range i is split i of each row.
-int launch_prefix(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
-                  int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream,
-                  bool kv8 = false);
+// The one-tile tensor-core kernel over an E4M3 cache (prefill_tc.cu): the
+// shared-prefix (cascade) pass (rows of every request that shares the first
+// `prefix_blocks` blocks of its table with request 0 attend once to those
+// blocks' keys, cut into `prefix_parts` ranges of KV tiles; range i is split
+// i of each row) and the chunks.  `grid` CTAs; CTAs beyond the plan's items
+// return at once.
+int launch_prefix_e4m3(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
+                       int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream);
+int launch_prefill_e4m3(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
+                        int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream);
 
 // Is the tensor-core prefill kernel available for this head layout?
 inline bool prefill_supported(int num_q_heads, int num_kv_heads, int head_size) {
@@ -117,10 +183,11 @@ inline bool prefill_supported(int num_q_heads, int num_kv_heads, int head_size) 
     return (head_size == 64 || head_size == 128) && G >= 1 && G <= kPrefillRows && (kPrefillRows % G) == 0;
 }
 
-// Host launcher of the prefill kernel (prefill_tc.cu).  `grid` CTAs; CTAs
-// beyond the plan's tile count return at once.
-int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
-                   const void *kv_cache, int64_t num_blocks, int32_t head_size, int64_t grid, int dev,
-                   cudaStream_t stream, bool kv8 = false);
+// Host launcher of the split-key prefill kernel over a bf16 cache
+// (prefill_sk.cu): chunks (cascade = false) or the shared-prefix pass
+// (cascade = true).  `grid` CTAs; CTAs beyond the plan's items return at once.
+int launch_prefill_sk(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
+                      const void *kv_cache, int64_t num_blocks, int32_t head_size, bool cascade, int64_t grid, int dev,
+                      cudaStream_t stream);
 
 }  // namespace pkv

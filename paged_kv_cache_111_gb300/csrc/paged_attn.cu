@@ -39,6 +39,7 @@ namespace pkv {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kSizeBins = 256;      // counting-sort bins for chunk sizes (pages or KV tiles)
+constexpr unsigned long long kOneChunkPages = 24;   // pages per warp up to which a warp takes one chunk
 
 // ---- workspace layout ---------------------------------------------------------
 
@@ -393,10 +394,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if ((tid & 31) == 0 && mine) atomicAdd(&total_pages, mine);
     __syncthreads();
     if (tid == 0) {
-        // about 3 chunks per warp of the decode grid, 4..64 pages each
+        // Chunks of 4..64 pages.  Each chunk starts with a chain of dependent loads
+        // (its record, the request's lengths, the block table and Q), so a small
+        // batch (at most kOneChunkPages pages per warp of the decode grid) gets one
+        // chunk per warp; a larger one about three per warp, largest first, so
+        // that the warps finish together.
         const unsigned long long work = total_pages * (unsigned long long)p.num_kv_heads;
-        const unsigned long long target = 3ull * (unsigned long long)max(p.total_warps, 1);
-        const unsigned long long per = (work + target - 1) / target;
+        const unsigned long long warps = (unsigned long long)max(p.total_warps, 1);
+        const unsigned long long per1 = (work + warps - 1) / warps;
+        const unsigned long long per = per1 <= kOneChunkPages ? per1 : (work + 3 * warps - 1) / (3 * warps);
         pages_per_split = (int)min(64ull, max(4ull, per));
     }
     __syncthreads();
@@ -571,69 +577,14 @@ __global__ void __launch_bounds__(256) combine_kernel(__nv_bfloat16 *out, const 
     const float *part_lse = reinterpret_cast<const float *>(ws + off_lse);
     const float *part_o = reinterpret_cast<const float *>(ws + off_o);
     const int lane = threadIdx.x & 31;
-    const float NEG_INF = -__int_as_float(0x7f800000);
-    constexpr int PER = HD / 32;              // dims per lane (2 or 4)
-    // partial rows loaded per batch, all in flight at once: the merge is a
-    // short chain of dependent loads, so it is bound by their latency
-    constexpr int U = HD == 64 ? 16 : 8;
-    auto load = [&](int64_t prow) -> float4 {
-        const float *src = part_o + prow * HD + lane * PER;
-        if constexpr (PER == 4) {
-            return __ldg(reinterpret_cast<const float4 *>(src));
-        } else {
-            const float2 v = __ldg(reinterpret_cast<const float2 *>(src));
-            return make_float4(v.x, v.y, 0.f, 0.f);
-        }
-    };
     // one warp per row (split token, q head), grid-strided over the rows
     const int64_t n_rows = static_cast<int64_t>(n_split) * num_q_heads;
     for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); row < n_rows;
          row += static_cast<int64_t>(gridDim.x) * 8) {
         const int4 st = __ldg(stoks + row / num_q_heads);   // {token, partial row of q head 0, splits, 0}
         const int h = static_cast<int>(row % num_q_heads);
-        const int n = st.z;
-        const int64_t base = st.y + static_cast<int64_t>(h) * n;
-        // the log-sum-exps and the first batch of partial rows, issued together
-        const float lse = lane < n ? __ldg(part_lse + base + lane) : NEG_INF;
-        float4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = u < n ? load(base + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float mx = lse;
-#pragma unroll
-        for (int s = 16; s; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-        // an empty split (lse = -inf) weighs 0; its partial row holds zeros
-        const float w = (lse == NEG_INF) ? 0.f : __expf(lse - mx);
-        float wsum = w;
-#pragma unroll
-        for (int s = 16; s; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
-        float acc[PER];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-        for (int s0 = 0;;) {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const float wt = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);   // 0 past the last split
-                acc[0] += wt * v[u].x;
-                acc[1] += wt * v[u].y;
-                if constexpr (PER == 4) {
-                    acc[2] += wt * v[u].z;
-                    acc[3] += wt * v[u].w;
-                }
-            }
-            s0 += U;
-            if (s0 >= n) break;
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                v[u] = s0 + u < n ? load(base + s0 + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-        __nv_bfloat16 *dst = out + (static_cast<int64_t>(st.x) * num_q_heads + h) * HD + lane * PER;
-        if constexpr (PER == 4) {
-            *reinterpret_cast<uint2 *>(dst) =
-                make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
-        } else {
-            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        }
+        merge_split_row<HD>(part_o, part_lse, st.y + static_cast<int64_t>(h) * st.z, st.z,
+                            out + (static_cast<int64_t>(st.x) * num_q_heads + h) * HD, lane);
     }
 }
 
@@ -750,17 +701,22 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     fp.k_scale = k_scale;
     fp.v_scale = v_scale;
     fp.ws = ap.ws;
+    // persistent kernels: one CTA per SM at most, and no more than their items
+    const int64_t max_ctas = std::min(sms, kStatsCtas);
     if (prefix_blocks > 0) {
-        // persistent kernels: one CTA per SM at most
-        rc = launch_prefix(fp, query, query_token_stride, kv_cache, num_blocks, head_size,
-                           std::min<int64_t>(std::min(sms, kStatsCtas), (lay.max_crows + kPrefillRows - 1) / kPrefillRows * num_kv_heads *
-                                                      lay.prefix_parts),
-                           dev, st, kv8);
+        const int64_t items = (lay.max_crows + kPrefillRows - 1) / kPrefillRows * num_kv_heads * lay.prefix_parts;
+        rc = kv8 ? launch_prefix_e4m3(fp, query, query_token_stride, kv_cache, num_blocks, head_size,
+                                      std::min(max_ctas, items), dev, st)
+                 : launch_prefill_sk(fp, query, query_token_stride, num_tokens, kv_cache, num_blocks, head_size,
+                                     true, std::min(max_ctas, items), dev, st);
         if (rc) return rc;
     }
     if (!may_prefill) return PKV_OK;
-    return launch_prefill(fp, query, query_token_stride, num_tokens, kv_cache, num_blocks, head_size,
-                          std::min<int64_t>(std::min(sms, kStatsCtas), lay.max_ptiles * num_kv_heads), dev, st, kv8);
+    const int64_t items = lay.max_ptiles * num_kv_heads;
+    return kv8 ? launch_prefill_e4m3(fp, query, query_token_stride, kv_cache, num_blocks, head_size,
+                                     std::min(max_ctas, items), dev, st)
+               : launch_prefill_sk(fp, query, query_token_stride, num_tokens, kv_cache, num_blocks, head_size,
+                                   false, std::min(max_ctas, items), dev, st);
 }
 
 }  // namespace pkv

@@ -1,4 +1,6 @@
-// Prefill-chunk paged attention on the 5th-generation tensor cores (tcgen05).
+// Prefill-chunk paged attention over an E4M3 (8-bit) KV cache, on the
+// 5th-generation tensor cores (tcgen05).  (The 16-bit cache has its own
+// kernel, in prefill_sk.cu.)
 //
 // The same computation as the decode path ("continuous batching and
 // PagedAttention" tutorial, section 3.6: loop over the request's blocks
@@ -12,28 +14,25 @@
 // takes items largest first from a shared counter.  Rows are
 // (query token, q head of the GQA group) pairs, so one K/V tile in shared
 // memory serves every q head of the group.  Per 128-key KV tile:
-//   S = Q K^T      tcgen05.mma, A = Q from tensor memory, B = K from shared
-//                  memory (K-major, 128-byte swizzle), D in tensor memory
-//                  (two S buffers)
+//   widen          the tile's raw E4M3 pages (TMA, one box per page and
+//                  lane) are widened to f16 (exactly) by warps 2, 3, 12 and
+//                  13 into a 16-bit ring, 128-byte swizzled
+//   S = Q K^T      tcgen05.mma kind::f16, A = Q from tensor memory, B = K
+//                  from shared memory (K-major), D in tensor memory (two S
+//                  buffers)
 //   softmax        two threads per row, each with half of the tile's keys,
 //                  read S from tensor memory, mask, share their row maxima
 //                  through shared memory, keep a running max (rescaling
 //                  their half of O only when the max grows by more than 2^8)
-//                  and write P (bf16) over S
+//                  and write P (f16) over S
 //   O += P V       tcgen05.mma, A = P from tensor memory, B = V (MN-major)
 //                  from shared memory, D = O in tensor memory
-// Every product reads A from tensor memory: on this part a change between
-// shared-memory and tensor-memory A operands from one group of MMAs to the
-// next costs about a third of the tensor pipe's rate.
-// Warp roles: warp 0 loads (TMA: K and V pages through the block table into
-// a three-stage ring), warp 1 issues the MMAs, warp 2 owns the
-// tensor-memory allocation, warps 4-11 do softmax and the epilogue.
-//
-// Over an E4M3 cache (KV8) the pages land raw in a ring of their own, and
-// warps 2, 3, 12 and 13 widen them to f16 (exact) into the 16-bit ring; Q
-// rows are scaled by a power of two into f16, P is f16, and the products
-// are kind::f16 with f16 operands.  k_scale enters the score factor and
-// v_scale the epilogue.
+// Both operands of a kind::f16 product share their type, so Q rows are
+// scaled by a power of two into f16 and P is f16; k_scale enters the score
+// factor and v_scale the epilogue.
+// Warp roles: warp 0 loads, warp 1 issues the MMAs, warp 2 owns the
+// tensor-memory allocation, warps 2, 3, 12 and 13 widen, warps 4-11 do
+// softmax and the epilogue.
 //
 // When any row of the tile puts a large share of its weight on few keys of
 // a KV tile (rows with few visible keys, or a peaked softmax), that tile's P
@@ -44,31 +43,28 @@
 // wait is bounded.
 #include <mutex>
 
-#include "attn_internal.cuh"
-#include "tc_common.cuh"
+#include "prefill_common.cuh"
 
 namespace pkv {
 
-// KV8: an E4M3 cache.  Its pages land in a ring of raw 8-bit tiles and
-// warps 2 (K) and 3 (V) widen them to f16 into the 16-bit ring the MMAs
-// read; Q and P are f16 too (both operands of a kind::f16 product share
-// their type).
-template <int HD, bool KV8 = false>
+// Shared memory: the 16-bit K and V rings the MMAs read, the raw E4M3 ring
+// the pages land in, barriers, the softmax exchange and the work items.
+template <int HD>
 struct PrefillCfg {
     static constexpr int kHalves = HD / 64;
-    static constexpr int kStages = (KV8 && HD == 128) ? 2 : 3;   // 16-bit K and V ring depth
+    static constexpr int kStages = HD == 128 ? 2 : 3;          // 16-bit K and V ring depth
     static constexpr int kKVBytes = kHalves * kPrefillKeys * 128;   // one K (or V) tile
-    static constexpr int kRawStages = 2;                     // raw E4M3 ring depth (KV8)
+    static constexpr int kRawStages = 2;                     // raw E4M3 ring depth
     static constexpr int kRawBytes = kPrefillKeys * HD;      // one raw K (or V) tile
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kStages * kKVBytes;
     static constexpr int kOffRaw = kOffV + kStages * kKVBytes;
-    static constexpr int kOffBar = kOffRaw + (KV8 ? kRawStages * 2 * kRawBytes : 0);
+    static constexpr int kOffBar = kOffRaw + kRawStages * 2 * kRawBytes;
     static constexpr int kOffXchg = kOffBar + 512;            // softmax halves' maxima, sums, Q maxima (4 KiB)
     static constexpr int kOffItems = kOffXchg + 4096;         // ring of work items (256 bytes)
     static constexpr int kSmem = kOffItems + 256 + 1024;      // + alignment slack
     // tensor memory: two S buffers (each later holding that tile's P and its
-    // bf16 remainder), O, and Q as the A operand of S = Q K^T
+    // f16 remainder), O, and Q as the A operand of S = Q K^T
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColQ = 384;
 };
@@ -80,115 +76,13 @@ enum PrefillBar { kQFull = 0, kKFull0, kKFull1, kKFull2, kVFull0, kVFull1, kVFul
                   kItemFull0, kItemFull1, kItemFull2, kItemFull3,      // work-item ring
                   kItemEmpty0, kItemEmpty1, kItemEmpty2, kItemEmpty3,
                   kOFree,                              // O read out by the epilogue
-                  kRFull0, kRFull1, kREmpty0, kREmpty1,  // raw E4M3 tiles (KV8)
+                  kRFull0, kRFull1, kREmpty0, kREmpty1,  // raw E4M3 tiles
                   kNumBars };
 static_assert(kNumBars * 8 + 16 + 64 <= 512, "barriers, the TMEM address slot and the votes fit their 512 bytes");
 // P of tile j is announced on kPFull0 + (j & 1): with one barrier per parity a
 // barrier never runs two phases ahead of the MMA thread's wait on it (the
 // softmax warps can finish tile j + 1 before the MMA thread looks at tile j).
 
-// A row whose weights in a KV tile are concentrated (sum of squared weights
-// of the tile above this fraction of the squared running sum) needs P's bf16
-// remainder in P V: bf16 rounding of a few large weights would otherwise
-// exceed the output tolerance.
-constexpr float kLoConcentration = 0.01f;
-
-// ---- softmax arithmetic on fp32 pairs (Blackwell f32x2 instructions) ----------------
-
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-// Four E4M3 values (one 32-bit word, element 0 in the low byte) -> two f16x2
-// words (elements 0,1 and 2,3), exactly.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &h01, uint32_t &h23) {
-    asm("{\n\t.reg .b16 lo, hi;\n\t"
-        "mov.b32 {lo, hi}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-        : "=r"(h01), "=r"(h23)
-        : "r"(w));
-}
-
-// P of a pair of keys as the 16-bit type of the products (bf16, or f16 over
-// an E4M3 cache), and the remainder that the rounding left.
-template <bool F16> __device__ __forceinline__ uint32_t pack_p(float a, float b) {
-    if constexpr (F16) {
-        const __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<const uint32_t *>(&h);
-    } else {
-        return pack_bf16x2(a, b);
-    }
-}
-template <bool F16> __device__ __forceinline__ uint32_t pack_p_rest(float a, float b) {
-    if constexpr (F16) {
-        const float2 hb = __half22float2(__floats2half2_rn(a, b));
-        const __half2 r = __floats2half2_rn(a - hb.x, b - hb.y);
-        return *reinterpret_cast<const uint32_t *>(&r);
-    } else {
-        const float2 hb = __bfloat1622float2(__floats2bfloat162_rn(a, b));
-        return pack_bf16x2(a - hb.x, b - hb.y);
-    }
-}
-
-// Bounded wait shared by every role; on timeout records the error and
-// reports it so the role can stop.
-__device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
-    if (mbar_wait_bounded(bar, parity)) return true;
-    set_status(status, PKV_ERR_DEVICE_TIMEOUT);
-    return false;
-}
-
-// One work item: one 128-row tile for one kv head.  CASCADE = false: rows of
-// one long request (a prefill chunk), causal, written to `out`.
-// CASCADE = true: 128 rows taken from every request that shares the first
-// prefix_blocks blocks of its table with request 0, against one range of
-// those blocks' KV tiles (every key of the prefix is visible to every such
-// row); the result for range i is split i of each row (normalised partial
-// output and its log-sum-exp), merged with the row's other splits by the
-// combine.
-struct PfItem {
-    int32_t valid;        // 0: no further item for this CTA
-    int32_t r;            // request whose block table is read
-    int32_t n_kv;         // KV tiles of the item
-    int32_t L;            // keys of the request (cascade: of the prefix)
-    int32_t qs, ctx;      // first query token, keys before the chunk
-    int32_t rows_total;   // rows of the request (cascade: of the pass)
-    int32_t row0;         // first row of the tile
-    int32_t n_pages;      // pages of the key range's sequence
-    int32_t part, t0;     // cascade split and its first KV tile (0 otherwise)
-    int32_t g;            // kv head
-};
-constexpr int kItemSlots = 4;
-
-// A workspace field written by the plan, loaded through L2 (not L1): the
-// prefill kernel reads the plan before its programmatic-launch wait.
-__device__ __forceinline__ int32_t ws_ld(const int32_t *a) { return __ldcg(a); }
-__device__ __forceinline__ int64_t ws_ld(const int64_t *a) {
-    return static_cast<int64_t>(__ldcg(reinterpret_cast<const long long *>(a)));
-}
-__device__ __forceinline__ int4 ws_ld(const int4 *a) { return __ldcg(a); }
-static_assert(kItemSlots * sizeof(PfItem) <= 256, "item ring fits its 256 bytes");
 
 // Persistent: one CTA per SM.  The CTA's first item is its index; each later
 // one is claimed from a counter the plan zeroes, in the plan's order
@@ -196,11 +90,11 @@ static_assert(kItemSlots * sizeof(PfItem) <= 256, "item ring fits its 256 bytes"
 // them through a ring in shared memory; tiles and their barriers are counted
 // across items, so the loads, the first products and the Q of the next item
 // overlap the epilogue of the current one.
-template <int HD, bool CASCADE, bool KV8>
-__global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
+template <int HD, bool CASCADE>
+__global__ void __launch_bounds__(448, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __nv_bfloat16 *__restrict__ query,
                    const int64_t q_stride, const PrefillParams p) {
-    using Cfg = PrefillCfg<HD, KV8>;
+    using Cfg = PrefillCfg<HD>;
     constexpr int S = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,9 +129,9 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
             int count = 1;
             if (b == kPFull0 || b == kPFull1 || b == kQFull || b == kOFree) count = 8;
             else if (b >= kXchg0 && b <= kXchg3) count = 2;
-            else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = KV8 ? 13 : 9;   // + converters
+            else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = 13;   // MMA, softmax, converters
             else if (b == kREmpty0 || b == kREmpty1) count = 4;      // every converter warp
-            else if (KV8 && (b == kKFull0 || b == kKFull1 || b == kKFull2 || b == kVFull0 || b == kVFull1 ||
+            else if ((b == kKFull0 || b == kKFull1 || b == kKFull2 || b == kVFull0 || b == kVFull1 ||
                              b == kVFull2 || b == kVFix0 || b == kVFix1 || b == kVFix2))
                 count = 2;                                           // the two converters of K (of V)
             mbar_init(&bars[b], count);
@@ -310,7 +204,6 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
             if (!it.valid) break;
             ++taken;
 
-            const int end_tile = end_tile_of(it.L);
             const int32_t *bt = p.block_tables + static_cast<int64_t>(it.r) * p.max_blocks_per_seq;
             // block ids in windows of 32 pages (4 KV tiles), one lane per page; the
             // next window is loaded a window ahead.  Pages past the sequence are -1
@@ -327,76 +220,29 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
             int win_next = load_window(1);
             for (int j = 0; j < it.n_kv && ok; ++j) {
                 const int gt = gj + j;
-                const int st = gt % S;
                 if (j > 0 && (j * kPagesPerTile) % 32 == 0) {
                     win_cur = win_next;
                     win_next = load_window(j * kPagesPerTile / 32 + 1);
                 }
                 const int wofs = (j * kPagesPerTile) % 32;
-                int pb[kPagesPerTile];
-#pragma unroll
-                for (int pg = 0; pg < kPagesPerTile; ++pg) pb[pg] = __shfl_sync(0xffffffffu, win_cur, wofs + pg);
-                if constexpr (KV8) {
-                    // the raw K and V pages of tile gt, once the converters are done
-                    // with tile gt - 2 (zeroing past the sequence end is theirs)
-                    const int rs = gt % Cfg::kRawStages;
-                    if (gt >= Cfg::kRawStages)
-                        ok = __all_sync(0xffffffffu, pf_wait(&bars[kREmpty0 + rs],
-                                                             ((gt - Cfg::kRawStages) / Cfg::kRawStages) & 1, status));
-                    if (!ok) break;
-                    if (lane == 0) {
-                        uint8_t *raw = smem + Cfg::kOffRaw + rs * 2 * Cfg::kRawBytes;
-                        mbar_arrive_expect_tx(&bars[kRFull0 + rs], 2 * Cfg::kRawBytes);
-#pragma unroll
-                        for (int pg = 0; pg < kPagesPerTile; ++pg) {
-                            tma_load_5d(raw + pg * kBlock * HD, &kv_map, &bars[kRFull0 + rs], 0, 0, 0, it.g, pb[pg]);
-                            tma_load_5d(raw + Cfg::kRawBytes + pg * kBlock * HD, &kv_map, &bars[kRFull0 + rs], 0, 0,
-                                        1, it.g, pb[pg]);
-                        }
-                    }
-                    continue;
-                }
-                // K of tile gt once S of tile gt-S has read its stage
-                if (gt >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kKEmpty0 + st], ((gt - S) / S) & 1, status));
+                // the raw K and V pages of tile gt, once the converters are done
+                // with tile gt - 2 (zeroing past the sequence end is theirs)
+                const int rs = gt % Cfg::kRawStages;
+                if (gt >= Cfg::kRawStages)
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kREmpty0 + rs],
+                                                         ((gt - Cfg::kRawStages) / Cfg::kRawStages) & 1, status));
                 if (!ok) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars[kKFull0 + st], Cfg::kKVBytes);
-#pragma unroll
-                    for (int pg = 0; pg < kPagesPerTile; ++pg)
-                        for (int h = 0; h < Cfg::kHalves; ++h)
-                            tma_load_5d(smem + Cfg::kOffK + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
-                                        &kv_map, &bars[kKFull0 + st], h * 64, 0, 0, it.g, pb[pg]);
-                }
-                // V of tile gt once P V of tile gt-S has read its stage
-                if (gt >= S) ok = __all_sync(0xffffffffu, pf_wait(&bars[kVEmpty0 + st], ((gt - S) / S) & 1, status));
-                if (!ok) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars[kVFull0 + st], Cfg::kKVBytes);
-#pragma unroll
-                    for (int pg = 0; pg < kPagesPerTile; ++pg)
-                        for (int h = 0; h < Cfg::kHalves; ++h)
-                            tma_load_5d(smem + Cfg::kOffV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + pg * 2048,
-                                        &kv_map, &bars[kVFull0 + st], h * 64, 0, 1, it.g, pb[pg]);
-                }
-                if (j == end_tile) {
-                    // zero V rows past the sequence end in its last (partial) page;
-                    // one fix barrier per stage, so none runs two phases ahead
-                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kVFull0 + st], (gt / S) & 1, status));
-                    if (!ok) break;
-                    const int lp = (it.L - 1) / kBlock - j * kPagesPerTile;   // page within the tile
-                    const int first = it.L % kBlock;
-                    const int nrows = kBlock - first;
-                    for (int e = lane; e < Cfg::kHalves * nrows * 8; e += 32) {
-                        const int h = e / (nrows * 8);
-                        const int rem = e % (nrows * 8);
-                        const int row = lp * kBlock + first + rem / 8;
-                        const uint32_t a =
-                            sV + st * Cfg::kKVBytes + h * (kPrefillKeys * 128) + row * 128 + (rem % 8) * 16;
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[kVFix0 + st]);
+                // one box per lane (lanes 0-7 the K rows of page lane, 8-15 the V
+                // rows of page lane - 8): the copy engine takes small boxes faster
+                // from many issuing lanes than from one
+                uint8_t *raw = smem + Cfg::kOffRaw + rs * 2 * Cfg::kRawBytes;
+                if (lane == 0) mbar_arrive_expect_tx(&bars[kRFull0 + rs], 2 * Cfg::kRawBytes);
+                __syncwarp();
+                const int my_blk = __shfl_sync(0xffffffffu, win_cur, wofs + (lane % kPagesPerTile));
+                if (lane < 2 * kPagesPerTile) {
+                    const int kv = lane / kPagesPerTile, pg = lane % kPagesPerTile;
+                    tma_load_5d(raw + kv * Cfg::kRawBytes + pg * kBlock * HD, &kv_map, &bars[kRFull0 + rs], 0, 0, kv,
+                                it.g, my_blk);
                 }
             }
             gj += it.n_kv;
@@ -410,9 +256,8 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t kIdescS = KV8 ? idesc_f16_f32(kPrefillRows, kPrefillKeys, 0, 0)
-                                             : idesc_bf16_f32(kPrefillRows, kPrefillKeys, 0, 0);
-            constexpr uint32_t kIdescO = KV8 ? idesc_f16_f32(kPrefillRows, HD, 0, 1) : idesc_bf16_f32(kPrefillRows, HD, 0, 1);
+            constexpr uint32_t kIdescS = idesc_f16_f32(kPrefillRows, kPrefillKeys, 0, 0);
+            constexpr uint32_t kIdescO = idesc_f16_f32(kPrefillRows, HD, 0, 1);
             // S(gt) = Q K^T into S buffer gt & 1; A = Q in tensor memory
             auto issue_s = [&](int gt) {
                 const int st = gt % S;
@@ -422,7 +267,7 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
                     const uint64_t b = smem_desc_sw128(sK + st * Cfg::kKVBytes + (kk >> 2) * (kPrefillKeys * 128) +
                                                            (kk & 3) * 32,
                                                        16, 1024);
-                    umma_bf16_ts(d, tmem + Cfg::kColQ + kk * 8, b, kIdescS, kk > 0);
+                    umma_f16_ts(d, tmem + Cfg::kColQ + kk * 8, b, kIdescS, kk > 0);
                 }
                 umma_commit(&bars[kSFull0 + (gt & 1)]);
                 umma_commit(&bars[kKEmpty0 + st]);
@@ -435,7 +280,7 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
 #pragma unroll
                 for (int kk = 0; kk < kPrefillKeys / 16; ++kk) {
                     const uint64_t b = smem_desc_sw128(sV + st * Cfg::kKVBytes + kk * 2048, kPrefillKeys * 128, 1024);
-                    umma_bf16_ts(tmem + Cfg::kColO, pcol + kk * 8 + (kk >> 2) * 32, b, kIdescO,
+                    umma_f16_ts(tmem + Cfg::kColO, pcol + kk * 8 + (kk >> 2) * 32, b, kIdescO,
                                  (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
@@ -499,7 +344,7 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
             }
         }
         __syncwarp();
-    } else if (KV8 && (warp == 2 || warp == 3 || warp >= 12)) {
+    } else if (warp == 2 || warp == 3 || warp >= 12) {
         // ---------------- converters (E4M3 cache): raw tiles -> f16 tiles ----------------
         // warps 2 and 12 widen K, 3 and 13 widen V (and zero V rows past the
         // sequence end: their scores are masked, but NaN times a zero weight
@@ -655,27 +500,25 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
                 qv[4 * c + 2] = w.z;
                 qv[4 * c + 3] = w.w;
             }
-            if constexpr (KV8) {
-                // the row scaled by 2^e into [2^14, 2^15) before rounding to f16 (exact
-                // but for parts below 2^-24 of its largest); the two halves agree on e
-                float a = 0.f;
+            // the row scaled by 2^e into [2^14, 2^15) before rounding to f16 (exact
+            // but for parts below 2^-24 of its largest); the two halves agree on e
+            float a = 0.f;
 #pragma unroll
-                for (int e = 0; e < kHalfDims / 2; ++e)
-                    a = fmaxf(a, fmaxf(fabsf(__uint_as_float(qv[e] << 16)), fabsf(__uint_as_float(qv[e] & 0xFFFF0000u))));
-                xq[half * kPrefillRows + row] = a;
-                post();
-                if (!meet()) a = 0.f;                  // timed out: the status says so
-                a = fmaxf(a, xq[(half ^ 1) * kPrefillRows + row]);
-                const int ex = a > 0.f ? min(126, max(-114, 14 - ilogbf(a))) : 0;
-                const float u = __int_as_float((ex + 127) << 23);
+            for (int e = 0; e < kHalfDims / 2; ++e)
+                a = fmaxf(a, fmaxf(fabsf(__uint_as_float(qv[e] << 16)), fabsf(__uint_as_float(qv[e] & 0xFFFF0000u))));
+            xq[half * kPrefillRows + row] = a;
+            post();
+            if (!meet()) a = 0.f;                  // timed out: the status says so
+            a = fmaxf(a, xq[(half ^ 1) * kPrefillRows + row]);
+            const int ex = a > 0.f ? min(126, max(-114, 14 - ilogbf(a))) : 0;
+            const float u = __int_as_float((ex + 127) << 23);
 #pragma unroll
-                for (int e = 0; e < kHalfDims / 2; ++e) {
-                    const __half2 h = __floats2half2_rn(__uint_as_float(qv[e] << 16) * u,
-                                                        __uint_as_float(qv[e] & 0xFFFF0000u) * u);
-                    qv[e] = *reinterpret_cast<const uint32_t *>(&h);
-                }
-                sl2 = p.scale_log2 * p.k_scale * __int_as_float((127 - ex) << 23);
+            for (int e = 0; e < kHalfDims / 2; ++e) {
+                const __half2 h = __floats2half2_rn(__uint_as_float(qv[e] << 16) * u,
+                                                    __uint_as_float(qv[e] & 0xFFFF0000u) * u);
+                qv[e] = *reinterpret_cast<const uint32_t *>(&h);
             }
+            sl2 = p.scale_log2 * p.k_scale * __int_as_float((127 - ex) << 23);
             if constexpr (kHalfDims / 2 == 32) {
                 tmem_st32(trow + Cfg::kColQ + half * 32, qv);
             } else {
@@ -829,19 +672,19 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
                         tmem_st32(trow + Cfg::kColO + half * kHalfDims + c * 32, v);
                     }
                 }
-                // P (bf16 pairs) of this half's keys into the tile's S buffer; the
+                // P (f16 pairs) of this half's keys into the tile's S buffer; the
                 // remainder too when this warp asks for it, zeros otherwise
                 // (16 columns at a time: fewer registers live)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t w[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) w[e] = pack_p<KV8>(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]);
+                    for (int e = 0; e < 16; ++e) w[e] = pack_p<true>(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]);
                     tmem_st16(sbuf + half * 64 + 16 * c, w);
                     if (wneed) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            w[e] = pack_p_rest<KV8>(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]);
+                            w[e] = pack_p_rest<true>(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]);
                         }
                     } else {
 #pragma unroll
@@ -875,7 +718,7 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
             }
             if (ok) {
                 tc_fence_after();
-                const float inv = l > 0.f ? (KV8 ? p.v_scale / l : 1.f / l) : 0.f;   // E4M3: V is code * v_scale
+                const float inv = l > 0.f ? p.v_scale / l : 0.f;   // E4M3: V is code * v_scale
                 uint32_t v[kHalfDims / 32][32];
 #pragma unroll
                 for (int c = 0; c < kHalfDims / 32; ++c) tmem_ld32(trow + Cfg::kColO + half * kHalfDims + c * 32, v[c]);
@@ -931,11 +774,7 @@ __global__ void __launch_bounds__(KV8 ? 448 : 384, 1)
 
 // ---- host side --------------------------------------------------------------------
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
+EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -949,67 +788,53 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int HD, bool CASCADE, bool KV8>
+template <int HD, bool CASCADE>
 static int launch_prefill_hd(const PrefillParams &p, const CUtensorMap &kvm, const void *query, int64_t q_stride,
                              int64_t grid, int dev, cudaStream_t stream) {
-    using Cfg = PrefillCfg<HD, KV8>;
+    using Cfg = PrefillCfg<HD>;
     static std::mutex mu;
     static uint64_t done_mask = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
         const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
         if (!bit || !(done_mask & bit)) {
-            if (cudaFuncSetAttribute(prefill_kernel<HD, CASCADE, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(prefill_kernel<HD, CASCADE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Cfg::kSmem) != cudaSuccess)
                 return PKV_ERR_CUDA;
             done_mask |= bit;
         }
     }
-    if (launch_pdl(prefill_kernel<HD, CASCADE, KV8>, dim3(static_cast<unsigned>(grid)), dim3(KV8 ? 448 : 384), Cfg::kSmem, stream,
+    if (launch_pdl(prefill_kernel<HD, CASCADE>, dim3(static_cast<unsigned>(grid)), dim3(448), Cfg::kSmem, stream,
                    kvm, static_cast<const __nv_bfloat16 *>(query), q_stride, p) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }
 
-static int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
-                         int32_t head_size);
-static int make_page_map_e4m3(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
-                              int32_t head_size);
 
-int launch_prefix(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
-                  int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream, bool kv8) {
+int launch_prefix_e4m3(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
+                       int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream) {
     if (grid <= 0) return PKV_OK;
     CUtensorMap kvm;
-    const int rc = kv8 ? make_page_map_e4m3(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size)
-                       : make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
+    const int rc = make_page_map_e4m3(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
     if (rc) return rc;
-    if (kv8)
-        return head_size == 64 ? launch_prefill_hd<64, true, true>(p, kvm, query, q_stride, grid, dev, stream)
-                               : launch_prefill_hd<128, true, true>(p, kvm, query, q_stride, grid, dev, stream);
-    if (head_size == 64) return launch_prefill_hd<64, true, false>(p, kvm, query, q_stride, grid, dev, stream);
-    return launch_prefill_hd<128, true, false>(p, kvm, query, q_stride, grid, dev, stream);
+    return head_size == 64 ? launch_prefill_hd<64, true>(p, kvm, query, q_stride, grid, dev, stream)
+                           : launch_prefill_hd<128, true>(p, kvm, query, q_stride, grid, dev, stream);
 }
 
-int launch_prefill(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
-                   const void *kv_cache, int64_t num_blocks, int32_t head_size, int64_t grid, int dev,
-                   cudaStream_t stream, bool kv8) {
-    (void)num_tokens;
+int launch_prefill_e4m3(const PrefillParams &p, const void *query, int64_t q_stride, const void *kv_cache,
+                        int64_t num_blocks, int32_t head_size, int64_t grid, int dev, cudaStream_t stream) {
     if (grid <= 0) return PKV_OK;
     CUtensorMap kvm;
-    const int rc = kv8 ? make_page_map_e4m3(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size)
-                       : make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
+    const int rc = make_page_map_e4m3(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
     if (rc) return rc;
-    if (kv8)
-        return head_size == 64 ? launch_prefill_hd<64, false, true>(p, kvm, query, q_stride, grid, dev, stream)
-                               : launch_prefill_hd<128, false, true>(p, kvm, query, q_stride, grid, dev, stream);
-    if (head_size == 64) return launch_prefill_hd<64, false, false>(p, kvm, query, q_stride, grid, dev, stream);
-    return launch_prefill_hd<128, false, false>(p, kvm, query, q_stride, grid, dev, stream);
+    return head_size == 64 ? launch_prefill_hd<64, false>(p, kvm, query, q_stride, grid, dev, stream)
+                           : launch_prefill_hd<128, false>(p, kvm, query, q_stride, grid, dev, stream);
 }
 
 // Tensor map of the cache as {head_size, 16, 2, kv heads, blocks}; a box is
 // the K (or V) rows of one page, 64 columns, 128-byte swizzle.
-static int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
-                         int32_t head_size) {
+int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                  int32_t head_size) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PKV_ERR_CUDA;
     const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2, static_cast<cuuint64_t>(num_kv_heads),
@@ -1028,8 +853,8 @@ static int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blo
 // Tensor map of an E4M3 cache as bytes {head_size, 16, 2, kv heads, blocks};
 // a box is the K (or V) rows of one page, unswizzled (the converter warps
 // widen them).
-static int make_page_map_e4m3(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
-                              int32_t head_size) {
+int make_page_map_e4m3(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t head_size) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return PKV_ERR_CUDA;
     const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2, static_cast<cuuint64_t>(num_kv_heads),

@@ -17,6 +17,7 @@ from gpu_path import new_pool, to_dev, workspace_for, write_history
 pytestmark = pytest.mark.gpu
 
 DECODE_TILE_MAX_ROWS = 64      # rows above this go to the tensor-core prefill kernel
+ITEM_ROWS = 128                # rows of one work item of that kernel
 
 
 def prefill_items(step):
@@ -25,7 +26,7 @@ def prefill_items(step):
     for r in range(step.num_seqs):
         rows = (int(step.query_start_loc[r + 1]) - int(step.query_start_loc[r])) * G
         if rows > DECODE_TILE_MAX_ROWS:
-            n += -(-rows // 128) * step.num_kv_heads
+            n += -(-rows // ITEM_ROWS) * step.num_kv_heads
     return n
 
 
