@@ -28,7 +28,7 @@ struct WsHeader {
     int32_t next_ptile_item;    // prefill kernel: next work item to claim, less its grid size
     int32_t next_prefix_item;   // shared-prefix pass: the same
     int32_t n_split_tokens;     // tokens whose rows the combine merges
-    int32_t pad_;
+    int32_t epoch;              // decode kernel that plans itself: bumped once the header is written
     int64_t off_req;         // int4 [num_seqs]: {splits (0: refused), partial row base, first chunk, chunks}
     int64_t off_stoks;       // int4 [num_tokens]: split tokens {token, partial row of q head 0, splits, 0}
     int64_t off_chunks;      // int4 [max_chunks]: {request, split or tile, page begin, page end}
@@ -55,6 +55,52 @@ struct WsLayout {
     int64_t max_chunks, max_ptiles, max_crows, max_prow;
     int32_t prefix_parts;     // splits of the shared prefix (0: no cascade)
 };
+
+// ---- splitting decode rows along their keys (the plan kernel, and the decode
+// kernel when it plans a call itself, take the same decisions) ----
+
+__host__ __device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
+
+// Pages per warp up to which a warp takes one chunk.
+constexpr unsigned long long kOneChunkPages = 24;
+
+// The automatic split size from the call's decode work (pages x kv heads)
+// and the decode grid's warps.  Chunks of 4..64 pages.  Each chunk starts with
+// a chain of dependent loads (its record, the request's lengths, the block
+// table and Q), so a small batch (at most kOneChunkPages pages per warp) gets
+// one chunk per warp; a larger one about three per warp, so that the warps
+// finish together.
+__device__ __forceinline__ int auto_pages_per_split(unsigned long long total_pages, int num_kv_heads,
+                                                    int total_warps) {
+    const unsigned long long work = total_pages * (unsigned long long)num_kv_heads;
+    const unsigned long long warps = (unsigned long long)max(total_warps, 1);
+    const unsigned long long per1 = (work + warps - 1) / warps;
+    const unsigned long long per = per1 <= kOneChunkPages ? per1 : (work + 3 * warps - 1) / (3 * warps);
+    return (int)min(64ull, max(4ull, per));
+}
+
+// {pages per split, splits} of a split row whose keys span `span` pages: at
+// most `cap` splits; num_splits > 0 asks for that many, else splits of about
+// pages_per_split pages; no split is empty.
+__device__ __forceinline__ int2 split_geometry(int span, int pages_per_split, int num_splits, int cap) {
+    int n;
+    if (num_splits > 0) {
+        n = min(min(num_splits, cap), span);
+    } else {
+        const int per = max(pages_per_split, div_up(span, cap));
+        n = div_up(span, per);
+    }
+    const int per_split = div_up(span, n);
+    return make_int2(per_split, div_up(span, per_split));
+}
+
+// Is request r's metadata consistent (query rows [q0, q1), L keys)?
+__device__ __forceinline__ bool request_valid(int q0, int q1, int L, int num_tokens, int max_seq_len,
+                                              int max_query_len, int max_blocks_per_seq) {
+    const int q = q1 - q0;
+    return !(q0 < 0 || q < 0 || q1 > num_tokens || L < q || L > max_seq_len || q > max_query_len ||
+             div_up(L, kBlock) > max_blocks_per_seq);
+}
 
 // CTAs the shared-prefix pass aims for: one per SM of a 152-SM part (the
 // kernel holds all of an SM's tensor memory).  Only the balance depends on it.
@@ -151,7 +197,33 @@ struct AttnParams {
     float scale_log2;         // scale * log2(e)
     float k_scale, v_scale;   // E4M3 cache: stored code * scale is the value (1 for bf16)
     uint8_t *ws;
+    // self_plan = 1: no plan kernel ran; the decode kernel plans the call
+    // itself (see decode_self_plan_ok) and writes what the combine reads
+    int32_t self_plan;
+    int32_t num_seqs, num_tokens, head_size, max_query_len, max_seq_len;
+    int32_t total_warps;      // warps of the decode grid
+    WsLayout lay;
 };
+
+// Requests a decode kernel plans by itself at most (their lengths and plans
+// sit in its shared memory before its rings are used).
+constexpr int kSelfPlanSeqs = 1024;
+
+// May the decode kernel plan this call itself?  Every request is a split row
+// (max_query_len * G <= 16), nothing else runs (no prefill, no shared
+// prefix), the split size is automatic, and the batch is small enough that
+// every warp takes at most two chunks: num_seqs * kv heads <= warps, and the
+// bound on the pages (num_seqs * ceil(max_seq_len / 16) * kv heads) is at
+// most kOneChunkPages per warp.  (Then the plan's size order is moot: the
+// chunks number at most the warps plus one per (request, kv head).)
+inline bool decode_self_plan_ok(int64_t num_seqs, int64_t max_query_len, int64_t max_seq_len, int64_t G,
+                                int64_t num_kv_heads, int64_t num_splits, int64_t prefix_blocks, int64_t warps) {
+    if (num_seqs < 1 || num_seqs > kSelfPlanSeqs || num_splits != 0 || prefix_blocks != 0) return false;
+    if (max_query_len * G > 16) return false;
+    if (num_seqs * num_kv_heads > warps) return false;
+    const int64_t pages = (max_seq_len + kBlock - 1) / kBlock;
+    return num_seqs * pages * num_kv_heads <= static_cast<int64_t>(kOneChunkPages) * warps;
+}
 
 // Decode grid: persistent CTAs of kDecodeWarps warps, decode_ctas_per_sm()
 // per SM (set by the tiling of the head size and cache type).

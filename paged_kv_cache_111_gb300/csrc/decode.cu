@@ -156,6 +156,218 @@ static_assert(DecodeTiling<64>::NW == kDecodeWarps && DecodeTiling<128>::NW == k
                   DecodeTiling<64, true>::NW == kDecodeWarps && DecodeTiling<128, true>::NW == kDecodeWarps,
               "every decode tiling has kDecodeWarps warps per CTA");
 
+// ---- the decode kernel's own plan ---------------------------------------------
+//
+// For a call that decode_self_plan_ok admits (every request a split row, a
+// batch small enough that every warp takes at most two chunks) no plan kernel
+// runs.  Every CTA plans the whole call in shared memory (the space its rings
+// take later) with the plan kernel's decisions (request_valid, the automatic
+// split size, split_geometry), lists chunks in request order, and takes its
+// warps' chunks from that list; CTA 0 also writes what the combine and the
+// caller read (header, status, split tokens).
+
+// One chunk of a warp: request, split, page range, the request's splits and
+// first partial row.
+struct SelfChunk {
+    int r, k, pb, npages, n_split, pbase;
+};
+
+struct SelfPlanShared {
+    unsigned long long total_pages;
+    int bad, fits;
+    int4 warp_tot[kDecodeWarps];
+    int4 tot;
+};
+
+// The plan of the call in `scr` (8 * num_seqs + 1 ints) and the chunks of
+// this warp (round 0 and round 1 of the snake order); returns the number of
+// items (chunks x kv heads), 0 when the metadata does not fit the workspace.
+template <int NW>
+__device__ int decode_self_plan(const AttnParams &p, int *scr, SelfPlanShared &sh, SelfChunk (&mine)[2]) {
+    const int S = p.num_seqs, tid = threadIdx.x, nthr = NW * 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    int *s_qsl = scr, *s_len = scr + S + 1, *s_cb = s_len + S, *s_nc = s_cb + S, *s_ps = s_nc + S;
+    int *s_pg = s_ps + S, *s_pb = s_pg + S, *s_sb = s_pb + S;
+    for (int r = tid; r <= S; r += nthr) s_qsl[r] = __ldg(p.qsl + r);
+    for (int r = tid; r < S; r += nthr) s_len[r] = __ldg(p.seq_lens + r);
+    if (tid == 0) {
+        sh.total_pages = 0;
+        sh.bad = 0;
+    }
+    __syncthreads();
+    // total key pages (sets the automatic split size), and the metadata check
+    unsigned long long pages = 0;
+    int bad = tid == 0 && s_qsl[0] != 0;
+    for (int r = tid; r < S; r += nthr) {
+        const int q0 = s_qsl[r], q1 = s_qsl[r + 1], L = s_len[r];
+        if (!request_valid(q0, q1, L, p.num_tokens, p.max_seq_len, p.max_query_len, p.max_blocks_per_seq)) bad = 1;
+        else if (q1 > q0) pages += static_cast<unsigned long long>(div_up(L, kBlock));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) pages += __shfl_xor_sync(0xffffffffu, pages, o);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        if (pages) atomicAdd(&sh.total_pages, pages);
+        if (bad) sh.bad = 1;
+    }
+    __syncthreads();
+    const int pps = auto_pages_per_split(sh.total_pages, p.num_kv_heads, p.total_warps);
+    // per request: chunks, pages per split, partial rows and split tokens; each
+    // thread a contiguous range of requests, one block scan for the bases
+    const int per_thr = div_up(S, nthr);
+    const int r_begin = min(S, tid * per_thr), r_end = min(S, r_begin + per_thr);
+    int4 cnt = make_int4(0, 0, 0, 0);
+    for (int r = r_begin; r < r_end; ++r) {
+        const int q0 = s_qsl[r], q1 = s_qsl[r + 1], L = s_len[r];
+        const int q = q1 - q0;
+        int n = 0, ps = 0, span = 0;
+        if (q > 0 && request_valid(q0, q1, L, p.num_tokens, p.max_seq_len, p.max_query_len, p.max_blocks_per_seq)) {
+            span = div_up(L, kBlock);
+            const int2 sg = split_geometry(span, pps, 0, kMaxSplits);
+            ps = sg.x;
+            n = sg.y;
+        }
+        s_nc[r] = n;
+        s_ps[r] = ps;
+        s_pg[r] = span;
+        cnt.x += n;
+        if (n > 1) {
+            cnt.y += q * p.num_q_heads * n;
+            cnt.z += q;
+        }
+    }
+    int4 inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, inc.x, o), b = __shfl_up_sync(0xffffffffu, inc.y, o);
+        const int c = __shfl_up_sync(0xffffffffu, inc.z, o);
+        if (lane >= o) {
+            inc.x += a;
+            inc.y += b;
+            inc.z += c;
+        }
+    }
+    if (lane == 31) sh.warp_tot[warp] = inc;
+    __syncthreads();
+    if (tid == 0) {
+        int4 acc = make_int4(0, 0, 0, 0);
+        for (int w = 0; w < NW; ++w) {
+            const int4 t = sh.warp_tot[w];
+            sh.warp_tot[w] = acc;
+            acc.x += t.x;
+            acc.y += t.y;
+            acc.z += t.z;
+        }
+        sh.tot = acc;
+        sh.fits = acc.x <= p.lay.max_chunks && acc.y <= p.lay.max_prow && acc.z <= p.num_tokens;
+        if (!sh.fits) sh.bad = 1;
+    }
+    __syncthreads();
+    {
+        const int4 wb = sh.warp_tot[warp];
+        int cb = wb.x + inc.x - cnt.x, pb = wb.y + inc.y - cnt.y, sb = wb.z + inc.z - cnt.z;
+        for (int r = r_begin; r < r_end; ++r) {
+            const int n = s_nc[r];
+            s_cb[r] = cb;
+            s_pb[r] = pb;
+            s_sb[r] = sb;
+            cb += n;
+            if (n > 1) {
+                const int q = s_qsl[r + 1] - s_qsl[r];
+                pb += q * p.num_q_heads * n;
+                sb += q;
+            }
+        }
+    }
+    __syncthreads();
+    const int n_items = sh.fits ? sh.tot.x * p.num_kv_heads : 0;
+    // this warp's chunks: items wid and 2 W - 1 - wid (the snake order of the loop)
+    const int W = gridDim.x * NW, wid = blockIdx.x * NW + warp;
+#pragma unroll
+    for (int round = 0; round < 2; ++round) {
+        const int item = round ? 2 * W - 1 - wid : wid;
+        SelfChunk c{-1, 0, 0, 0, 1, 0};
+        if (item < n_items) {
+            const int ch = item / p.num_kv_heads;
+            // the request of chunk ch: the last with chunk base <= ch, past any
+            // request without chunks
+            int lo = 0, hi = S - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_cb[mid] <= ch) lo = mid;
+                else hi = mid - 1;
+            }
+            while (lo < S - 1 && s_nc[lo] == 0) ++lo;
+            c.r = lo;
+            c.k = ch - s_cb[lo];
+            c.pb = c.k * s_ps[lo];
+            c.npages = min(s_pg[lo], c.pb + s_ps[lo]) - c.pb;
+            c.n_split = s_nc[lo] > 1 ? s_nc[lo] : 1;
+            c.pbase = s_nc[lo] > 1 ? s_pb[lo] : 0;
+        }
+        mine[round] = c;
+    }
+    return n_items;
+}
+
+// CTA 0 of a self-planned call: the header, status, request table and split
+// tokens the plan kernel would have written (after every earlier kernel on
+// the stream is complete), then the header's epoch is bumped.
+template <int NW>
+__device__ void decode_self_plan_publish(const AttnParams &p, const int *scr, const SelfPlanShared &sh) {
+    const int S = p.num_seqs, tid = threadIdx.x, nthr = NW * 32;
+    const int *s_qsl = scr, *s_len = scr + S + 1, *s_cb = s_len + S, *s_nc = s_cb + S;
+    const int *s_pb = s_nc + 2 * S + S, *s_sb = s_pb + S;
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
+    int4 *req_ws = reinterpret_cast<int4 *>(p.ws + p.lay.off_req);
+    int4 *stoks = reinterpret_cast<int4 *>(p.ws + p.lay.off_stoks);
+    const bool fits = sh.fits != 0;
+    for (int i = tid; i < 2 * kStatsCtas; i += nthr) reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[i] = 0;
+    for (int r = tid; r < S; r += nthr) {
+        const int n = fits ? s_nc[r] : 0;
+        const int q0 = s_qsl[r];
+        const int q = s_qsl[r + 1] - q0;
+        const bool valid = request_valid(q0, s_qsl[r + 1], s_len[r], p.num_tokens, p.max_seq_len, p.max_query_len,
+                                         p.max_blocks_per_seq);
+        req_ws[r] = make_int4(valid && fits ? (n > 1 ? n : 1) : 0, n > 1 ? s_pb[r] : 0, s_cb[r], n);
+        if (n > 1)
+            for (int i = 0; i < q; ++i)
+                stoks[s_sb[r] + i] = make_int4(q0 + i, s_pb[r] + i * p.num_q_heads * n, n, 0);
+    }
+    if (tid == 0) {
+        hdr->status = sh.bad ? PKV_ERR_DEVICE_METADATA : PKV_OK;
+        hdr->magic = kMagic;
+        hdr->n_chunks = fits ? sh.tot.x : 0;
+        hdr->num_tokens = p.num_tokens;
+        hdr->num_q_heads = p.num_q_heads;
+        hdr->head_size = p.head_size;
+        hdr->num_seqs = S;
+        hdr->pages_per_split = auto_pages_per_split(sh.total_pages, p.num_kv_heads, p.total_warps);
+        hdr->n_ptiles = 0;
+        hdr->n_crows = 0;
+        hdr->prefix_blocks = 0;
+        hdr->prefix_parts = 0;
+        hdr->next_ptile_item = 0;
+        hdr->next_prefix_item = 0;
+        hdr->n_split_tokens = fits ? sh.tot.z : 0;
+        hdr->off_req = p.lay.off_req;
+        hdr->off_stoks = p.lay.off_stoks;
+        hdr->off_chunks = p.lay.off_chunks;
+        hdr->off_ptiles = p.lay.off_ptiles;
+        hdr->off_crows = p.lay.off_crows;
+        hdr->off_part_lse = p.lay.off_part_lse;
+        hdr->off_part_o = p.lay.off_part_o;
+        hdr->max_chunks = p.lay.max_chunks;
+        hdr->max_ptiles = p.lay.max_ptiles;
+        hdr->max_crows = p.lay.max_crows;
+        hdr->max_prow = p.lay.max_prow;
+        hdr->prow_used = sh.tot.y;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) atomicAdd(&hdr->epoch, 1);
+}
+
 template <int HD, int NW, int DEPTH, bool KV8>
 __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const AttnParams p) {
@@ -179,15 +391,40 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
     }
     fence_barrier_init();
     __syncwarp();
-    pdl_wait();       // the plan (and the cache write before it) are complete
-    pdl_trigger();
-    const WsHeader *hdr = reinterpret_cast<const WsHeader *>(p.ws);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
     int32_t *status = reinterpret_cast<int32_t *>(p.ws);
-    const int4 *req = reinterpret_cast<const int4 *>(p.ws + hdr->off_req);
-    const int4 *chunks = reinterpret_cast<const int4 *>(p.ws + hdr->off_chunks);
-    float *part_lse = reinterpret_cast<float *>(p.ws + hdr->off_part_lse);
-    float *part_o = reinterpret_cast<float *>(p.ws + hdr->off_part_o);
-    const int n_items = hdr->n_chunks * p.num_kv_heads;
+    // a self-planned call: the plan in shared memory (the rings' space), read
+    // and made while the kernel before this one may still run (it reads only
+    // the call's metadata)
+    __shared__ SelfPlanShared sp_shared;
+    SelfChunk self_chunks[2];
+    int n_items = 0;
+    if (p.self_plan) {
+        n_items = decode_self_plan<NW>(p, reinterpret_cast<int *>(smem), sp_shared, self_chunks);
+        // the cache write before this kernel (and everything before it) is complete
+        pdl_wait();
+        if (blockIdx.x == 0) decode_self_plan_publish<NW>(p, reinterpret_cast<const int *>(smem), sp_shared);
+        __syncthreads();         // the plan's shared memory is the rings' from here on
+    } else {
+        pdl_wait();       // the plan (and the cache write before it) are complete
+    }
+    pdl_trigger();
+    // an error of a self-planned call is stored once CTA 0 has reset the status
+    // (the header's epoch moved on), so that the reset never overwrites it
+    const int epoch0 = p.self_plan ? *reinterpret_cast<volatile int32_t *>(&hdr->epoch) : 0;
+    auto report = [&](int32_t code) {
+        if (p.self_plan && blockIdx.x != 0) {
+            const uint64_t t0 = global_ns();
+            while (*reinterpret_cast<volatile int32_t *>(&hdr->epoch) == epoch0 && global_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        set_status(status, code);
+    };
+    const int4 *req = reinterpret_cast<const int4 *>(p.ws + (p.self_plan ? p.lay.off_req : hdr->off_req));
+    const int4 *chunks = reinterpret_cast<const int4 *>(p.ws + (p.self_plan ? p.lay.off_chunks : hdr->off_chunks));
+    float *part_lse = reinterpret_cast<float *>(p.ws + (p.self_plan ? p.lay.off_part_lse : hdr->off_part_lse));
+    float *part_o = reinterpret_cast<float *>(p.ws + (p.self_plan ? p.lay.off_part_o : hdr->off_part_o));
+    if (!p.self_plan) n_items = hdr->n_chunks * p.num_kv_heads;
 
     const int W = gridDim.x * NW;
     const int wid = blockIdx.x * NW + warp;
@@ -199,7 +436,9 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
     for (int round = 0; round * W < n_items; ++round) {
         const int item = (round & 1) ? round * W + (W - 1 - wid) : round * W + wid;   // snake order
         if (item >= n_items) continue;
-        const int4 ch = chunks[item / p.num_kv_heads];
+        // (a self-planned call has at most two rounds)
+        const SelfChunk sc = (round & 1) ? self_chunks[1] : self_chunks[0];
+        const int4 ch = p.self_plan ? make_int4(sc.r, sc.k, sc.pb, sc.pb + sc.npages) : chunks[item / p.num_kv_heads];
         const int g = item % p.num_kv_heads;
         const int r = ch.x;
         const int pb = ch.z;
@@ -212,7 +451,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
         const bool split_mode = rows_total <= 16;
         const int tile = split_mode ? 0 : ch.y;
         const int split = split_mode ? ch.y : 0;
-        const int4 info = req[r];
+        const int4 info = p.self_plan ? make_int4(sc.n_split, sc.pbase, 0, 0) : req[r];
         const int n_split = split_mode ? info.x : 1;
         const int rows = min(16, rows_total - 16 * tile);
 
@@ -231,7 +470,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
         auto issue = [&](int k) {            // page k of this chunk -> its ring stage
             const int blk = __shfl_sync(0xffffffffu, win, k - wbase);
             if (lane == 0) {
-                if (blk < 0 || blk >= p.num_blocks) set_status(status, PKV_ERR_DEVICE_INDEX);
+                if (blk < 0 || blk >= p.num_blocks) report(PKV_ERR_DEVICE_INDEX);
                 const uint32_t st = (seq + k) % DEPTH;
                 uint8_t *dst = ring + st * Cfg::kStageBytes;
                 mbar_arrive_expect_tx(&bars[st], Cfg::kStageBytes);
@@ -472,7 +711,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
         }
 
         if (failed_at >= 0) {
-            set_status(status, PKV_ERR_DEVICE_TIMEOUT);
+            report(PKV_ERR_DEVICE_TIMEOUT);
             // let copies already in flight land before the CTA's memory is released
             for (int k = failed_at; k < issued; ++k) {
                 const uint32_t st = (seq + k) % DEPTH;

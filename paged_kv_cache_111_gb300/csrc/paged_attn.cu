@@ -39,7 +39,6 @@ namespace pkv {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kSizeBins = 256;      // counting-sort bins for chunk sizes (pages or KV tiles)
-constexpr unsigned long long kOneChunkPages = 24;   // pages per warp up to which a warp takes one chunk
 
 // ---- workspace layout ---------------------------------------------------------
 
@@ -114,8 +113,6 @@ struct PlanParams {
 
 // ---- 1. planning ------------------------------------------------------------------
 
-__device__ __forceinline__ int div_up(int a, int b) { return (a + b - 1) / b; }
-
 // Work of request r.  mode 0: rows split along key pages (q_r * G <= 16);
 // mode 1: 16-row tiles on the decode kernel; mode 2: 128-row tiles on the
 // tensor-core prefill kernel.
@@ -149,9 +146,7 @@ __device__ ReqPlan plan_request(const PlanParams &p, const int *qsl, const int *
     const int q0 = qsl[r], q1 = qsl[r + 1];
     const int q = q1 - q0;
     const int L = lens[r];
-    if (q0 < 0 || q < 0 || q1 > p.num_tokens || L < q || L > p.max_seq_len || q > p.max_query_len ||
-        div_up(L, kBlock) > p.max_blocks_per_seq)
-        return rp;
+    if (!request_valid(q0, q1, L, p.num_tokens, p.max_seq_len, p.max_query_len, p.max_blocks_per_seq)) return rp;
     rp.valid = 1;
     rp.q = q;
     rp.ctx = L - q;
@@ -162,17 +157,11 @@ __device__ ReqPlan plan_request(const PlanParams &p, const int *qsl, const int *
         rp.pages = div_up(L, kBlock);
         rp.first = cascade ? p.prefix_blocks : 0;
         const int span = rp.pages - rp.first;            // >= 1: a cascade row sees a key past the prefix
-        int n;
         // at most kMaxSplits splits in all (the combine's limit), prefix ranges included
         const int cap = cascade ? kMaxSplits - p.lay.prefix_parts : kMaxSplits;
-        if (p.num_splits > 0) {
-            n = min(min(p.num_splits, cap), span);
-        } else {
-            const int per = max(pages_per_split, div_up(span, cap));
-            n = div_up(span, per);
-        }
-        rp.per_split = div_up(span, n);
-        rp.n_chunks = div_up(span, rp.per_split);        // no empty split
+        const int2 sg = split_geometry(span, pages_per_split, p.num_splits, cap);
+        rp.per_split = sg.x;
+        rp.n_chunks = sg.y;
     } else if (p.prefill_ok && rp.rows > kDecodeTileMaxRows) {
         rp.mode = 2;
         rp.n_chunks = div_up(rp.rows, kPrefillRows);
@@ -393,18 +382,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     mine = warp_sum_u64(mine);
     if ((tid & 31) == 0 && mine) atomicAdd(&total_pages, mine);
     __syncthreads();
-    if (tid == 0) {
-        // Chunks of 4..64 pages.  Each chunk starts with a chain of dependent loads
-        // (its record, the request's lengths, the block table and Q), so a small
-        // batch (at most kOneChunkPages pages per warp of the decode grid) gets one
-        // chunk per warp; a larger one about three per warp, largest first, so
-        // that the warps finish together.
-        const unsigned long long work = total_pages * (unsigned long long)p.num_kv_heads;
-        const unsigned long long warps = (unsigned long long)max(p.total_warps, 1);
-        const unsigned long long per1 = (work + warps - 1) / warps;
-        const unsigned long long per = per1 <= kOneChunkPages ? per1 : (work + 3 * warps - 1) / (3 * warps);
-        pages_per_split = (int)min(64ull, max(4ull, per));
-    }
+    if (tid == 0) pages_per_split = auto_pages_per_split(total_pages, p.num_kv_heads, p.total_warps);
     __syncthreads();
     const int pps = pages_per_split;
 
@@ -435,8 +413,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (staged) pdl_wait();       // the previous kernel on the stream may still read this workspace
     for (int i = tid; i < 2 * kStatsCtas; i += nthr) reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[i] = 0;
     const int n_total = totals.x;
+    // (split tokens too: with inconsistent query starts the requests' rows may
+    // overlap and number more than the tokens)
     const bool fits = n_total <= p.lay.max_chunks + p.lay.max_ptiles && totals.y <= p.lay.max_prow &&
-                      totals.z <= p.lay.max_crows;
+                      totals.z <= p.lay.max_crows && totals.w <= p.num_tokens;
     {
         int cb = pre.x, pbase = pre.y, crow = pre.z, sbase = pre.w;
         for (int r = r_begin; r < r_end; ++r) {
@@ -666,7 +646,11 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     pp.prefix_blocks = prefix_blocks;
     pp.block_tables = block_tables;
     pp.lay = lay;
-    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess) return PKV_ERR_CUDA;
+    // a small decode-only batch is planned by the decode kernel itself
+    const bool self_plan = !may_prefill && decode_self_plan_ok(num_seqs, max_query_len, max_seq_len, G, num_kv_heads,
+                                                               num_splits, prefix_blocks, grid * nw);
+    if (!self_plan && launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess)
+        return PKV_ERR_CUDA;
 
     AttnParams ap;
     ap.out = static_cast<__nv_bfloat16 *>(out);
@@ -684,6 +668,14 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     ap.k_scale = k_scale;
     ap.v_scale = v_scale;
     ap.ws = static_cast<uint8_t *>(workspace);
+    ap.self_plan = self_plan ? 1 : 0;
+    ap.num_seqs = num_seqs;
+    ap.num_tokens = num_tokens;
+    ap.head_size = head_size;
+    ap.max_query_len = max_query_len;
+    ap.max_seq_len = max_seq_len;
+    ap.total_warps = static_cast<int32_t>(grid * nw);
+    ap.lay = lay;
     rc = launch_decode_path(map, ap, head_size, kv8, static_cast<int>(grid), dev, st);
     if (rc || (!may_prefill && prefix_blocks == 0)) return rc;
     PrefillParams fp;
