@@ -45,17 +45,29 @@ SETTLE_S = 1.5          # seconds of untimed steps under the clock sampler befor
 # kernels.  Traffic grows with the KV bytes read, so a full launch's traffic is
 # the ratio times its algorithmic bytes.  A ratio holds only for the kernel
 # sources it was measured on (hash of the files below); otherwise null.
-TRAFFIC_SOURCES = ("decode.cu", "pkv_common.cuh", "paged_attn.cu", "prefill_tc.cu", "tc_common.cuh",
-                   "attn_internal.cuh")
+TRAFFIC_SOURCES = ("decode.cu", "pkv_common.cuh", "paged_attn.cu", "prefill_tc.cu", "prefill_sk.cu",
+                   "prefill_common.cuh", "tc_common.cuh", "attn_internal.cuh")
 TRAFFIC = {
     # "<cache> <kernels of the call>": decode (plan + decode), cascade (plus the
-    # shared-prefix pass), prefill (plus the tcgen05 chunk kernel)
-    "bf16 decode": {"sources_sha256_16": "", "ratio": None, "source": ""},
-    "e4m3 decode": {"sources_sha256_16": "", "ratio": None, "source": ""},
-    "bf16 cascade": {"sources_sha256_16": "", "ratio": None, "source": ""},
-    "e4m3 cascade": {"sources_sha256_16": "", "ratio": None, "source": ""},
-    "bf16 prefill": {"sources_sha256_16": "", "ratio": None, "source": ""},
-    "e4m3 prefill": {"sources_sha256_16": "", "ratio": None, "source": ""},
+    # shared-prefix pass), prefill (plus the tcgen05 chunk kernel).  ratio =
+    # (dram__bytes_read.sum + dram__bytes_write.sum of the call's kernels, one
+    # call, ncu with its default cache flush) / the call's algorithmic bytes.
+    # Writes that stay in L2 until after the kernel do not count, so a call
+    # whose output is large (a prefill chunk) reads below 1.
+    "bf16 decode": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 1045.1005e6 / 1033884588,
+                    "source": "ncu DRAM counters of plan + decode on llama13b-decode, first 64 requests"},
+    "e4m3 decode": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 524.3762e6 / 517604268,
+                    "source": "ncu DRAM counters of plan + decode on llama13b-decode, first 64 requests, E4M3"},
+    "bf16 cascade": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 29.4867e6 / 28294800,
+                     "source": "ncu DRAM counters of plan + decode + shared-prefix pass on llama3-70b-prefix, "
+                               "first 24 requests"},
+    "e4m3 cascade": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 15.2633e6 / 14544528,
+                     "source": "ncu DRAM counters of plan + decode + shared-prefix pass on llama3-70b-prefix, "
+                               "first 24 requests, E4M3"},
+    "bf16 prefill": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 34.3946e6 / 50947140,
+                     "source": "ncu DRAM counters of plan + decode + prefill on llama3-8b-mixed"},
+    "e4m3 prefill": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 25.7021e6 / 42251332,
+                     "source": "ncu DRAM counters of plan + decode + prefill on llama3-8b-mixed, E4M3"},
 }
 
 

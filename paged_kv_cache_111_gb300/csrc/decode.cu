@@ -163,8 +163,9 @@ static_assert(DecodeTiling<64>::NW == kDecodeWarps && DecodeTiling<128>::NW == k
 // runs.  Every CTA plans the whole call in shared memory (the space its rings
 // take later) with the plan kernel's decisions (request_valid, the automatic
 // split size, split_geometry), lists chunks in request order, and takes its
-// warps' chunks from that list; CTA 0 also writes what the combine and the
-// caller read (header, status, split tokens).
+// warps' chunks from that list.  The grid's last CTA takes no chunks: it
+// writes what the combine and the caller read (header, status, split tokens),
+// beside the other CTAs' work rather than before it.
 
 // One chunk of a warp: request, split, page range, the request's splits and
 // first partial row.
@@ -281,13 +282,14 @@ __device__ int decode_self_plan(const AttnParams &p, int *scr, SelfPlanShared &s
     }
     __syncthreads();
     const int n_items = sh.fits ? sh.tot.x * p.num_kv_heads : 0;
-    // this warp's chunks: items wid and 2 W - 1 - wid (the snake order of the loop)
-    const int W = gridDim.x * NW, wid = blockIdx.x * NW + warp;
+    // this warp's chunks: items wid and 2 W - 1 - wid (the snake order of the
+    // loop), W the warps of every CTA but the last
+    const int W = (gridDim.x - 1) * NW, wid = blockIdx.x * NW + warp;
 #pragma unroll
     for (int round = 0; round < 2; ++round) {
         const int item = round ? 2 * W - 1 - wid : wid;
         SelfChunk c{-1, 0, 0, 0, 1, 0};
-        if (item < n_items) {
+        if (wid < W && item < n_items) {
             const int ch = item / p.num_kv_heads;
             // the request of chunk ch: the last with chunk base <= ch, past any
             // request without chunks
@@ -310,26 +312,26 @@ __device__ int decode_self_plan(const AttnParams &p, int *scr, SelfPlanShared &s
     return n_items;
 }
 
-// CTA 0 of a self-planned call: the header, status, request table and split
-// tokens the plan kernel would have written (after every earlier kernel on
-// the stream is complete), then the header's epoch is bumped.
+// The last CTA of a self-planned call: the header, status and split tokens
+// the plan kernel would have written (after every earlier kernel on the
+// stream is complete), then the header's epoch is bumped.  (The request table
+// is the plan kernel's record for its own decode launches; a self-planned
+// call does not read it.)
 template <int NW>
 __device__ void decode_self_plan_publish(const AttnParams &p, const int *scr, const SelfPlanShared &sh) {
     const int S = p.num_seqs, tid = threadIdx.x, nthr = NW * 32;
     const int *s_qsl = scr, *s_len = scr + S + 1, *s_cb = s_len + S, *s_nc = s_cb + S;
     const int *s_pb = s_nc + 2 * S + S, *s_sb = s_pb + S;
     WsHeader *hdr = reinterpret_cast<WsHeader *>(p.ws);
-    int4 *req_ws = reinterpret_cast<int4 *>(p.ws + p.lay.off_req);
     int4 *stoks = reinterpret_cast<int4 *>(p.ws + p.lay.off_stoks);
     const bool fits = sh.fits != 0;
     for (int i = tid; i < 2 * kStatsCtas; i += nthr) reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[i] = 0;
+    (void)s_len;
+    (void)s_cb;
     for (int r = tid; r < S; r += nthr) {
         const int n = fits ? s_nc[r] : 0;
         const int q0 = s_qsl[r];
         const int q = s_qsl[r + 1] - q0;
-        const bool valid = request_valid(q0, s_qsl[r + 1], s_len[r], p.num_tokens, p.max_seq_len, p.max_query_len,
-                                         p.max_blocks_per_seq);
-        req_ws[r] = make_int4(valid && fits ? (n > 1 ? n : 1) : 0, n > 1 ? s_pb[r] : 0, s_cb[r], n);
         if (n > 1)
             for (int i = 0; i < q; ++i)
                 stoks[s_sb[r] + i] = make_int4(q0 + i, s_pb[r] + i * p.num_q_heads * n, n, 0);
@@ -403,17 +405,21 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
         n_items = decode_self_plan<NW>(p, reinterpret_cast<int *>(smem), sp_shared, self_chunks);
         // the cache write before this kernel (and everything before it) is complete
         pdl_wait();
-        if (blockIdx.x == 0) decode_self_plan_publish<NW>(p, reinterpret_cast<const int *>(smem), sp_shared);
+        if (blockIdx.x == gridDim.x - 1) {
+            decode_self_plan_publish<NW>(p, reinterpret_cast<const int *>(smem), sp_shared);
+            pdl_trigger();
+            return;                              // (no chunks of its own)
+        }
         __syncthreads();         // the plan's shared memory is the rings' from here on
     } else {
         pdl_wait();       // the plan (and the cache write before it) are complete
     }
     pdl_trigger();
-    // an error of a self-planned call is stored once CTA 0 has reset the status
-    // (the header's epoch moved on), so that the reset never overwrites it
+    // an error of a self-planned call is stored once the last CTA has reset the
+    // status (the header's epoch moved on), so that the reset never overwrites it
     const int epoch0 = p.self_plan ? *reinterpret_cast<volatile int32_t *>(&hdr->epoch) : 0;
     auto report = [&](int32_t code) {
-        if (p.self_plan && blockIdx.x != 0) {
+        if (p.self_plan) {
             const uint64_t t0 = global_ns();
             while (*reinterpret_cast<volatile int32_t *>(&hdr->epoch) == epoch0 && global_ns() - t0 < kWaitLimitNs) {
             }
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
     float *part_o = reinterpret_cast<float *>(p.ws + (p.self_plan ? p.lay.off_part_o : hdr->off_part_o));
     if (!p.self_plan) n_items = hdr->n_chunks * p.num_kv_heads;
 
-    const int W = gridDim.x * NW;
+    const int W = (p.self_plan ? gridDim.x - 1 : gridDim.x) * NW;   // (a self-planned call: not the last CTA)
     const int wid = blockIdx.x * NW + warp;
     uint32_t seq = 0;              // pages consumed so far by this warp (ring position)
     const int g4 = lane >> 2;      // fragment row within 8

@@ -621,10 +621,19 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
 
     const int nw = kDecodeWarps;
     const int per_sm = decode_ctas_per_sm(head_size, kv8);
-    int64_t grid = static_cast<int64_t>(sms) * per_sm;
+    const int64_t resident = static_cast<int64_t>(sms) * per_sm;
     const int64_t max_items = lay.max_chunks * num_kv_heads;
-    if (grid > (max_items + nw - 1) / nw) grid = (max_items + nw - 1) / nw;
-    if (grid < 1) grid = 1;
+    int64_t grid = std::max<int64_t>(1, std::min(resident, (max_items + nw - 1) / nw));
+    const int G = num_q_heads / num_kv_heads;
+    const bool may_prefill = prefill_ok && static_cast<int64_t>(max_query_len) * G > kDecodeTileMaxRows;
+    // a small decode-only batch is planned by the decode kernel itself: its
+    // last CTA writes the header, the others (still one wave) take the chunks
+    const int64_t sp_ctas = std::max<int64_t>(1, std::min(resident - 1, (max_items + nw - 1) / nw));
+    const bool self_plan = !may_prefill && resident >= 2 &&
+                           decode_self_plan_ok(num_seqs, max_query_len, max_seq_len, G, num_kv_heads, num_splits,
+                                               prefix_blocks, sp_ctas * nw);
+    if (self_plan) grid = sp_ctas + 1;
+    const int64_t chunk_warps = (self_plan ? sp_ctas : grid) * nw;
 
     PlanParams pp;
     pp.ws = static_cast<uint8_t *>(workspace);
@@ -639,16 +648,11 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     pp.max_query_len = max_query_len;
     pp.max_seq_len = max_seq_len;
     pp.num_splits = num_splits;
-    pp.total_warps = static_cast<int32_t>(grid * nw);
-    const int G = num_q_heads / num_kv_heads;
-    const bool may_prefill = prefill_ok && static_cast<int64_t>(max_query_len) * G > kDecodeTileMaxRows;
+    pp.total_warps = static_cast<int32_t>(chunk_warps);
     pp.prefill_ok = prefill_ok ? 1 : 0;
     pp.prefix_blocks = prefix_blocks;
     pp.block_tables = block_tables;
     pp.lay = lay;
-    // a small decode-only batch is planned by the decode kernel itself
-    const bool self_plan = !may_prefill && decode_self_plan_ok(num_seqs, max_query_len, max_seq_len, G, num_kv_heads,
-                                                               num_splits, prefix_blocks, grid * nw);
     if (!self_plan && launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess)
         return PKV_ERR_CUDA;
 
@@ -674,7 +678,7 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     ap.head_size = head_size;
     ap.max_query_len = max_query_len;
     ap.max_seq_len = max_seq_len;
-    ap.total_warps = static_cast<int32_t>(grid * nw);
+    ap.total_warps = static_cast<int32_t>(chunk_warps);
     ap.lay = lay;
     rc = launch_decode_path(map, ap, head_size, kv8, static_cast<int>(grid), dev, st);
     if (rc || (!may_prefill && prefix_blocks == 0)) return rc;
