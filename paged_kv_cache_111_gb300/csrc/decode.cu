@@ -33,16 +33,19 @@ __device__ __forceinline__ uint32_t swz(uint32_t box_base, int row, int chunk) {
 }
 
 // KV8 = false: bf16 cache; ring stages hold pages in the 16-bit layout the
-// MMA loads read (128-byte swizzled 64-column boxes).  KV8 = true: E4M3
-// cache; ring stages hold the raw 8-bit page, which the warp widens to f16
-// into a private staging page of the 16-bit layout before the MMAs.
+// MMA loads read (128-byte swizzled 64-column boxes of 32 rows, K rows 0..15
+// and V rows 16..31).  KV8 = true: E4M3 cache; ring stages hold the raw 8-bit
+// page, whose V rows the warp widens to f16 into a private staging area
+// before the MMAs (K is read from the raw page): the V halves of the 16-bit
+// boxes only, kVBoxBytes apart.
 template <int HD, int NW, int DEPTH, bool KV8>
 struct DecodeCfg {
     static constexpr int kBoxes = HD / 64;                 // 64-element boxes per row
     static constexpr int kBoxBytes = 2 * kBlock * 128;     // K and V rows of one box: 4 KiB
     static constexpr int kPageBytes = kBoxes * kBoxBytes;  // one 16-bit page of one kv head
     static constexpr int kStageBytes = KV8 ? 2 * kBlock * HD : kPageBytes;
-    static constexpr int kWarpBytes = DEPTH * kStageBytes + (KV8 ? kPageBytes : 0);
+    static constexpr int kVBoxBytes = kBlock * 128;        // V rows of one box: 2 KiB
+    static constexpr int kWarpBytes = DEPTH * kStageBytes + (KV8 ? kBoxes * kVBoxBytes : 0);
     static constexpr int kSmem = NW * kWarpBytes + NW * DEPTH * 8 + 1024;
 };
 
@@ -87,8 +90,9 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &h01, uint3
 }
 
 // Widen the V rows of one raw E4M3 page (linear [2][16][HD] bytes) into the
-// 16-bit staging page: f16 values, 128-byte swizzled 64-column boxes of 32
-// rows (V rows 16..31; K is read from the raw page directly).  Every lane
+// 16-bit staging area: f16 values, 128-byte swizzled 64-column boxes of the
+// V rows only (rows 16..31 of the 16-bit page's boxes, 2 KiB per box; `dst`
+// is the address row 0 of box 0 would have, 2 KiB before the area).  Every lane
 // converts 16-byte pieces, loading all of its pieces before converting any.
 // At HD = 128 a quarter-warp takes two rows, half a row each, in alternating
 // halves, so that both its 8-bit reads and its 16-bit stores hit eight
@@ -98,7 +102,7 @@ __device__ __forceinline__ void widen_e4m3_values(uint32_t src, uint32_t dst, in
     constexpr int kChunks = 2 * kBlock * HD / 16;          // pieces of the page (K and V)
     constexpr int kFirst = kChunks / 2;                    // the V rows' pieces
     constexpr int kPerLane = (kChunks - kFirst) / 32;      // 2 or 4
-    constexpr int kBoxBytes = 2 * kBlock * 128;
+    constexpr int kBoxBytes = kBlock * 128;                // V rows of one box
     static_assert(kChunks % 64 == 0, "whole V pieces per lane");
     auto piece = [&](int q, int &row, int &col) {
         if constexpr (HD == 128) {
@@ -385,7 +389,9 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
     uint8_t *ring = smem + warp * Cfg::kWarpBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * Cfg::kWarpBytes) + warp * DEPTH;
     const uint32_t ring_u32 = smem_u32(ring);
-    const uint32_t staging_u32 = ring_u32 + DEPTH * Cfg::kStageBytes;   // KV8 only
+    // E4M3: the staging area's V boxes, addressed as rows 16..31 of boxes kVBox apart
+    const uint32_t vbase_kv8 = ring_u32 + DEPTH * Cfg::kStageBytes - Cfg::kVBoxBytes;
+    constexpr uint32_t kVBox = KV8 ? Cfg::kVBoxBytes : Cfg::kBoxBytes;
 
     if (lane == 0) {
         for (int s = 0; s < DEPTH; ++s) mbar_init(&bars[s], 1);
@@ -570,7 +576,10 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
                 failed_at = k;
                 break;
             }
-            uint32_t page = ring_u32 + st * Cfg::kStageBytes;
+            const uint32_t page = ring_u32 + st * Cfg::kStageBytes;
+            // V rows 16..31 of box bx at swz(vbase + bx * kVBox, row, chunk): the ring
+            // stage's own boxes (bf16), or the staging area's V-only boxes (E4M3)
+            const uint32_t vbase = KV8 ? vbase_kv8 : page;
             const int j0 = (pb + k) * kBlock;       // first key of this page
             // E4M3: this lane's K bytes of keys g4 and 8 + g4 (HD/4 each, see the Q
             // fragments), straight from the raw page
@@ -585,8 +594,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
                                        "=r"(kraw[n][4 * v + 3])
                                      : "r"(page + (8 * n + g4) * HD + t4 * (HD / 4) + 16 * v));
                 // widen the V rows, then hand the stage back to the copy engine
-                widen_e4m3_values<HD>(page, staging_u32, lane);
-                page = staging_u32;
+                widen_e4m3_values<HD>(page, vbase_kv8, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 const int nk = k + DEPTH;
@@ -609,7 +617,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
                     const int rem = e % (nrows * 8);
                     const int row = kBlock + vfirst + rem / 8;
                     const int chunk = rem % 8;
-                    const uint32_t a = swz(page + bx * Cfg::kBoxBytes, row, chunk);
+                    const uint32_t a = swz(vbase + bx * kVBox, row, chunk);
                     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
                 }
                 __syncwarp();
@@ -691,7 +699,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
                 const int tok = ((lane >> 3) & 1) * 8 + (lane & 7);
                 const int chunk = (n % 8) + (lane >> 4);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(swz(page + bx * Cfg::kBoxBytes, kBlock + tok, chunk), b0, b1, b2, b3);
+                ldsm_x4_trans(swz(vbase + bx * kVBox, kBlock + tok, chunk), b0, b1, b2, b3);
                 Math::mma(o[n], pa, b0, b1);
                 Math::mma(o[n + 1], pa, b2, b3);
                 Math::mma(o[n], pl, b0, b1);
