@@ -54,19 +54,19 @@ TRAFFIC = {
     # call, ncu with its default cache flush) / the call's algorithmic bytes.
     # Writes that stay in L2 until after the kernel do not count, so a call
     # whose output is large (a prefill chunk) reads below 1.
-    "bf16 decode": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 1045.1005e6 / 1033884588,
+    "bf16 decode": {"sources_sha256_16": "75597ebd11531778", "ratio": 1045.1946e6 / 1033884588,
                     "source": "ncu DRAM counters of plan + decode on llama13b-decode, first 64 requests"},
-    "e4m3 decode": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 524.3762e6 / 517604268,
+    "e4m3 decode": {"sources_sha256_16": "75597ebd11531778", "ratio": 524.1284e6 / 517604268,
                     "source": "ncu DRAM counters of plan + decode on llama13b-decode, first 64 requests, E4M3"},
-    "bf16 cascade": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 29.4867e6 / 28294800,
+    "bf16 cascade": {"sources_sha256_16": "75597ebd11531778", "ratio": 29.4851e6 / 28294800,
                      "source": "ncu DRAM counters of plan + decode + shared-prefix pass on llama3-70b-prefix, "
                                "first 24 requests"},
-    "e4m3 cascade": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 15.2633e6 / 14544528,
+    "e4m3 cascade": {"sources_sha256_16": "75597ebd11531778", "ratio": 15.2561e6 / 14544528,
                      "source": "ncu DRAM counters of plan + decode + shared-prefix pass on llama3-70b-prefix, "
                                "first 24 requests, E4M3"},
-    "bf16 prefill": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 34.3946e6 / 50947140,
+    "bf16 prefill": {"sources_sha256_16": "75597ebd11531778", "ratio": 34.3895e6 / 50947140,
                      "source": "ncu DRAM counters of plan + decode + prefill on llama3-8b-mixed"},
-    "e4m3 prefill": {"sources_sha256_16": "8d40eb3c96341a6f", "ratio": 25.7021e6 / 42251332,
+    "e4m3 prefill": {"sources_sha256_16": "75597ebd11531778", "ratio": 25.7020e6 / 42251332,
                      "source": "ncu DRAM counters of plan + decode + prefill on llama3-8b-mixed, E4M3"},
 }
 
@@ -140,14 +140,40 @@ def shared_prefix_blocks(step: wl.Step) -> int:
     return min(k, ctx_min // step.block_size)
 
 
-def launches_per_step(step: wl.Step, prefix_blocks: int) -> int:
-    """Kernels of one layer-step: kv_write, plan, decode, combine; the prefill
-    kernel when some request has more than 64 rows (q_r * G) and the head
-    layout has a tensor-core tile; the shared-prefix kernel when asked for."""
+def has_prefill(step: wl.Step) -> bool:
+    """Does the call run the tensor-core chunk kernel (some request with more
+    than 64 rows q_r * G, and a head layout with a tensor-core tile)?"""
     G = step.num_q_heads // step.num_kv_heads
     tile_ok = step.head_size in (64, 128) and 128 % G == 0
-    n = 4
-    if tile_ok and step.max_query_len * G > 64:
+    return tile_ok and step.max_query_len * G > 64
+
+
+def decode_self_planned(step: wl.Step, prefix_blocks: int, fp8: bool, sms: int) -> bool:
+    """The library's rule (paged_attn.cu, decode_self_plan_ok) for a call whose
+    decode kernel plans itself, so that no plan kernel runs: every request a
+    split row, nothing else on the call, automatic splits, and a batch small
+    for the decode grid (its warps less the last CTA's)."""
+    G = step.num_q_heads // step.num_kv_heads
+    per_sm = {(64, False): 4, (128, False): 2, (64, True): 3, (128, True): 2}[(step.head_size, fp8)]
+    resident = sms * per_sm
+    pages = -(-step.max_seq_len // step.block_size)
+    splits = max(1, min(pages, 32))
+    max_chunks = step.num_seqs * splits + -(-(step.num_tokens * G) // 16) + step.num_seqs
+    max_items = max_chunks * step.num_kv_heads
+    warps = max(1, min(resident - 1, -(-max_items // 4))) * 4
+    return (not has_prefill(step) and resident >= 2 and prefix_blocks == 0 and 1 <= step.num_seqs <= 1024
+            and step.max_query_len * G <= 16 and step.num_seqs * step.num_kv_heads <= warps
+            and step.num_seqs * pages * step.num_kv_heads <= 24 * warps)
+
+
+def launches_per_step(step: wl.Step, prefix_blocks: int, fp8: bool, sms: int) -> int:
+    """Kernels of one layer-step: kv_write, plan (not when the decode kernel
+    plans the call itself), decode, combine; the prefill kernel when some
+    request has more than 64 rows; the shared-prefix kernel when asked for."""
+    G = step.num_q_heads // step.num_kv_heads
+    tile_ok = step.head_size in (64, 128) and 128 % G == 0
+    n = 3 if decode_self_planned(step, prefix_blocks if tile_ok else 0, fp8, sms) else 4
+    if has_prefill(step):
         n += 1
     if tile_ok and prefix_blocks > 0:
         n += 1
@@ -518,7 +544,9 @@ def run_gpu(args, rank: int, world: int) -> dict:
         read_gbs = x.numel() * 4 / (best * 1e-3) / 1e9
         del x
 
-    return {"step": step, "shared_prefix_blocks": K, "launches_per_step": launches_per_step(step, K),
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return {"step": step, "shared_prefix_blocks": K,
+            "launches_per_step": launches_per_step(step, K, args.kv_dtype == "fp8", sms),
             "fp8_scales": scales,
             "total_ms": total_ms, "kvw_ms": kvw_ms, "attn_ms": attn_ms, "comb_ms": comb_ms,
             "phase_step_ms": phase_per,
@@ -668,7 +696,7 @@ def traffic_key(step: wl.Step, fp8: bool, prefix_blocks: int) -> str:
     kind = "decode"
     if prefix_blocks:
         kind = "cascade"
-    elif launches_per_step(step, 0) > 4:
+    elif has_prefill(step):
         kind = "prefill"
     return ("e4m3 " if fp8 else "bf16 ") + kind
 
