@@ -68,13 +68,10 @@ template <> struct DecodeMath<true> {
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     }
-    // (x, y) -> f16x2 pair plus its f16x2 remainder (about 22 bits together)
-    static __device__ __forceinline__ void split(float x, float y, uint32_t &big, uint32_t &rest) {
+    // (x, y) -> one f16x2 pair
+    static __device__ __forceinline__ void round(float x, float y, uint32_t &h) {
         const __half2 b = __floats2half2_rn(x, y);
-        const float2 bf = __half22float2(b);
-        const __half2 r = __floats2half2_rn(x - bf.x, y - bf.y);
-        big = *reinterpret_cast<const uint32_t *>(&b);
-        rest = *reinterpret_cast<const uint32_t *>(&r);
+        h = *reinterpret_cast<const uint32_t *>(&b);
     }
 };
 
@@ -684,13 +681,22 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
             for (int e = 0; e < 8; ++e) pr[e] = fast_exp2(x[e] - (((e >> 1) & 1) ? ref1 : ref0));
             l0 += (pr[0] + pr[1] + pr[4] + pr[5]);
             l1 += (pr[2] + pr[3] + pr[6] + pr[7]);
-            // P as a 16-bit pair (hi + remainder): the PV product keeps about
-            // 16 bits (bf16) or 22 bits (f16) of each weight
+            // P for P V.  bf16 cache: a bf16 pair (hi + remainder), about 16 bits of
+            // each weight (one bf16 round, 8 bits, broke the tolerance on short rows).
+            // E4M3 cache: one f16 per weight, 11 bits (a relative error below 2^-11
+            // per weight, several times inside the tolerance), so one product per tile
             uint32_t pa[4], pl[4];
-            Math::split(pr[0], pr[1], pa[0], pl[0]);
-            Math::split(pr[2], pr[3], pa[1], pl[1]);
-            Math::split(pr[4], pr[5], pa[2], pl[2]);
-            Math::split(pr[6], pr[7], pa[3], pl[3]);
+            if constexpr (KV8) {
+                Math::round(pr[0], pr[1], pa[0]);
+                Math::round(pr[2], pr[3], pa[1]);
+                Math::round(pr[4], pr[5], pa[2]);
+                Math::round(pr[6], pr[7], pa[3]);
+            } else {
+                Math::split(pr[0], pr[1], pa[0], pl[0]);
+                Math::split(pr[2], pr[3], pa[1], pl[1]);
+                Math::split(pr[4], pr[5], pa[2], pl[2]);
+                Math::split(pr[6], pr[7], pa[3], pl[3]);
+            }
 
             // O += P V (V rows are the page's tokens, read transposed)
 #pragma unroll
@@ -702,8 +708,10 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
                 ldsm_x4_trans(swz(vbase + bx * kVBox, kBlock + tok, chunk), b0, b1, b2, b3);
                 Math::mma(o[n], pa, b0, b1);
                 Math::mma(o[n + 1], pa, b2, b3);
-                Math::mma(o[n], pl, b0, b1);
-                Math::mma(o[n + 1], pl, b2, b3);
+                if constexpr (!KV8) {
+                    Math::mma(o[n], pl, b0, b1);
+                    Math::mma(o[n + 1], pl, b2, b3);
+                }
             }
 
             if constexpr (!KV8) {
