@@ -120,11 +120,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_fn();
 
-// Tensor maps of the cache for the tile kernels: {head_size, 16, 2, kv heads,
-// blocks}; a box is the K (or V) rows of one page, 64 columns with 128-byte
-// swizzle (bf16), or a whole unswizzled row of bytes (E4M3).
-int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
-                  int32_t head_size);
+// Tensor map of an E4M3 cache for its tile kernels: {head_size, 16, 2, kv
+// heads, blocks}; a box is the K (or V) rows of one page as unswizzled bytes.
 int make_page_map_e4m3(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
                        int32_t head_size);
 

@@ -30,10 +30,15 @@
 // written.  Tensor memory: S0, S1, O_0, O_1 (512 columns at head size 128).
 // Q arrives by TMA (at head size 64 into the second of two buffers while the
 // current item runs; at 128 into the one buffer once the item's last S has
-// read it, about two tiles before the item ends).
+// read it, about two tiles before the item ends).  K and V of a tile arrive
+// together, one 4 KiB box per (page, 64-column half), into a ring stage that
+// both products read in place (K's rows at one stride for S, each page's V
+// rows for P V).
 // Warp roles (384 threads): warp 0 claims items and loads Q (TMA, for a
-// chunk) and K and V pages through the block table (TMA, separate rings);
-// warp 1 issues the MMAs; warp 2 owns the tensor-memory allocation; for the
+// chunk) and the tiles' pages through the block table (TMA); warp 1 issues
+// the MMAs, each as soon as its operands are ready (an S product while the
+// previous tile's P is still being written, a P V product while the next
+// stage is still loading); warp 2 owns the tensor-memory allocation; for the
 // shared-prefix pass, whose rows come from many requests, warps 2 and 3
 // gather Q rows with asynchronous copies instead; warps 4-7 take keys 0-63 of
 // every tile, warps 8-11 keys 64-127 (warp w reads the tensor-memory lanes of
@@ -46,12 +51,14 @@
 // P V, so NaN in unwritten cache slots never meets a zero weight.  Every wait
 // is bounded.
 //
-// What bounds it: every item re-reads its K and V tiles from L2 (64 KB per
-// tile at head size 128), and with every SM loading page boxes the copies
-// arrive at about 28 bytes per clock per SM (~8 TB/s in all), below what the
-// tensor pipe and the softmax need per tile; the tiles' loads, not the
-// products, set the pace.  More query rows per K/V tile (two row tiles
-// sharing one K/V stream) is the way past it.
+// What bounds it: the MMA thread's issue.  A tile takes 16 products of
+// 128 x 128 x 16 (8 for S, 8 for P V), about 1,000 cycles of tensor pipe, but
+// the issuing thread shares its sub-partition's scheduler with the two
+// softmax warps of tensor-memory lane quadrant 1 (a warp reads only its
+// quadrant's lanes, and the quadrant is the sub-partition), and their
+// tensor-memory loads and stores and exponentials slow each issue from about
+// 90 to 130-240 cycles.  The softmax reads S once and stores P and its
+// remainder in one instruction per 32 keys for that reason.
 #include <mutex>
 
 #include "prefill_common.cuh"
@@ -61,22 +68,34 @@ namespace pkv {
 template <int HD>
 struct SKCfg {
     static constexpr int kHalves = HD / 64;
-    static constexpr int kTileBytes = kHalves * 128 * 128;   // 128 rows x HD bf16, 64-column boxes
-    // Q buffers and K / V ring depths.  A V tile is read at the end of its
-    // tile's work and its stage is refilled only then, so the V ring is the
-    // deeper one; a K stage frees as soon as S is computed.  At head size 128
-    // one Q buffer: the next item's Q loads after the item's last S, about two
-    // tiles before the item ends.
+    static constexpr int kTileBytes = kHalves * 128 * 128;   // 128 rows x HD bf16 (a Q tile, or K or V of 128 keys)
+    // A ring stage holds K and V of one 128-key tile as they land: one box per
+    // (page, 64-column half of the head) of 4 KiB, laid out
+    //   [token half th][K, V][token t % 8][64 columns]    (128-byte rows, 128-byte swizzle)
+    // at half * kHalfBytes + page * kBoxBytes.  K's rows of the tile then sit at
+    // one stride (8-row groups 2 KiB apart, in key order) for the S product, and
+    // each page's V rows likewise for P V, so both products read the stage in
+    // place: 16 boxes per tile at head size 128 instead of 32 separate K and V
+    // boxes of 2 KiB, and the copy engine takes a box in about the same time
+    // whatever its size up to 4 KiB.
+    static constexpr int kBoxBytes = 4096;
+    static constexpr int kHalfBytes = (kPrefillKeys / kBlock) * kBoxBytes;
+    static constexpr int kStageBytes = kHalves * kHalfBytes;    // = 2 kTileBytes
+    // Q buffers and ring depth.  A stage is refilled once both P V products of
+    // its tile have read it, so the copies of tile j + 3 start when tile j's
+    // products complete.  At head size 128 three stages (192 KiB) leave room for
+    // one Q buffer, loaded once the item's last S product has read the previous
+    // Q (about two tiles before the item ends), and for no alignment slack: the
+    // dynamic shared memory must start 1 KiB-aligned (checked at entry).
     static constexpr int kQBufs = HD == 128 ? 1 : 2;
-    static constexpr int kStagesK = HD == 128 ? 2 : 4;
-    static constexpr int kStagesV = HD == 128 ? 3 : 4;
+    static constexpr int kStages = HD == 128 ? 3 : 4;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBufs * kTileBytes;
-    static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-    static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
-    static constexpr int kOffXchg = kOffBar + 512;            // the halves' final maxima and sums
-    static constexpr int kOffItems = kOffXchg + 2 * 2 * 2 * kPrefillRows * 4;
-    static constexpr int kSmem = kOffItems + 256 + 1024;      // + alignment slack
+    static constexpr int kOffKV = kOffQ + kQBufs * kTileBytes;
+    static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+    static constexpr int kOffXchg = kOffBar + 384;            // the halves' final maxima and sums
+    static constexpr int kOffItems = kOffXchg + 2 * 2 * kPrefillRows * 4;
+    static constexpr int kSlack = HD == 128 ? 0 : 1024;       // alignment slack
+    static constexpr int kSmem = kOffItems + 256 + kSlack;
     static constexpr uint32_t kTmemCols = 512;
     // S buffer b at columns 128 b (P and its remainder are written over it);
     // O of key half h at 256 + HD h
@@ -93,11 +112,13 @@ enum SKBar {
     kSKOReady = 12,               // the item's last P V completed
     kSKOFree = 13,                // O_0 and O_1 read out by the epilogue
     kSKXchg = 14,                 // the two threads of a row meet (+ quadrant)
-    kSKKFull = 18, kSKKEmpty = 22, kSKVFull = 26, kSKVEmpty = 30, kSKVFix = 34,   // (+ stage, up to four)
-    kSKItemFull = 38, kSKItemEmpty = 42,
-    kSKNumBars = 46
+    kSKKVFull = 18,               // K and V of ring stage s landed (+ s, up to four)
+    kSKKVEmpty = 22,              // both P V products of stage s's tile completed (+ s)
+    kSKVFix = 26,                 // V rows past the sequence end zeroed in stage s (+ s)
+    kSKItemFull = 30, kSKItemEmpty = 34,
+    kSKNumBars = 38
 };
-static_assert(kSKNumBars * 8 + 16 + 64 <= 512, "barriers, the TMEM address slot and the votes fit 512 bytes");
+static_assert(kSKNumBars * 8 + 16 + 64 <= 384, "barriers, the TMEM address slot and the votes fit 384 bytes");
 
 constexpr int kSKThreads = 384;
 
@@ -118,13 +139,20 @@ __global__ void __launch_bounds__(kSKThreads, 1)
     prefill_sk_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const __nv_bfloat16 *__restrict__ query, const int64_t q_stride, const PrefillParams p) {
     using Cfg = SKCfg<HD>;
-    constexpr int SK = Cfg::kStagesK, SV = Cfg::kStagesV, NQ = Cfg::kQBufs;
-    static_assert(SK <= 4 && SV <= 4 && NQ <= 2, "barriers of the rings and Q buffers");
+    constexpr int R = Cfg::kStages, NQ = Cfg::kQBufs;
+    static_assert(R <= 4 && NQ <= 2, "barriers of the ring and Q buffers");
     constexpr int kPagesPerTile = kPrefillKeys / kBlock;
-    constexpr int kBoxesPerTile = kPagesPerTile * Cfg::kHalves;     // TMA boxes of a K (or V) tile
+    constexpr int kBoxesPerTile = kPagesPerTile * Cfg::kHalves;     // TMA boxes of a K and V tile
+    static_assert(Cfg::kStageBytes == 2 * Cfg::kTileBytes, "a stage holds K and V of a tile");
     static_assert(kBoxesPerTile <= 32, "one box per lane");
     constexpr int kHalfKeys = kPrefillKeys / 2;
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (Cfg::kSlack == 0 && (smem_u32(smem_raw) & 1023u)) {     // uniform over the grid
+        // the kernel would not fit: no work, reported as a failed asynchronous step
+        if (threadIdx.x == 0) set_status(reinterpret_cast<int32_t *>(p.ws), PKV_ERR_DEVICE_TIMEOUT);
+        pdl_wait();
+        return;
+    }
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kSKNumBars);
@@ -133,8 +161,7 @@ __global__ void __launch_bounds__(kSKThreads, 1)
     volatile uint8_t *votes = reinterpret_cast<volatile uint8_t *>(tmem_slot + 4);
     volatile PfItem *items = reinterpret_cast<volatile PfItem *>(smem + Cfg::kOffItems);
     const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
-    const uint32_t sK = smem_u32(smem + Cfg::kOffK);
-    const uint32_t sV = smem_u32(smem + Cfg::kOffV);
+    const uint32_t sKV = smem_u32(smem + Cfg::kOffKV);
 
     // The kernel launched just before this one (the decode kernel, or the
     // shared-prefix pass) may still be running: it writes other rows and other
@@ -254,73 +281,62 @@ __global__ void __launch_bounds__(kSKThreads, 1)
 
             const int end_tile = end_tile_of(it.L);
             const int32_t *bt = p.block_tables + static_cast<int64_t>(it.r) * p.max_blocks_per_seq;
-            // block ids in windows of 32 pages (4 KV tiles), one lane per page; the
-            // next window is loaded a window ahead.  Pages past the sequence are -1
-            // and load as zeros (outside the tensor map).
+            // the pages' coordinates in the tensor map (block id x kv heads + head) in
+            // windows of 32 pages (4 KV tiles), one lane per page; the next window is
+            // loaded a window ahead.  Pages past the sequence, and block ids outside
+            // the cache (reported), get -1 and load as zeros (outside the tensor map).
             auto load_window = [&](int w) -> int {
                 const int page = it.t0 * kPagesPerTile + w * 32 + lane;
                 const int b = page < it.n_pages ? __ldg(bt + page) : -1;
-                if (page < it.n_pages && (b < 0 || b >= p.num_blocks))
-                    set_status(status, PKV_ERR_DEVICE_INDEX);   // loaded as zeros by the bounded TMA, reported
-                return b;
+                if (page >= it.n_pages) return -1;
+                if (b < 0 || b >= p.num_blocks) {
+                    set_status(status, PKV_ERR_DEVICE_INDEX);
+                    return -1;
+                }
+                return b * p.num_kv_heads + it.g;
             };
             int win_cur = load_window(0);
             int win_next = load_window(1);
             for (int j = 0; j < it.n_kv && ok; ++j) {
                 const int gt = gj + j;
-                const int sk = gt % SK, sv = gt % SV;
+                const int st = gt % R;
                 if (j > 0 && (j * kPagesPerTile) % 32 == 0) {
                     win_cur = win_next;
                     win_next = load_window(j * kPagesPerTile / 32 + 1);
                 }
                 const int wofs = (j * kPagesPerTile) % 32;
-                // this lane's box: page lane / kHalves of the tile
-                const int my_blk = __shfl_sync(0xffffffffu, win_cur, wofs + (lane / Cfg::kHalves) % kPagesPerTile);
-                // K of tile gt once S of tile gt - SK has read its stage (two stages:
-                // the S buffer's barrier, committed with that product, tells it)
-                if (gt >= SK) {
-                    uint64_t *freed = SK == 2 ? &bars[kSKSFull + sk] : &bars[kSKKEmpty + sk];
-                    ok = __all_sync(0xffffffffu, pf_wait(freed, ((gt - SK) / SK) & 1, status));
-                }
+                // this lane's box: page lane / kHalves of the tile, columns 64 (lane % kHalves)
+                const int my_pg = __shfl_sync(0xffffffffu, win_cur, wofs + (lane / Cfg::kHalves) % kPagesPerTile);
+                // K and V of tile gt once both P V products of tile gt - R have read the stage
+                if (gt >= R) ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKKVEmpty + st], ((gt - R) / R) & 1, status));
                 if (!ok) break;
-                // one box per lane (page lane / kHalves, 64 columns lane % kHalves): the
-                // boxes are small and the copy engine takes them faster from many
+                // one box per lane: the copy engine takes boxes faster from several
                 // issuing lanes than from one
-                if (lane == 0) mbar_arrive_expect_tx(&bars[kSKKFull + sk], Cfg::kTileBytes);
+                if (lane == 0) mbar_arrive_expect_tx(&bars[kSKKVFull + st], Cfg::kStageBytes);
                 __syncwarp();
                 if (lane < kBoxesPerTile)
-                    tma_load_5d(smem + Cfg::kOffK + sk * Cfg::kTileBytes + (lane % Cfg::kHalves) * (kPrefillKeys * 128) +
-                                    (lane / Cfg::kHalves) * 2048,
-                                &kv_map, &bars[kSKKFull + sk], (lane % Cfg::kHalves) * 64, 0, 0, it.g, my_blk);
-                // V of tile gt once both P V products of tile gt - SV have read its stage
-                if (gt >= SV)
-                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKVEmpty + sv], ((gt - SV) / SV) & 1, status));
-                if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(&bars[kSKVFull + sv], Cfg::kTileBytes);
-                __syncwarp();
-                if (lane < kBoxesPerTile)
-                    tma_load_5d(smem + Cfg::kOffV + sv * Cfg::kTileBytes + (lane % Cfg::kHalves) * (kPrefillKeys * 128) +
-                                    (lane / Cfg::kHalves) * 2048,
-                                &kv_map, &bars[kSKVFull + sv], (lane % Cfg::kHalves) * 64, 0, 1, it.g, my_blk);
+                    tma_load_5d(smem + Cfg::kOffKV + st * Cfg::kStageBytes + (lane % Cfg::kHalves) * Cfg::kHalfBytes +
+                                    (lane / Cfg::kHalves) * Cfg::kBoxBytes,
+                                &kv_map, &bars[kSKKVFull + st], (lane % Cfg::kHalves) * 64, 0, 0, 0, my_pg);
                 if (j == end_tile) {
                     // zero V rows past the sequence end in its last (partial) page;
                     // one fix barrier per stage, so none runs two phases ahead
-                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKVFull + sv], (gt / SV) & 1, status));
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKKVFull + st], (gt / R) & 1, status));
                     if (!ok) break;
                     const int lp = (it.L - 1) / kBlock - j * kPagesPerTile;   // page within the tile
                     const int first = it.L % kBlock;
                     const int nrows = kBlock - first;
                     for (int e = lane; e < Cfg::kHalves * nrows * 8; e += 32) {
-                        const int h = e / (nrows * 8);
+                        const int c = e / (nrows * 8);
                         const int rem = e % (nrows * 8);
-                        const int row = lp * kBlock + first + rem / 8;
-                        const uint32_t a =
-                            sV + sv * Cfg::kTileBytes + h * (kPrefillKeys * 128) + row * 128 + (rem % 8) * 16;
+                        const int t = first + rem / 8;                       // token within the page
+                        const uint32_t a = sKV + st * Cfg::kStageBytes + c * Cfg::kHalfBytes + lp * Cfg::kBoxBytes +
+                                           (t >> 3) * 2048 + 1024 + (t & 7) * 128 + (rem % 8) * 16;
                         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[kSKVFix + sv]);
+                    if (lane == 0) mbar_arrive(&bars[kSKVFix + st]);
                 }
             }
             gj += it.n_kv;
@@ -336,30 +352,30 @@ __global__ void __launch_bounds__(kSKThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillRows, kPrefillKeys, 0, 0);
             constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillRows, HD, 0, 1);
-            // S(gt) = Q K^T into S buffer gt & 1: both operands K-major in shared memory
+            // S(gt) = Q K^T into S buffer gt & 1: both operands K-major in shared
+            // memory, Q's 8-row groups 1 KiB apart, K's 2 KiB apart in the stage
             auto issue_s = [&](int qb, int gt) {
-                const int st = gt % SK;
+                const int st = gt % R;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kPrefillRows * 128) + (kk & 3) * 32;
-                    const uint64_t a = smem_desc_sw128(sQ + qb * Cfg::kTileBytes + off, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(sK + st * Cfg::kTileBytes + off, 16, 1024);
+                    const uint64_t a = smem_desc_sw128(
+                        sQ + qb * Cfg::kTileBytes + (kk >> 2) * (kPrefillRows * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(
+                        sKV + st * Cfg::kStageBytes + (kk >> 2) * Cfg::kHalfBytes + (kk & 3) * 32, 16, 2048);
                     umma_f16_ss(tmem + Cfg::col_s(gt & 1), a, b, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&bars[kSKSFull + (gt & 1)]);
-                // with two K stages, stage gt % 2 is free exactly when S buffer gt & 1
-                // is written, and the producer waits on that barrier instead
-                if constexpr (SK != 2) umma_commit(&bars[kSKKEmpty + st]);
             };
             // O_h (+)= P_h V: A = P of key half h in S buffer gt & 1, keys 64 h + 32 c ..
             // 64 h + 32 c + 31 at columns 64 h + 32 c + [0, 16) (their bf16 remainder at
-            // + [16, 32)); B = rows 64 h .. 64 h + 63 of V (MN-major) in shared memory
+            // + [16, 32)); B = V rows of page 4 h + kk of the stage (MN-major: the two
+            // 8-row groups 2 KiB apart, the column halves kHalfBytes apart)
             auto issue_pv = [&](int h, int gt, uint32_t lo, uint32_t accumulate) {
-                const int st = gt % SV;
+                const int st = gt % R;
 #pragma unroll
                 for (int kk = 0; kk < kHalfKeys / 16; ++kk) {
-                    const uint64_t b = smem_desc_sw128(sV + st * Cfg::kTileBytes + (4 * h + kk) * 2048,
-                                                       kPrefillKeys * 128, 1024);
+                    const uint64_t b = smem_desc_sw128(
+                        sKV + st * Cfg::kStageBytes + (4 * h + kk) * Cfg::kBoxBytes + 1024, Cfg::kHalfBytes, 2048);
                     const uint32_t a = tmem + Cfg::col_s(gt & 1) + 64 * h + (kk >> 1) * 32 + (kk & 1) * 8 + lo;
                     umma_f16_ts(tmem + Cfg::col_o(h), a, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
                 }
@@ -378,51 +394,62 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                 if (!valid) break;
                 const int qb = k % NQ;
                 ok = pf_wait(&bars[kSKQFull + qb], (k / NQ) & 1, status);
-                // the item's first two S products.  S buffer gt & 1 last held P of
-                // tile gt - 2, whose P V products were issued before: the tcgen05.mma
-                // operations of one thread execute in issue order, so they have read
-                // P before S is written
-                for (int j0 = 0; j0 < 2 && j0 < n_kv && ok; ++j0) {
-                    const int gt = gj + j0;
-                    ok = pf_wait(&bars[kSKKFull + gt % SK], (gt / SK) & 1, status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(qb, gt);
-                    if (j0 + 1 == n_kv) umma_commit(&bars[kSKQEmpty + qb]);
-                }
-                for (int j = 0; j < n_kv && ok; ++j) {
-                    const int gt = gj + j;
-                    const int st = gt % SV, sb = gt & 1;
-                    // O_h += P_h V for both halves, issued back to back once both halves'
-                    // P are written (they land within a few hundred cycles of each other),
-                    // V has landed (and been fixed), and O has been read out by the
-                    // previous item's epilogue
-                    ok = pf_wait(&bars[kSKPFull + sb], (gt >> 1) & 1, status);
-                    if (ok) ok = pf_wait(&bars[kSKVFull + st], (gt / SV) & 1, status);
-                    if (ok && j == end_tile) {
-                        ok = pf_wait(&bars[kSKVFix + st], (vfix_par >> st) & 1u, status);
-                        vfix_par ^= 1u << st;
-                    }
-                    if (ok && j == 0 && k > 0) ok = pf_wait(&bars[kSKOFree], (k - 1) & 1, status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t vote = *reinterpret_cast<volatile const uint64_t *>(votes + 8 * sb);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        issue_pv(h, gt, 0, j > 0 ? 1u : 0u);
-                        if ((vote >> (32 * h)) & 0xFFFFFFFFull) issue_pv(h, gt, 16, 1u);
-                    }
-                    umma_commit(&bars[kSKODone]);
-                    umma_commit(&bars[kSKVEmpty + st]);
-                    if (j + 1 == n_kv) umma_commit(&bars[kSKOReady]);
-                    // S of tile gt + 2 into the same S buffer, right behind this tile's
-                    // P V products (issue order, as above)
-                    if (j + 2 < n_kv) {
-                        ok = pf_wait(&bars[kSKKFull + (gt + 2) % SK], ((gt + 2) / SK) & 1, status);
-                        if (!ok) break;
+                // the item's S and P V products in dependency order, each as soon as
+                // it may go: S(j) once its stage has landed and P V(j - 2) has been
+                // issued (S buffer j & 1 last held P of tile j - 2, and the tcgen05.mma
+                // operations of one thread execute in issue order, so that product has
+                // read P before S is written); P V(j) once both halves' P of tile j
+                // are written, V has been fixed (end tile) and, for the item's first
+                // tile, O has been read out by the previous item's epilogue.  S goes
+                // first when both may: the softmax waits on it.
+                int js = 0, jp = 0;
+                uint64_t t_idle = 0;                   // start of the current wait (0: none)
+                while (ok && jp < n_kv) {
+                    const bool s_can = js < n_kv && js <= jp + 1;
+                    const bool p_can = jp < js;
+                    if (s_can && mbar_test_wait(&bars[kSKKVFull + (gj + js) % R], ((gj + js) / R) & 1)) {
                         tc_fence_after();
-                        issue_s(qb, gt + 2);
-                        if (j + 3 == n_kv) umma_commit(&bars[kSKQEmpty + qb]);
+                        issue_s(qb, gj + js);
+                        if (++js == n_kv) umma_commit(&bars[kSKQEmpty + qb]);
+                        t_idle = 0;
+                        continue;
+                    }
+                    if (p_can) {
+                        const int gt = gj + jp;
+                        const int st = gt % R, sb = gt & 1;
+                        bool ready = mbar_test_wait(&bars[kSKPFull + sb], (gt >> 1) & 1);
+                        if (ready && jp == end_tile) ready = mbar_test_wait(&bars[kSKVFix + st], (vfix_par >> st) & 1u);
+                        if (ready && jp == 0 && k > 0) ready = mbar_test_wait(&bars[kSKOFree], (k - 1) & 1);
+                        if (ready) {
+                            if (jp == end_tile) vfix_par ^= 1u << st;
+                            tc_fence_after();
+                            const uint64_t vote = *reinterpret_cast<volatile const uint64_t *>(votes + 8 * sb);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                issue_pv(h, gt, 0, jp > 0 ? 1u : 0u);
+                                if ((vote >> (32 * h)) & 0xFFFFFFFFull) issue_pv(h, gt, 16, 1u);
+                            }
+                            umma_commit(&bars[kSKODone]);
+                            umma_commit(&bars[kSKKVEmpty + st]);
+                            if (++jp == n_kv) umma_commit(&bars[kSKOReady]);
+                            t_idle = 0;
+                            continue;
+                        }
+                    }
+                    // nothing may go yet: sleep on the likelier next event (the
+                    // softmax's P while a P V may go, with a short hint so that a stage
+                    // landing meanwhile is seen soon; else the stage S waits for),
+                    // bounded like every other wait
+                    if (p_can)
+                        mbar_try_wait_for(&bars[kSKPFull + ((gj + jp) & 1)], ((gj + jp) >> 1) & 1, 200);
+                    else
+                        mbar_try_wait(&bars[kSKKVFull + (gj + js) % R], ((gj + js) / R) & 1);
+                    const uint64_t now = global_ns();
+                    if (t_idle == 0) {
+                        t_idle = now;
+                    } else if (now - t_idle > kWaitLimitNs) {
+                        set_status(status, PKV_ERR_DEVICE_TIMEOUT);
+                        ok = false;
                     }
                 }
                 gj += n_kv;
@@ -484,10 +511,10 @@ __global__ void __launch_bounds__(kSKThreads, 1)
         const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const uint32_t tOh = trow + Cfg::col_o(h);
         const float sl2 = p.scale_log2;
-        // the halves' final maxima and sums, [item parity][half][row] (a half may
-        // reach the next item's end before the other has read this item's values)
+        // the halves' final maxima and sums, [half][row]; written once every
+        // softmax warp has read the previous item's (its arrival on O-free)
         float *xm = reinterpret_cast<float *>(smem + Cfg::kOffXchg);
-        float *xl = xm + 2 * 2 * kPrefillRows;
+        float *xl = xm + 2 * kPrefillRows;
         uint64_t *xbar = &bars[kSKXchg + quad];
         bool ok = true;
         int gj = 0;                                     // KV tiles of this CTA so far
@@ -530,17 +557,19 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                 // some row's limit)
                 const int key0 = kbase + j * kPrefillKeys;
                 const bool masked = __any_sync(0xffffffffu, key0 + kHalfKeys > lim);
-                // pass 1: max of this half's 64 scores (four chains of three-input maxima)
+                // this half's 64 scores, read once (the tensor-memory instructions of
+                // the softmax warps delay the MMA thread's on the same sub-partition)
+                float s[kHalfKeys];
+                tmem_ld32f(tS, s);
+                tmem_ld32f(tS + 32, s + 32);
+                tmem_ld_wait();
+                if (masked) {
+#pragma unroll
+                    for (int c = 0; c < kHalfKeys; ++c) s[c] = (key0 + c < lim) ? s[c] : NEG_INF;
+                }
+                // pass 1: their max (four chains of three-input maxima)
                 float mx;
                 {
-                    float s[kHalfKeys];
-                    tmem_ld32f(tS, s);
-                    tmem_ld32f(tS + 32, s + 32);
-                    tmem_ld_wait();
-                    if (masked) {
-#pragma unroll
-                        for (int c = 0; c < kHalfKeys; ++c) s[c] = (key0 + c < lim) ? s[c] : NEG_INF;
-                    }
                     float mx4[4] = {fmaxf(s[0], s[1]), fmaxf(s[2], s[3]), fmaxf(s[4], s[5]), fmaxf(s[6], s[7])};
 #pragma unroll
                     for (int c = 8; c < kHalfKeys; c += 8) {
@@ -559,11 +588,36 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                 const bool grow = !first && m_new > m_ref + 8.f;
                 const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
                 if (first || grow) m_ref = m_new;
+                // pass 2, one 32-key piece at a time: weights p = 2^(s scale - ref)
+                // with their sum and sum of squares; P as bf16 pairs and its bf16
+                // remainder written over the piece's own 32 columns (32 c + [0, 16)
+                // and 32 c + [16, 32) of this half) in one store.  The remainder
+                // enters P V only when some warp of this half votes for it.
+                const float ref = m_ref == NEG_INF ? 0.f : m_ref;
+                const uint64_t sc2 = f2_pack(sl2, sl2), nref2 = f2_pack(-ref, -ref);
+                uint64_t ps2[2] = {0, 0}, pq2[2] = {0, 0};
+#pragma unroll
+                for (int c = 0; c < kHalfKeys / 32; ++c) {
+                    uint32_t wr[32];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint64_t y2 = f2_fma(f2_pack(s[32 * c + 2 * e], s[32 * c + 2 * e + 1]), sc2, nref2);
+                        float y0, y1;
+                        f2_unpack(y2, y0, y1);
+                        const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+                        const uint64_t p2 = f2_pack(p0, p1);
+                        ps2[e & 1] = f2_add(ps2[e & 1], p2);
+                        pq2[e & 1] = f2_fma(p2, p2, pq2[e & 1]);
+                        split_bf16x2(p0, p1, wr[e], wr[16 + e]);
+                    }
+                    tmem_st32(tS + 32 * c, wr);
+                }
                 if (__any_sync(0xffffffffu, grow)) {
-                    // rare: O_h rescaled, once O_h += P_h V of the previous tile has
-                    // completed (grow needs an earlier tile of this item, so gt >= 1;
-                    // that product's barrier cannot be two phases behind: S of this tile
-                    // was committed after the products of tile gt - 2)
+                    // rare: O_h rescaled before this tile's P V is issued, once O_h +=
+                    // P_h V of the previous tile has completed (grow needs an earlier
+                    // tile of this item, so gt >= 1; that product's barrier cannot be
+                    // two phases behind: S of this tile was committed after the
+                    // products of tile gt - 2)
                     ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKODone], (gt - 1) & 1, status));
                     if (!ok) break;
                     tc_fence_after();
@@ -576,39 +630,6 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
                         tmem_st32(tOh + c * 32, v);
                     }
-                }
-                // pass 2, one 32-key piece at a time (a short loop body): weights
-                // p = 2^(s scale - ref) with their sum and sum of squares; P as bf16
-                // pairs and its bf16 remainder written over the piece's own 32 columns
-                // (32 c + [0, 16) and 32 c + [16, 32) of this half), which this pass has
-                // just read.  The remainder enters P V only when some warp of this
-                // half votes for it.
-                const float ref = m_ref == NEG_INF ? 0.f : m_ref;
-                const uint64_t sc2 = f2_pack(sl2, sl2), nref2 = f2_pack(-ref, -ref);
-                uint64_t ps2[2] = {0, 0}, pq2[2] = {0, 0};
-#pragma unroll 1
-                for (int c = 0; c < kHalfKeys / 32; ++c) {
-                    float v[32];
-                    tmem_ld32f(tS + c * 32, v);
-                    tmem_ld_wait();
-                    if (masked) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = (key0 + 32 * c + e < lim) ? v[e] : NEG_INF;
-                    }
-                    uint32_t w[16], r[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const uint64_t y2 = f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), sc2, nref2);
-                        float y0, y1;
-                        f2_unpack(y2, y0, y1);
-                        const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
-                        const uint64_t p2 = f2_pack(p0, p1);
-                        ps2[e & 1] = f2_add(ps2[e & 1], p2);
-                        pq2[e & 1] = f2_fma(p2, p2, pq2[e & 1]);
-                        split_bf16x2(p0, p1, w[e], r[e]);
-                    }
-                    tmem_st16(tS + 32 * c, w);
-                    tmem_st16(tS + 32 * c + 16, r);
                 }
                 float a0, a1, b0, b1;
                 f2_unpack(f2_add(ps2[0], ps2[1]), a0, a1);
@@ -628,18 +649,18 @@ __global__ void __launch_bounds__(kSKThreads, 1)
             gj += n_kv;
             // epilogue: the two halves' states merged by log-sum-exp; this thread
             // writes output dims 64 h .. 64 h + 63 of its row
-            const int xo = (k & 1) * 2 * kPrefillRows;
+            if (ok && k > 0) ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKOFree], (k - 1) & 1, status));
             if (ok) {
-                xm[xo + h * kPrefillRows + row] = m_ref;
-                xl[xo + h * kPrefillRows + row] = l;
+                xm[h * kPrefillRows + row] = m_ref;
+                xl[h * kPrefillRows + row] = l;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xbar);
                 ok = __all_sync(0xffffffffu, pf_wait(xbar, k & 1, status));
             }
             if (ok) ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKOReady], k & 1, status));
             if (ok) {
-                const float m0 = xm[xo + row], m1 = xm[xo + kPrefillRows + row];
-                const float l0 = xl[xo + row], l1 = xl[xo + kPrefillRows + row];
+                const float m0 = xm[row], m1 = xm[kPrefillRows + row];
+                const float l0 = xl[row], l1 = xl[kPrefillRows + row];
                 const float M = fmaxf(m0, m1);
                 // a half that saw no key has m = -inf and weight 0 (and O_h = 0)
                 const float w0 = M == NEG_INF ? 0.f : fast_exp2(m0 - M);
@@ -761,12 +782,36 @@ static int make_query_map(CUtensorMap *qm, const void *query, int64_t q_stride, 
     return PKV_OK;
 }
 
+// Tensor map of the cache as {head_size, 8 tokens, K/V, 2 token halves, pages
+// of every kv head (block id x kv heads + head)}: a box {64, 8, 2, 2, 1} is
+// the K and V rows of one page, 64 columns, landing as [token half][K, V]
+// [token % 8][64 columns] with 128-byte swizzle (4 KiB).
+static int make_kv_tile_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
+                            int32_t head_size) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PKV_ERR_CUDA;
+    const cuuint64_t row = static_cast<cuuint64_t>(head_size) * 2;
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), 8, 2, 2,
+                                static_cast<cuuint64_t>(num_blocks) * static_cast<cuuint64_t>(num_kv_heads)};
+    const cuuint64_t strides[4] = {row, row * kBlock, row * 8, row * kBlock * 2};
+    const cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (enc(kvm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
 int launch_prefill_sk(const PrefillParams &p, const void *query, int64_t q_stride, int32_t num_tokens,
                       const void *kv_cache, int64_t num_blocks, int32_t head_size, bool cascade, int64_t grid, int dev,
                       cudaStream_t stream) {
     if (grid <= 0) return PKV_OK;
+    // the kernel forms a page's coordinate block id x kv heads + head in 32 bits
+    // (a cache of 2^31 page-heads is terabytes, past any device's memory)
+    if (num_blocks * static_cast<int64_t>(p.num_kv_heads) > INT32_MAX) return PKV_ERR_SHAPE;
     CUtensorMap kvm, qm;
-    int rc = make_page_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
+    int rc = make_kv_tile_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
     if (rc) return rc;
     if (cascade) {
         qm = kvm;                                  // not read: the pass gathers its query rows itself

@@ -831,25 +831,6 @@ int launch_prefill_e4m3(const PrefillParams &p, const void *query, int64_t q_str
                            : launch_prefill_hd<128, false>(p, kvm, query, q_stride, grid, dev, stream);
 }
 
-// Tensor map of the cache as {head_size, 16, 2, kv heads, blocks}; a box is
-// the K (or V) rows of one page, 64 columns, 128-byte swizzle.
-int make_page_map(CUtensorMap *kvm, const void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
-                  int32_t head_size) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return PKV_ERR_CUDA;
-    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(head_size), kBlock, 2, static_cast<cuuint64_t>(num_kv_heads),
-                                static_cast<cuuint64_t>(num_blocks)};
-    const cuuint64_t row = static_cast<cuuint64_t>(head_size) * 2;
-    const cuuint64_t strides[4] = {row, row * kBlock, row * kBlock * 2, row * kBlock * 2 * num_kv_heads};
-    const cuuint32_t box[5] = {64, kBlock, 1, 1, 1};
-    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    if (enc(kvm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(kv_cache), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return PKV_ERR_CUDA;
-    return PKV_OK;
-}
-
 // Tensor map of an E4M3 cache as bytes {head_size, 16, 2, kv heads, blocks};
 // a box is the K (or V) rows of one page, unswizzled (the converter warps
 // widen them).
