@@ -35,14 +35,13 @@
 // both products read in place (K's rows at one stride for S, each page's V
 // rows for P V).
 // Warp roles (384 threads): warp 0 claims items and loads Q (TMA, for a
-// chunk) and the tiles' pages through the block table (TMA); warp 1 issues
-// the MMAs, each as soon as its operands are ready (an S product while the
-// previous tile's P is still being written, a P V product while the next
-// stage is still loading); warp 2 owns the tensor-memory allocation; for the
-// shared-prefix pass, whose rows come from many requests, warps 2 and 3
-// gather Q rows with asynchronous copies instead; warps 4-7 take keys 0-63 of
-// every tile, warps 8-11 keys 64-127 (warp w reads the tensor-memory lanes of
-// quadrant w % 4).
+// chunk) and the tiles' pages through the block table (TMA); warps 1 and 2
+// issue the MMAs of key halves 0 and 1 (each its half's S and P V), each
+// product as soon as its operands are ready; warp 2 also owns the
+// tensor-memory allocation; for the shared-prefix pass, whose rows come from
+// many requests, warp 3 gathers Q rows with asynchronous copies instead;
+// warps 4-7 take keys 0-63 of every tile, warps 8-11 keys 64-127 (warp w
+// reads the tensor-memory lanes of quadrant w % 4).
 //
 // When any row of a warp puts a large share of its weight on few keys of a
 // tile (rows with few visible keys, or a peaked softmax), P's bf16 remainder
@@ -51,14 +50,14 @@
 // P V, so NaN in unwritten cache slots never meets a zero weight.  Every wait
 // is bounded.
 //
-// What bounds it: the MMA thread's issue.  A tile takes 16 products of
-// 128 x 128 x 16 (8 for S, 8 for P V), about 1,000 cycles of tensor pipe, but
-// the issuing thread shares its sub-partition's scheduler with the two
-// softmax warps of tensor-memory lane quadrant 1 (a warp reads only its
-// quadrant's lanes, and the quadrant is the sub-partition), and their
-// tensor-memory loads and stores and exponentials slow each issue from about
-// 90 to 130-240 cycles.  The softmax reads S once and stores P and its
-// remainder in one instruction per 32 keys for that reason.
+// What bounds it: the MMA threads' issue.  A tile takes 24 products (per key
+// half 8 of 128 x 64 x 16 for S and 4 of 128 x 128 x 16 for P V), about 1,300
+// cycles of tensor pipe, but an issuing thread shares its sub-partition's
+// scheduler with two softmax warps (a warp reads only its tensor-memory lane
+// quadrant, and the quadrant is the sub-partition), and their tensor-memory
+// loads and stores and exponentials slow each issue from about 90 to
+// 130-240 cycles.  Hence two issuing threads, and a softmax that reads S
+// once and stores P with its remainder in one instruction per 32 keys.
 #include <mutex>
 
 #include "prefill_common.cuh"
@@ -92,7 +91,7 @@ struct SKCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBufs * kTileBytes;
     static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-    static constexpr int kOffXchg = kOffBar + 384;            // the halves' final maxima and sums
+    static constexpr int kOffXchg = kOffBar + 448;            // the halves' final maxima and sums
     static constexpr int kOffItems = kOffXchg + 2 * 2 * kPrefillRows * 4;
     static constexpr int kSlack = HD == 128 ? 0 : 1024;       // alignment slack
     static constexpr int kSmem = kOffItems + 256 + kSlack;
@@ -105,20 +104,20 @@ struct SKCfg {
 
 enum SKBar {
     kSKQFull = 0,                 // Q buffer b loaded (+ b, up to two buffers)
-    kSKQEmpty = 2,                // the item's last S has read Q buffer b
-    kSKSFull = 4,                 // S buffer b written
-    kSKPFull = 6,                 // P of S buffer b written, both key halves (+ b)
-    kSKODone = 10,                // O_0 += P_0 V and O_1 += P_1 V completed
-    kSKOReady = 12,               // the item's last P V completed
-    kSKOFree = 13,                // O_0 and O_1 read out by the epilogue
-    kSKXchg = 14,                 // the two threads of a row meet (+ quadrant)
-    kSKKVFull = 18,               // K and V of ring stage s landed (+ s, up to four)
-    kSKKVEmpty = 22,              // both P V products of stage s's tile completed (+ s)
-    kSKVFix = 26,                 // V rows past the sequence end zeroed in stage s (+ s)
-    kSKItemFull = 30, kSKItemEmpty = 34,
-    kSKNumBars = 38
+    kSKQEmpty = 2,                // both MMA threads' last S of the item have read Q buffer b (+ b)
+    kSKSFull = 4,                 // key half h of S buffer b written (+ 2 b + h)
+    kSKPFull = 8,                 // P of key half h in S buffer b written (+ 2 b + h)
+    kSKODone = 12,                // O_h += P_h V completed (+ h)
+    kSKOReady = 14,               // the item's last O_h += P_h V completed (+ h)
+    kSKOFree = 16,                // O_0 and O_1 read out by the epilogue
+    kSKXchg = 17,                 // the two threads of a row meet (+ quadrant)
+    kSKKVFull = 21,               // K and V of ring stage s landed (+ s, up to four)
+    kSKKVEmpty = 25,              // both key halves' P V products of stage s's tile completed (+ s)
+    kSKVFix = 29,                 // V rows past the sequence end zeroed in stage s (+ s)
+    kSKItemFull = 33, kSKItemEmpty = 37,
+    kSKNumBars = 41
 };
-static_assert(kSKNumBars * 8 + 16 + 64 <= 384, "barriers, the TMEM address slot and the votes fit 384 bytes");
+static_assert(kSKNumBars * 8 + 16 + 64 <= 448, "barriers, the TMEM address slot and the votes fit 448 bytes");
 
 constexpr int kSKThreads = 384;
 
@@ -157,7 +156,7 @@ __global__ void __launch_bounds__(kSKThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kSKNumBars);
     // the softmax warps' votes for the remainder of P, one byte each,
-    // [S buffer][key half][quadrant]: the MMA issuer reads a buffer's eight at once
+    // [S buffer][key half][quadrant]: an MMA thread reads its half's four at once
     volatile uint8_t *votes = reinterpret_cast<volatile uint8_t *>(tmem_slot + 4);
     volatile PfItem *items = reinterpret_cast<volatile PfItem *>(smem + Cfg::kOffItems);
     const uint32_t sQ = smem_u32(smem + Cfg::kOffQ);
@@ -185,12 +184,13 @@ __global__ void __launch_bounds__(kSKThreads, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < kSKNumBars; ++b) {
             int count = 1;
-            if (b >= kSKPFull && b < kSKPFull + 2) count = 8;            // every softmax warp
-            else if (b == kSKOFree) count = 8;
+            if (b >= kSKPFull && b < kSKPFull + 4) count = 4;            // the key half's softmax warps
+            else if (b == kSKOFree) count = 8;                            // every softmax warp
             else if (b >= kSKXchg && b < kSKXchg + 4) count = 2;         // the two warps of a quadrant
-            else if (CASCADE && b >= kSKQFull && b < kSKQFull + 2) count = 2;   // the two Q gatherers
+            else if (b >= kSKQEmpty && b < kSKQEmpty + 2) count = 2;     // both MMA threads
+            else if (b >= kSKKVEmpty && b < kSKKVEmpty + 4) count = 2;   // both MMA threads
             else if (b >= kSKItemEmpty && b < kSKItemEmpty + kItemSlots)
-                count = CASCADE ? 11 : 9;              // MMA, 8 softmax warps (+ 2 Q gatherers)
+                count = CASCADE ? 11 : 10;             // 2 MMA threads, 8 softmax warps (+ the Q gatherer)
             mbar_init(&bars[b], count);
         }
         tma_prefetch_desc(&kv_map);
@@ -347,37 +347,47 @@ __global__ void __launch_bounds__(kSKThreads, 1)
         // this CTA's share of the schedule
         if (lane == 0)
             reinterpret_cast<int32_t *>(p.ws + kStatsOffset)[(CASCADE ? kStatsCtas : 0) + blockIdx.x] = taken;
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA issuers: warp 1 key half 0, warp 2 key half 1 ----------------
+        // Each thread issues its key half's S (N = 64, into its half of the S
+        // buffer) and P V (into its O_h): the softmax warps of a sub-partition
+        // slow the issue of an MMA thread beside them, and two threads on two
+        // sub-partitions issue twice as many products at once.  A thread owns
+        // its S columns and its O_h, so issue order within the thread covers
+        // every hazard between its products.
+        const int hh = warp - 1;
         if (lane == 0) {
-            constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillRows, kPrefillKeys, 0, 0);
+            constexpr uint32_t kIdescS = idesc_bf16_f32(kPrefillRows, kHalfKeys, 0, 0);
             constexpr uint32_t kIdescO = idesc_bf16_f32(kPrefillRows, HD, 0, 1);
-            // S(gt) = Q K^T into S buffer gt & 1: both operands K-major in shared
-            // memory, Q's 8-row groups 1 KiB apart, K's 2 KiB apart in the stage
+            // S_h(gt) = Q K_h^T into columns 64 hh of S buffer gt & 1: both operands
+            // K-major in shared memory, Q's 8-row groups 1 KiB apart, K's 2 KiB apart
+            // in the stage (keys 64 hh .. 64 hh + 63: pages 4 hh .. 4 hh + 3)
             auto issue_s = [&](int qb, int gt) {
                 const int st = gt % R;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint64_t a = smem_desc_sw128(
                         sQ + qb * Cfg::kTileBytes + (kk >> 2) * (kPrefillRows * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(
-                        sKV + st * Cfg::kStageBytes + (kk >> 2) * Cfg::kHalfBytes + (kk & 3) * 32, 16, 2048);
-                    umma_f16_ss(tmem + Cfg::col_s(gt & 1), a, b, kIdescS, kk > 0 ? 1u : 0u);
+                    const uint64_t b = smem_desc_sw128(sKV + st * Cfg::kStageBytes + (kk >> 2) * Cfg::kHalfBytes +
+                                                           hh * (kHalfKeys / kBlock) * Cfg::kBoxBytes + (kk & 3) * 32,
+                                                       16, 2048);
+                    umma_f16_ss(tmem + Cfg::col_s(gt & 1) + hh * kHalfKeys, a, b, kIdescS, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(&bars[kSKSFull + (gt & 1)]);
+                umma_commit(&bars[kSKSFull + 2 * (gt & 1) + hh]);
             };
-            // O_h (+)= P_h V: A = P of key half h in S buffer gt & 1, keys 64 h + 32 c ..
-            // 64 h + 32 c + 31 at columns 64 h + 32 c + [0, 16) (their bf16 remainder at
-            // + [16, 32)); B = V rows of page 4 h + kk of the stage (MN-major: the two
-            // 8-row groups 2 KiB apart, the column halves kHalfBytes apart)
-            auto issue_pv = [&](int h, int gt, uint32_t lo, uint32_t accumulate) {
+            // O_hh (+)= P_hh V: A = P of key half hh in S buffer gt & 1, keys 64 hh +
+            // 32 c .. 64 hh + 32 c + 31 at columns 64 hh + 32 c + [0, 16) (their bf16
+            // remainder at + [16, 32)); B = V rows of page 4 hh + kk of the stage
+            // (MN-major: the two 8-row groups 2 KiB apart, the column halves
+            // kHalfBytes apart)
+            auto issue_pv = [&](int gt, uint32_t lo, uint32_t accumulate) {
                 const int st = gt % R;
 #pragma unroll
                 for (int kk = 0; kk < kHalfKeys / 16; ++kk) {
                     const uint64_t b = smem_desc_sw128(
-                        sKV + st * Cfg::kStageBytes + (4 * h + kk) * Cfg::kBoxBytes + 1024, Cfg::kHalfBytes, 2048);
-                    const uint32_t a = tmem + Cfg::col_s(gt & 1) + 64 * h + (kk >> 1) * 32 + (kk & 1) * 8 + lo;
-                    umma_f16_ts(tmem + Cfg::col_o(h), a, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+                        sKV + st * Cfg::kStageBytes + (4 * hh + kk) * Cfg::kBoxBytes + 1024, Cfg::kHalfBytes, 2048);
+                    const uint32_t a = tmem + Cfg::col_s(gt & 1) + 64 * hh + (kk >> 1) * 32 + (kk & 1) * 8 + lo;
+                    umma_f16_ts(tmem + Cfg::col_o(hh), a, b, kIdescO, (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
             bool ok = true;
@@ -398,10 +408,10 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                 // it may go: S(j) once its stage has landed and P V(j - 2) has been
                 // issued (S buffer j & 1 last held P of tile j - 2, and the tcgen05.mma
                 // operations of one thread execute in issue order, so that product has
-                // read P before S is written); P V(j) once both halves' P of tile j
-                // are written, V has been fixed (end tile) and, for the item's first
-                // tile, O has been read out by the previous item's epilogue.  S goes
-                // first when both may: the softmax waits on it.
+                // read P before S is written); P V(j) once this half's P of tile j is
+                // written, V has been fixed (end tile) and, for the item's first tile,
+                // O has been read out by the previous item's epilogue.  S goes first
+                // when both may: the softmax waits on it.
                 int js = 0, jp = 0;
                 uint64_t t_idle = 0;                   // start of the current wait (0: none)
                 while (ok && jp < n_kv) {
@@ -417,21 +427,18 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                     if (p_can) {
                         const int gt = gj + jp;
                         const int st = gt % R, sb = gt & 1;
-                        bool ready = mbar_test_wait(&bars[kSKPFull + sb], (gt >> 1) & 1);
+                        bool ready = mbar_test_wait(&bars[kSKPFull + 2 * sb + hh], (gt >> 1) & 1);
                         if (ready && jp == end_tile) ready = mbar_test_wait(&bars[kSKVFix + st], (vfix_par >> st) & 1u);
                         if (ready && jp == 0 && k > 0) ready = mbar_test_wait(&bars[kSKOFree], (k - 1) & 1);
                         if (ready) {
                             if (jp == end_tile) vfix_par ^= 1u << st;
                             tc_fence_after();
-                            const uint64_t vote = *reinterpret_cast<volatile const uint64_t *>(votes + 8 * sb);
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                issue_pv(h, gt, 0, jp > 0 ? 1u : 0u);
-                                if ((vote >> (32 * h)) & 0xFFFFFFFFull) issue_pv(h, gt, 16, 1u);
-                            }
-                            umma_commit(&bars[kSKODone]);
+                            const uint32_t vote = *reinterpret_cast<volatile const uint32_t *>(votes + 8 * sb + 4 * hh);
+                            issue_pv(gt, 0, jp > 0 ? 1u : 0u);
+                            if (vote) issue_pv(gt, 16, 1u);
+                            umma_commit(&bars[kSKODone + hh]);
                             umma_commit(&bars[kSKKVEmpty + st]);
-                            if (++jp == n_kv) umma_commit(&bars[kSKOReady]);
+                            if (++jp == n_kv) umma_commit(&bars[kSKOReady + hh]);
                             t_idle = 0;
                             continue;
                         }
@@ -441,7 +448,7 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                     // landing meanwhile is seen soon; else the stage S waits for),
                     // bounded like every other wait
                     if (p_can)
-                        mbar_try_wait_for(&bars[kSKPFull + ((gj + jp) & 1)], ((gj + jp) >> 1) & 1, 200);
+                        mbar_try_wait_for(&bars[kSKPFull + 2 * ((gj + jp) & 1) + hh], ((gj + jp) >> 1) & 1, 200);
                     else
                         mbar_try_wait(&bars[kSKKVFull + (gj + js) % R], ((gj + js) / R) & 1);
                     const uint64_t now = global_ns();
@@ -456,8 +463,8 @@ __global__ void __launch_bounds__(kSKThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 2 || warp == 3) {
-        // ---------------- shared-prefix pass: Q gatherers, two rows per thread ----------------
+    } else if (warp == 3) {
+        // ---------------- shared-prefix pass: Q gatherer, four rows per thread ----------------
         if constexpr (CASCADE) {
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -469,20 +476,26 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[kSKItemEmpty + slot]);
                 if (!valid) break;
+                // rows {token, request, query index, q head in group}, all four of this
+                // lane's looked up at once, before the wait for the buffer; zeros past
+                // the rows
+                const int4 *crows = reinterpret_cast<const int4 *>(p.ws + ws_ld(&hdr->off_crows));
+                int4 crow4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = row0 + i * 32 + lane;
+                    crow4[i] = rr < rows_total ? ws_ld(crows + rr) : make_int4(0, 0, 0, 0);
+                }
                 // Q buffer k % NQ, once the item NQ back has read it
                 const int qb = k % NQ;
                 if (k >= NQ) ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKQEmpty + qb], (k / NQ - 1) & 1, status));
                 if (!ok) break;
                 const uint32_t qbase = sQ + qb * Cfg::kTileBytes;
-                // rows {token, request, query index, q head in group}; zeros past the rows
-                const int4 *crows = reinterpret_cast<const int4 *>(p.ws + ws_ld(&hdr->off_crows));
-#pragma unroll 1
-                for (int i = 0; i < 2; ++i) {
-                    const int r = (warp - 2) * 64 + i * 32 + lane;   // row within the tile
-                    const int rr = row0 + r;
-                    const bool vrow = rr < rows_total;
-                    int4 crow = make_int4(0, 0, 0, 0);
-                    if (vrow) crow = ws_ld(crows + rr);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = i * 32 + lane;                     // row within the tile
+                    const bool vrow = row0 + r < rows_total;
+                    const int4 crow = crow4[i];
                     const __nv_bfloat16 *src =
                         query + static_cast<int64_t>(crow.x) * q_stride + static_cast<int64_t>(g * G + crow.w) * HD;
 #pragma unroll
@@ -549,7 +562,7 @@ __global__ void __launch_bounds__(kSKThreads, 1)
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int gt = gj + j;
                 const int sb = gt & 1;
-                ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKSFull + sb], (gt >> 1) & 1, status));
+                ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKSFull + 2 * sb + h], (gt >> 1) & 1, status));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tS = trow + Cfg::col_s(sb) + h * kHalfKeys;
@@ -618,7 +631,7 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                     // tile of this item, so gt >= 1; that product's barrier cannot be
                     // two phases behind: S of this tile was committed after the
                     // products of tile gt - 2)
-                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKODone], (gt - 1) & 1, status));
+                    ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKODone + h], (gt - 1) & 1, status));
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll 1
@@ -644,7 +657,7 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                 if (lane == 0) votes[8 * sb + 4 * h + quad] = wneed ? 1 : 0;
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kSKPFull + sb]);
+                if (lane == 0) mbar_arrive(&bars[kSKPFull + 2 * sb + h]);
             }
             gj += n_kv;
             // epilogue: the two halves' states merged by log-sum-exp; this thread
@@ -658,6 +671,7 @@ __global__ void __launch_bounds__(kSKThreads, 1)
                 ok = __all_sync(0xffffffffu, pf_wait(xbar, k & 1, status));
             }
             if (ok) ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKOReady], k & 1, status));
+            if (ok) ok = __all_sync(0xffffffffu, pf_wait(&bars[kSKOReady + 1], k & 1, status));
             if (ok) {
                 const float m0 = xm[row], m1 = xm[kPrefillRows + row];
                 const float l0 = xl[row], l1 = xl[kPrefillRows + row];
