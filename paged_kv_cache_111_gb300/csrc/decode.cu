@@ -313,6 +313,117 @@ __device__ int decode_self_plan(const AttnParams &p, int *scr, SelfPlanShared &s
     return n_items;
 }
 
+// The same plan made by one warp alone, in registers, for a batch of at most
+// 32 x kWarpPlanPer requests: lane l holds requests [l per, (l + 1) per), the
+// page total and the bases come from warp shuffles, and the owner of each of
+// the warp's chunks is found by a ballot over the lanes' chunk ranges.  No
+// block barrier and no shared memory: a chunk CTA's warps go from the
+// metadata read to their first page loads on their own.  Decisions and
+// bases are those of decode_self_plan (the grid's last CTA still makes that
+// one, for the header and the split tokens).
+constexpr int kWarpPlanPer = 2;
+
+__device__ int decode_warp_plan(const AttnParams &p, SelfChunk (&mine)[2], int W, int wid) {
+    const int S = p.num_seqs, lane = threadIdx.x & 31;
+    const int per = div_up(S, 32);
+    const int r0 = min(S, lane * per), r1 = min(S, r0 + per);
+    int q0a[kWarpPlanPer], qa[kWarpPlanPer], La[kWarpPlanPer];
+#pragma unroll
+    for (int i = 0; i < kWarpPlanPer; ++i) {
+        const int r = r0 + i;
+        const bool in = i < per && r < r1;
+        q0a[i] = in ? __ldg(p.qsl + r) : 0;
+        qa[i] = in ? __ldg(p.qsl + r + 1) : 0;       // q1 for now
+        La[i] = in ? __ldg(p.seq_lens + r) : 0;
+    }
+    // total key pages of the valid requests (the automatic split size)
+    unsigned long long pages = 0;
+    bool valid[kWarpPlanPer];
+#pragma unroll
+    for (int i = 0; i < kWarpPlanPer; ++i) {
+        const bool in = i < per && r0 + i < r1;
+        valid[i] = in && request_valid(q0a[i], qa[i], La[i], p.num_tokens, p.max_seq_len, p.max_query_len,
+                                       p.max_blocks_per_seq);
+        qa[i] -= q0a[i];                                 // query tokens
+        if (valid[i] && qa[i] > 0) pages += static_cast<unsigned long long>(div_up(La[i], kBlock));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) pages += __shfl_xor_sync(0xffffffffu, pages, o);
+    const int pps = auto_pages_per_split(pages, p.num_kv_heads, p.total_warps);
+    // per request: chunks, pages per split, page span; per lane: chunks,
+    // partial rows, split tokens
+    int na[kWarpPlanPer], psa[kWarpPlanPer], spa[kWarpPlanPer];
+    int4 cnt = make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < kWarpPlanPer; ++i) {
+        int n = 0, ps = 0, span = 0;
+        if (valid[i] && qa[i] > 0) {
+            span = div_up(La[i], kBlock);
+            const int2 sg = split_geometry(span, pps, 0, kMaxSplits);
+            ps = sg.x;
+            n = sg.y;
+        }
+        na[i] = n;
+        psa[i] = ps;
+        spa[i] = span;
+        cnt.x += n;
+        if (n > 1) {
+            cnt.y += qa[i] * p.num_q_heads * n;
+            cnt.z += qa[i];
+        }
+    }
+    int4 inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, inc.x, o), b = __shfl_up_sync(0xffffffffu, inc.y, o);
+        const int c = __shfl_up_sync(0xffffffffu, inc.z, o);
+        if (lane >= o) {
+            inc.x += a;
+            inc.y += b;
+            inc.z += c;
+        }
+    }
+    const int tot_x = __shfl_sync(0xffffffffu, inc.x, 31), tot_y = __shfl_sync(0xffffffffu, inc.y, 31);
+    const int tot_z = __shfl_sync(0xffffffffu, inc.z, 31);
+    const bool fits = tot_x <= p.lay.max_chunks && tot_y <= p.lay.max_prow && tot_z <= p.num_tokens;
+    const int n_items = fits ? tot_x * p.num_kv_heads : 0;
+    const int cb0 = inc.x - cnt.x, pb0 = inc.y - cnt.y;      // this lane's first chunk and partial row
+#pragma unroll
+    for (int round = 0; round < 2; ++round) {
+        const int item = round ? 2 * W - 1 - wid : wid;
+        SelfChunk c{-1, 0, 0, 0, 1, 0};
+        if (wid < W && item < n_items) {                     // uniform over the warp
+            const int ch = item / p.num_kv_heads;
+            const unsigned owners = __ballot_sync(0xffffffffu, cb0 <= ch && ch < cb0 + cnt.x);
+            const int owner = __ffs(owners) - 1;
+            int cb = cb0, pb = pb0;
+            bool done = false;
+#pragma unroll
+            for (int i = 0; i < kWarpPlanPer; ++i) {
+                if (!done && ch < cb + na[i]) {
+                    done = true;
+                    c.r = r0 + i;
+                    c.k = ch - cb;
+                    c.pb = c.k * psa[i];
+                    c.npages = min(spa[i], c.pb + psa[i]) - c.pb;
+                    c.n_split = na[i] > 1 ? na[i] : 1;
+                    c.pbase = na[i] > 1 ? pb : 0;
+                }
+                cb += na[i];
+                if (na[i] > 1) pb += qa[i] * p.num_q_heads * na[i];
+            }
+            c.r = __shfl_sync(0xffffffffu, c.r, owner);
+            c.k = __shfl_sync(0xffffffffu, c.k, owner);
+            c.pb = __shfl_sync(0xffffffffu, c.pb, owner);
+            c.npages = __shfl_sync(0xffffffffu, c.npages, owner);
+            c.n_split = __shfl_sync(0xffffffffu, c.n_split, owner);
+            c.pbase = __shfl_sync(0xffffffffu, c.pbase, owner);
+        }
+        mine[round] = c;
+    }
+    return n_items;
+}
+
 // The last CTA of a self-planned call: the header, status and split tokens
 // the plan kernel would have written (after every earlier kernel on the
 // stream is complete), then the header's epoch is bumped.  (The request table
@@ -405,7 +516,14 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
     SelfChunk self_chunks[2];
     int n_items = 0;
     if (p.self_plan) {
-        n_items = decode_self_plan<NW>(p, reinterpret_cast<int *>(smem), sp_shared, self_chunks);
+        // (uniform over the CTA) a chunk CTA of a batch of at most 32 x
+        // kWarpPlanPer requests plans per warp; the last CTA, and every CTA of a
+        // larger batch, in shared memory
+        const bool warp_plan = p.num_seqs <= 32 * kWarpPlanPer && blockIdx.x != gridDim.x - 1;
+        if (warp_plan)
+            n_items = decode_warp_plan(p, self_chunks, (gridDim.x - 1) * NW, blockIdx.x * NW + warp);
+        else
+            n_items = decode_self_plan<NW>(p, reinterpret_cast<int *>(smem), sp_shared, self_chunks);
         // the cache write before this kernel (and everything before it) is complete
         pdl_wait();
         if (blockIdx.x == gridDim.x - 1) {
@@ -413,7 +531,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
             pdl_trigger();
             return;                              // (no chunks of its own)
         }
-        __syncthreads();         // the plan's shared memory is the rings' from here on
+        if (!warp_plan) __syncthreads();         // the plan's shared memory is the rings' from here on
     } else {
         pdl_wait();       // the plan (and the cache write before it) are complete
     }
