@@ -136,7 +136,9 @@ int pkv_kv_write(void *kv_cache, int64_t num_blocks, int32_t num_kv_heads,
  *  out               bf16 [num_tokens][num_q_heads][head_size], contiguous, 16-byte aligned.
  *  query             bf16; token t, head h at query + t*query_token_stride + h*head_size;
  *                    16-byte aligned, stride a multiple of 8.
- *  kv_cache          bf16, layout above, 16-byte aligned; num_blocks in [1, 2^31).
+ *  kv_cache          bf16, layout above, 16-byte aligned; num_blocks in [1, 2^31) and
+ *                    num_blocks * num_kv_heads < 2^31 (PKV_ERR_SHAPE otherwise; such a
+ *                    cache is terabytes).
  *  block_tables      int32 [num_seqs][max_blocks_per_seq]; entries past
  *                    ceil(L_r/16) are never read.
  *  seq_lens          int32 [num_seqs].

@@ -587,6 +587,8 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     if (max_query_len > max_seq_len) return PKV_ERR_SHAPE;
     if (static_cast<int64_t>(max_blocks_per_seq) * kBlock < max_seq_len) return PKV_ERR_SHAPE;
     if (num_blocks < 1 || num_blocks > INT32_MAX) return PKV_ERR_SHAPE;
+    // the tile kernels address a page of one kv head as block id x kv heads + head in 32 bits
+    if (num_blocks * static_cast<int64_t>(num_kv_heads) > INT32_MAX) return PKV_ERR_SHAPE;
     if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return PKV_ERR_SHAPE;
     if (!(k_scale > 0.f) || !(v_scale > 0.f) || k_scale > 3.0e38f || v_scale > 3.0e38f) return PKV_ERR_SHAPE;
 

@@ -821,9 +821,8 @@ int launch_prefill_sk(const PrefillParams &p, const void *query, int64_t q_strid
                       const void *kv_cache, int64_t num_blocks, int32_t head_size, bool cascade, int64_t grid, int dev,
                       cudaStream_t stream) {
     if (grid <= 0) return PKV_OK;
-    // the kernel forms a page's coordinate block id x kv heads + head in 32 bits
-    // (a cache of 2^31 page-heads is terabytes, past any device's memory)
-    if (num_blocks * static_cast<int64_t>(p.num_kv_heads) > INT32_MAX) return PKV_ERR_SHAPE;
+    // (the kernel forms a page's coordinate block id x kv heads + head in 32 bits:
+    // the call's argument checks hold num_blocks x kv heads below 2^31)
     CUtensorMap kvm, qm;
     int rc = make_kv_tile_map(&kvm, kv_cache, num_blocks, p.num_kv_heads, head_size);
     if (rc) return rc;

@@ -94,6 +94,7 @@ def test_paged_attn_argument_errors_and_size_query(lib):
     assert _attn(lib, maxq=65)[0] == 2
     assert _attn(lib, out=None)[0] == 1
     assert _attn(lib, scale=float("nan"))[0] == 2
+    assert _attn(lib, nb=1 << 30, Hkv=2, H=4)[0] == 2   # blocks x kv heads past 2^31 - 1
     assert _attn(lib, ws=0x40000, wsb=need - 1)[0] == 5
     assert _attn(lib, ws=0x40010, wsb=need)[0] == 4     # workspace not 256-byte aligned
     assert _attn(lib, qstride=500, ws=0x40000, wsb=need)[0] == 2
