@@ -547,11 +547,13 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
         }
         set_status(status, code);
     };
-    const int4 *req = reinterpret_cast<const int4 *>(p.ws + (p.self_plan ? p.lay.off_req : hdr->off_req));
-    const int4 *chunks = reinterpret_cast<const int4 *>(p.ws + (p.self_plan ? p.lay.off_chunks : hdr->off_chunks));
-    float *part_lse = reinterpret_cast<float *>(p.ws + (p.self_plan ? p.lay.off_part_lse : hdr->off_part_lse));
-    float *part_o = reinterpret_cast<float *>(p.ws + (p.self_plan ? p.lay.off_part_o : hdr->off_part_o));
-    if (!p.self_plan) n_items = hdr->n_chunks * p.num_kv_heads;
+    // the plan's lists, read through L2 (the plan wrote them; the offsets are the
+    // layout the plan was given)
+    const int4 *req = reinterpret_cast<const int4 *>(p.ws + p.lay.off_req);
+    const int4 *chunks = reinterpret_cast<const int4 *>(p.ws + p.lay.off_chunks);
+    float *part_lse = reinterpret_cast<float *>(p.ws + p.lay.off_part_lse);
+    float *part_o = reinterpret_cast<float *>(p.ws + p.lay.off_part_o);
+    if (!p.self_plan) n_items = __ldcg(&hdr->n_chunks) * p.num_kv_heads;
 
     const int W = (p.self_plan ? gridDim.x - 1 : gridDim.x) * NW;   // (a self-planned call: not the last CTA)
     const int wid = blockIdx.x * NW + warp;
@@ -565,7 +567,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
         if (item >= n_items) continue;
         // (a self-planned call has at most two rounds)
         const SelfChunk sc = (round & 1) ? self_chunks[1] : self_chunks[0];
-        const int4 ch = p.self_plan ? make_int4(sc.r, sc.k, sc.pb, sc.pb + sc.npages) : chunks[item / p.num_kv_heads];
+        const int4 ch = p.self_plan ? make_int4(sc.r, sc.k, sc.pb, sc.pb + sc.npages) : __ldcg(chunks + item / p.num_kv_heads);
         const int g = item % p.num_kv_heads;
         const int r = ch.x;
         const int pb = ch.z;
@@ -578,7 +580,7 @@ __global__ void __launch_bounds__(NW * 32, DecodeTiling<HD, KV8>::CTAS_PER_SM)
         const bool split_mode = rows_total <= 16;
         const int tile = split_mode ? 0 : ch.y;
         const int split = split_mode ? ch.y : 0;
-        const int4 info = p.self_plan ? make_int4(sc.n_split, sc.pbase, 0, 0) : req[r];
+        const int4 info = p.self_plan ? make_int4(sc.n_split, sc.pbase, 0, 0) : __ldcg(req + r);
         const int n_split = split_mode ? info.x : 1;
         const int rows = min(16, rows_total - 16 * tile);
 
