@@ -655,7 +655,11 @@ static int paged_attn_impl(void *out, const void *query, int64_t query_token_str
     pp.prefix_blocks = prefix_blocks;
     pp.block_tables = block_tables;
     pp.lay = lay;
-    if (!self_plan && launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess)
+    // the plan's phases are chains of barriers and short loads: a batch of at
+    // most 256 requests without a shared prefix plans faster on 256 threads
+    // (the prefix comparison of every table with request 0's wants all of them)
+    const int plan_threads = (prefix_blocks == 0 && num_seqs <= 256) ? 256 : kPlanThreads;
+    if (!self_plan && launch_pdl(plan_kernel, dim3(1), dim3(plan_threads), 0, st, pp) != cudaSuccess)
         return PKV_ERR_CUDA;
 
     AttnParams ap;
