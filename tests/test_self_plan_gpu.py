@@ -2,8 +2,10 @@
 
 A small batch of split rows (every request's q_r * G <= 16, automatic splits,
 few enough (request, kv head) pairs and pages for the decode grid) runs with
-no plan kernel: every decode CTA plans the call in shared memory and the
-grid's last CTA writes the header and the split tokens for the combine.  A
+no plan kernel: with at most 64 requests every warp of a chunk CTA plans the
+call by itself in registers, with more every decode CTA plans it in shared
+memory, and the grid's last CTA writes the header and the split tokens for
+the combine.  A
 forced split count, a shared-prefix call or a large batch goes through the
 plan kernel instead.  Either way the rows must match the oracle; the status
 word must report a bad block id, bad lengths, and clear on the next clean call.
@@ -43,6 +45,8 @@ def test_the_same_batch_with_and_without_the_plan_kernel(num_splits):
     (1, 8, 8, 128, 1),       # one request: a grid of one chunk CTA and the header CTA
     (3, 32, 8, 128, 2),      # two query tokens per row group (G = 4, 8 rows)
     (16, 40, 40, 128, 1),    # MHA
+    (64, 8, 2, 64, 1),       # the most requests every warp plans by itself (two per lane)
+    (65, 8, 2, 64, 1),       # one more: the chunk CTAs plan in shared memory
     (300, 8, 2, 64, 1),
     (1100, 8, 2, 64, 1),     # more requests than the decode kernel plans itself: the plan kernel
 ])
