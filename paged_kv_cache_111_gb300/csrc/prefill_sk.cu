@@ -181,18 +181,21 @@ __global__ void __launch_bounds__(kSKThreads, 1)
     const int G = p.G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // one barrier per thread: an mbarrier.init takes over a hundred cycles, and
+    // one thread initialising all of them in turn held every CTA ~2.5 us
+    if (threadIdx.x < kSKNumBars) {
+        const int b = threadIdx.x;
+        int count = 1;
+        if (b >= kSKPFull && b < kSKPFull + 4) count = 4;            // the key half's softmax warps
+        else if (b == kSKOFree) count = 8;                            // every softmax warp
+        else if (b >= kSKXchg && b < kSKXchg + 4) count = 2;         // the two warps of a quadrant
+        else if (b >= kSKQEmpty && b < kSKQEmpty + 2) count = 2;     // both MMA threads
+        else if (b >= kSKKVEmpty && b < kSKKVEmpty + 4) count = 2;   // both MMA threads
+        else if (b >= kSKItemEmpty && b < kSKItemEmpty + kItemSlots)
+            count = CASCADE ? 11 : 10;             // 2 MMA threads, 8 softmax warps (+ the Q gatherer)
+        mbar_init(&bars[b], count);
+    }
     if (threadIdx.x == 0) {
-        for (int b = 0; b < kSKNumBars; ++b) {
-            int count = 1;
-            if (b >= kSKPFull && b < kSKPFull + 4) count = 4;            // the key half's softmax warps
-            else if (b == kSKOFree) count = 8;                            // every softmax warp
-            else if (b >= kSKXchg && b < kSKXchg + 4) count = 2;         // the two warps of a quadrant
-            else if (b >= kSKQEmpty && b < kSKQEmpty + 2) count = 2;     // both MMA threads
-            else if (b >= kSKKVEmpty && b < kSKKVEmpty + 4) count = 2;   // both MMA threads
-            else if (b >= kSKItemEmpty && b < kSKItemEmpty + kItemSlots)
-                count = CASCADE ? 11 : 10;             // 2 MMA threads, 8 softmax warps (+ the Q gatherer)
-            mbar_init(&bars[b], count);
-        }
         tma_prefetch_desc(&kv_map);
         if (!CASCADE) tma_prefetch_desc(&q_map);
     }

@@ -124,20 +124,21 @@ __global__ void __launch_bounds__(448, 1)
     const int G = p.G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
-        for (int b = 0; b < kNumBars; ++b) {
-            int count = 1;
-            if (b == kPFull0 || b == kPFull1 || b == kQFull || b == kOFree) count = 8;
-            else if (b >= kXchg0 && b <= kXchg3) count = 2;
-            else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = 13;   // MMA, softmax, converters
-            else if (b == kREmpty0 || b == kREmpty1) count = 4;      // every converter warp
-            else if ((b == kKFull0 || b == kKFull1 || b == kKFull2 || b == kVFull0 || b == kVFull1 ||
-                             b == kVFull2 || b == kVFix0 || b == kVFix1 || b == kVFix2))
-                count = 2;                                           // the two converters of K (of V)
-            mbar_init(&bars[b], count);
-        }
-        tma_prefetch_desc(&kv_map);
+    // one barrier per thread: an mbarrier.init takes over a hundred cycles, and
+    // one thread initialising all of them in turn held every CTA several us
+    if (threadIdx.x < kNumBars) {
+        const int b = threadIdx.x;
+        int count = 1;
+        if (b == kPFull0 || b == kPFull1 || b == kQFull || b == kOFree) count = 8;
+        else if (b >= kXchg0 && b <= kXchg3) count = 2;
+        else if (b >= kItemEmpty0 && b < kItemEmpty0 + kItemSlots) count = 13;   // MMA, softmax, converters
+        else if (b == kREmpty0 || b == kREmpty1) count = 4;      // every converter warp
+        else if ((b == kKFull0 || b == kKFull1 || b == kKFull2 || b == kVFull0 || b == kVFull1 ||
+                         b == kVFull2 || b == kVFix0 || b == kVFix1 || b == kVFix2))
+            count = 2;                                           // the two converters of K (of V)
+        mbar_init(&bars[b], count);
     }
+    if (threadIdx.x == 0) tma_prefetch_desc(&kv_map);
     if (warp == 2) {
         tmem_alloc(tmem_slot, Cfg::kTmemCols);
         tmem_relinquish();
