@@ -54,19 +54,19 @@ TRAFFIC = {
     # call, ncu with its default cache flush) / the call's algorithmic bytes.
     # Writes that stay in L2 until after the kernel do not count, so a call
     # whose output is large (a prefill chunk) reads below 1.
-    "bf16 decode": {"sources_sha256_16": "8bdcddf416d4e414", "ratio": 1045.0129e6 / 1033884588,
+    "bf16 decode": {"sources_sha256_16": "f1eb5d212e731fb2", "ratio": 1045.1558e6 / 1033884588,
                     "source": "ncu DRAM counters of plan + decode on llama13b-decode, first 64 requests"},
-    "e4m3 decode": {"sources_sha256_16": "8bdcddf416d4e414", "ratio": 524.2429e6 / 517604268,
+    "e4m3 decode": {"sources_sha256_16": "f1eb5d212e731fb2", "ratio": 524.2228e6 / 517604268,
                     "source": "ncu DRAM counters of plan + decode on llama13b-decode, first 64 requests, E4M3"},
-    "bf16 cascade": {"sources_sha256_16": "8bdcddf416d4e414", "ratio": 29.4992e6 / 28294800,
+    "bf16 cascade": {"sources_sha256_16": "f1eb5d212e731fb2", "ratio": 29.5035e6 / 28294800,
                      "source": "ncu DRAM counters of plan + decode + shared-prefix pass on llama3-70b-prefix, "
                                "first 24 requests"},
-    "e4m3 cascade": {"sources_sha256_16": "8bdcddf416d4e414", "ratio": 15.2621e6 / 14544528,
+    "e4m3 cascade": {"sources_sha256_16": "f1eb5d212e731fb2", "ratio": 15.2649e6 / 14544528,
                      "source": "ncu DRAM counters of plan + decode + shared-prefix pass on llama3-70b-prefix, "
                                "first 24 requests, E4M3"},
-    "bf16 prefill": {"sources_sha256_16": "8bdcddf416d4e414", "ratio": 34.4002e6 / 50947140,
+    "bf16 prefill": {"sources_sha256_16": "f1eb5d212e731fb2", "ratio": 34.3981e6 / 50947140,
                      "source": "ncu DRAM counters of plan + decode + prefill on llama3-8b-mixed"},
-    "e4m3 prefill": {"sources_sha256_16": "8bdcddf416d4e414", "ratio": 25.7065e6 / 42251332,
+    "e4m3 prefill": {"sources_sha256_16": "f1eb5d212e731fb2", "ratio": 25.7139e6 / 42251332,
                      "source": "ncu DRAM counters of plan + decode + prefill on llama3-8b-mixed, E4M3"},
 }
 
